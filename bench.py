@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Throughput of one dropless MoE layer step (forward + backward) on GB300.
+
+A step is the whole hot path on one batch: route -> permute -> grouped GEMM
+gate/up (+SwiGLU*w) -> grouped GEMM down -> combine -> combine backward ->
+grouped-GEMM backward (4 GEMMs) -> un-permute -> route backward.
+
+Default workload: the Mixtral-8x7B-shaped layer (T=8192 tokens, d=4096, f=14336,
+E=8, top-2, softmax routing with a N(0,0.5) per-expert bias), bf16 operands with
+fp32 accumulation.  Inputs are synthetic (seeded) and resident in HBM; the 2.8 GB
+of weights exceed the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
+
+--impl reference times the CPU oracle (the plain NumPy implementation the tests
+compare against) on the host cores, on a bounded token sample of the same
+workload per step.  Under torchrun, rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd TFLOPS & tokens/s on 1 GB300; % of bf16/MXFP8 tensor peak"
+UNIT = "TFLOP/s"
+GEMMS = ["gate_up", "down", "down_dgrad", "down_wgrad", "gate_up_dgrad", "gate_up_wgrad"]
+GEMM_FLOP_FACTOR = {"gate_up": 4, "down": 2, "down_dgrad": 2, "down_wgrad": 2, "gate_up_dgrad": 4,
+                    "gate_up_wgrad": 4}   # x R*d*f
+GEMM_KERNEL = {"gate_up": "grouped_gemm_kernel<0,1,0,0>", "down": "grouped_gemm_kernel<0,0,0,0>",
+               "down_dgrad": "grouped_gemm_kernel<0,2,0,1> + dw_reduce_kernel",
+               "down_wgrad": "grouped_gemm_kernel<1,0,1,1>", "gate_up_dgrad": "grouped_gemm_kernel<0,0,0,1>",
+               "gate_up_wgrad": "grouped_gemm_kernel<1,0,1,1>"}
+
+
+def workload_name(cfg) -> str:
+    names = {"tiny": "tiny MoE layer", "mixtral": "Mixtral-8x7B-shaped MoE layer",
+             "qwen30b": "Qwen3-30B-A3B-shaped MoE layer", "qwen235b": "Qwen3-235B-A22B-shaped MoE layer",
+             "qwen235b-zipf": "Qwen3-235B-A22B-shaped MoE layer (Zipf routing)",
+             "dsv3": "DeepSeek-V3-shaped routed-expert layer"}
+    return names.get(cfg.name, cfg.name) + " fwd+bwd"
+
+
+def config_json(cfg, prec="bf16"):
+    bias = {"normal": f"N(0,{cfg.bias_param})", "zipf": f"Zipf(s={cfg.bias_param})", "zero": "0"}[cfg.bias]
+    return {"workload": workload_name(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
+            "f_shared": cfg.f_shared, "routing": f"{cfg.score} top-{cfg.k}, router bias {bias}",
+            "precision": prec, "l2": "inputs larger than L2 (weights alone exceed 129 MB)",
+            "parallelism": "replicas"}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dropless_mixture_experts_warp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel_key: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernels have not changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key and parts[2] == cur:
+            return float(parts[1])
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return json.load(open(path)), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.lower().replace("gpu-", "")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        mine = [r for r in rows if self.uuid and self.uuid in r[0].lower()] or rows
+        if not mine:
+            return None
+        sm = [float(r[1]) for r in mine if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in mine if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in mine for i in range(4) if r[4 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(mine)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: float, chunk: int, seed=0):
+    """Run the CPU oracle (fp32) on random token chunks for about `seconds`; returns FLOP/s and tokens."""
+    import numpy as np
+    from oracle import moe_oracle as om
+    from dropless_mixture_experts_warp_gb300 import synth
+    rng = np.random.default_rng(seed)
+    done_tok, t_total = 0, 0.0
+    while t_total < seconds or done_tok == 0:
+        sub = np.sort(rng.choice(x_bits.shape[0], size=chunk, replace=False))
+        x = synth.bf16_to_f32(x_bits[sub])
+        dy = synth.bf16_to_f32(dy_bits[sub])
+        lg = logits[sub]
+        t0 = time.perf_counter()
+        fwd = om.moe_forward(x, lg, w_gu32, w_d32, cfg.k, cfg.score, dtype=np.float32)
+        om.moe_backward(x, lg, w_gu32, w_d32, dy, fwd, cfg.k, cfg.score, dtype=np.float32)
+        t_total += time.perf_counter() - t0
+        done_tok += chunk
+    flops = 18.0 * done_tok * cfg.k * cfg.d * cfg.f
+    return flops / t_total, done_tok, t_total
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle, timed per step on a bounded token sample."""
+    import numpy as np
+    from dropless_mixture_experts_warp_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = synth.token_inputs(cfg)
+    w_gu_b, w_d_b = synth.all_expert_weights(cfg)
+    w_gu32 = synth.bf16_to_f32(w_gu_b).reshape(w_gu_b.shape)
+    w_d32 = synth.bf16_to_f32(w_d_b).reshape(w_d_b.shape)
+    del w_gu_b, w_d_b
+    chunk = max(1, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk)
+    times, tok = [], 0
+    for s in range(args.steps):
+        rate, n, t = oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk, seed=s + 1)
+        times.append(t)
+        tok += n
+    total = sum(times)
+    flops = 18.0 * tok * cfg.k * cfg.d * cfg.f
+    value = flops / total / 1e12
+    ms = total / args.steps * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_json(cfg, "fp32 oracle"),
+            "tokens_per_s": tok / total,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{chunk} random tokens of the {cfg.T}-token batch per step (fp32 NumPy)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- native
+
+def run_native(args, cfg):
+    import numpy as np
+    import torch
+    from dropless_mixture_experts_warp_gb300 import binding as B, build, layer, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    B.lib()
+
+    dev = torch.device("cuda", local)
+    inp = synth.torch_inputs(cfg, dev, seed=cfg.seed + 7919 * rank)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
+    bufs = layer.allocate(dims, dev)
+    stream = torch.cuda.current_stream(dev)
+    x, logits, dy, w_gu, w_d = inp["x"], inp["logits"], inp["dy"], inp["w_gu"], inp["w_d"]
+    R = cfg.T * cfg.k
+    unit = R * cfg.d * cfg.f
+
+    def step(ev=None):
+        b, dm = bufs, dims
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
+                         b.workspace, b.status, stream)
+        B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
+                      b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
+        mark(0)
+        B.moe_gemm_gate_up(dm, b.xp, b.row_offsets, b.w_rows, w_gu, b.gu, b.h, b.status, stream)
+        mark(1)
+        B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
+        mark(2)
+        B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, None, b.y, stream)
+        B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
+        mark(3)
+        B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
+                              b.workspace, b.status, stream)
+        mark(4)
+        B.moe_gemm_down_wgrad(dm, b.dy_rows, b.h, b.row_offsets, b.dw_d, b.status, stream)
+        mark(5)
+        B.moe_gemm_gate_up_dgrad(dm, b.dgu, b.row_offsets, w_gu, b.dxp, b.status, stream)
+        mark(6)
+        B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
+        mark(7)
+        B.moe_combine_fwd(dm, b.dxp, b.token_to_row, None, b.dx, stream)
+        B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
+
+    for _ in range(args.warmup):
+        step()
+    layer.check(bufs, stream)
+
+    uuid = ""
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = B.moe_launch_count()
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    launches = B.moe_launch_count() - launches0
+    if dist:
+        dist.barrier()
+    layer.check(bufs, stream)
+    ms = start.elapsed_time(end) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    gemm_ms = {g: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+               for i, g in enumerate(GEMMS)}
+
+    # end to end through the same calls with host buffers: H2D of this step's inputs,
+    # D2H of its results (Y, dX, d_logits), inside the timed region
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
+    lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True).copy_(logits)
+    dy_h = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True).copy_(dy)
+    y_h = torch.empty(bufs.y.shape, dtype=bufs.y.dtype, pin_memory=True)
+    dx_h = torch.empty(bufs.dx.shape, dtype=bufs.dx.dtype, pin_memory=True)
+    dl_h = torch.empty(bufs.d_logits.shape, dtype=bufs.d_logits.dtype, pin_memory=True)
+    h2d = x_h.nbytes + lg_h.nbytes + dy_h.nbytes
+    d2h = y_h.nbytes + dx_h.nbytes + dl_h.nbytes
+    e2e_steps = max(1, min(args.steps, 10))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_h, non_blocking=True)
+        logits.copy_(lg_h, non_blocking=True)
+        dy.copy_(dy_h, non_blocking=True)
+        step()
+        y_h.copy_(bufs.y, non_blocking=True)
+        dx_h.copy_(bufs.dx, non_blocking=True)
+        dl_h.copy_(bufs.d_logits, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = start.elapsed_time(end) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    layer.check(bufs, stream)
+
+    peaks, peak_src = measured_peaks()
+    flops = cfg.flops_fwd_bwd()
+    value = world * flops / (ms * 1e-3) / 1e12
+    dom = max(GEMMS, key=lambda g: gemm_ms[g])
+    dom_flops = GEMM_FLOP_FACTOR[dom] * unit
+    achieved = dom_flops / (gemm_ms[dom] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = read_traffic(dom)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_json(cfg),
+        "tokens_per_s": world * cfg.T / (ms * 1e-3),
+        "frac_of_bf16_peak": value / world / peak,
+        "roofline": {"bound": "tensor", "kernel": f"{dom} ({GEMM_KERNEL[dom]})", "achieved": achieved,
+                     "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (timed inside a long step)",
+                     "flops_per_launch": dom_flops, "ms_per_launch": gemm_ms[dom]},
+        "gemm_ms": {g: round(v, 4) for g, v in gemm_ms.items()},
+        "gemm_tflops": {g: GEMM_FLOP_FACTOR[g] * unit / (gemm_ms[g] * 1e-3) / 1e12 for g in GEMMS},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle as it stands, on this host's cores, on a bounded random token sample
+        ex = {"x": x.view(torch.int16).cpu().numpy().view(np.uint16),
+              "dy": dy.view(torch.int16).cpu().numpy().view(np.uint16), "logits": logits.cpu().numpy()}
+        w_gu32 = w_gu.float().cpu().numpy()
+        w_d32 = w_d.float().cpu().numpy()
+        rate, ntok, secs = oracle_sample_rate(cfg, ex["x"], ex["logits"], ex["dy"], w_gu32, w_d32,
+                                              args.cpu_seconds, args.ref_tokens)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{ntok} random tokens of the {cfg.T}-token batch, fp32 NumPy, "
+                                          f"{secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from dropless_mixture_experts_warp_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_native(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,375 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage ring
+//   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator;
+//               owns the TMEM allocation (two accumulators of 256 fp32 columns)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU / SwiGLU'
+//               arithmetic, bf16 stores.  Warp w reads TMEM lanes 32*(w%4)..+31.
+// The two accumulators let the epilogue of one tile overlap the mainloop of the
+// next.  Work tiles come from a device-side schedule derived from row_offsets, so
+// the host never waits for the per-expert counts.
+//
+// Scheduling modes
+//   SCHED_ROWS    ragged M: expert e owns output rows [row_offsets[e], row_offsets[e+1]),
+//                 a multiple of 128, and multiplies them by its own weight B[e]
+//                 (grouped GEMM of the forward and of the data-gradient backward).
+//   SCHED_KGROUP  ragged K: out[e] = A_e^T B_e summed over the rows of expert e
+//                 (weight gradients); an expert without rows gets zeros.
+// Operand majorness: K-major tiles come straight from row-major [rows][K] tensors;
+// MN-major tiles (A or B stored [K][MN]) use the transpose bits of the instruction
+// descriptor, so no operand is ever transposed in memory.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_STAGE_BYTES_MAX = 256 * BK * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES_MAX;
+constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int TMEM_COLS = 512;
+constexpr int ACC_STRIDE = 256;
+constexpr int GEMM_THREADS = 192;
+constexpr int MAX_EXPERTS = 1024;
+constexpr long long WAIT_LIMIT_CYCLES = 1ll << 31;  // about one second
+
+enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+enum Sched { SCHED_ROWS = 0, SCHED_KGROUP = 1 };
+
+struct GemmParams {
+  int BN;                       // accumulator width: 64, 128 or 256
+  int N;                        // output columns (SWIGLU_FWD: h columns = f)
+  int K;                        // contraction length (SCHED_ROWS)
+  int M;                        // SCHED_KGROUP: output rows per expert; dense mode: rows
+  int E;                        // groups
+  const int32_t* row_offsets;   // [E+1] padded row offsets; NULL = one group of M rows
+  int b_rows_per_expert;        // B K-major: rows of the B tensor per expert
+  int b_k_per_expert;           // B MN-major (SCHED_ROWS): K rows per expert
+  int m_fastest;                // tile order inside a group: 1 = M fastest
+  int f;                        // SwiGLU epilogues: intermediate width (offset of U)
+  moe_bf16* out;                // EPI_STORE output
+  long long ldo;                // its leading dimension (elements)
+  long long row_limit;          // rows >= row_limit are not stored
+  const float* w_rows;          // routing weight per row (SwiGLU epilogues)
+  moe_bf16* gu_out;             // SWIGLU_FWD: saved G|U [rows][2f]
+  moe_bf16* h_out;              // SWIGLU_FWD: h [rows][f]
+  const moe_bf16* gu_in;        // SWIGLU_BWD: saved G|U
+  moe_bf16* dgu_out;            // SWIGLU_BWD: dG|dU [rows][2f]
+  float* dw_part;               // SWIGLU_BWD: per-row partial of dw, one per N tile
+  int dw_stride;                // its row stride (= number of N tiles)
+  int32_t* status;              // device status word
+};
+
+struct TileCoord {
+  int e, m, n, kblocks;
+  int a_m, a_k;       // A: first row (K-major) / first column (MN-major), first K index
+  int b_n, b_k;       // B: first N index (row for K-major, column for MN-major), first K index
+  long long out_row;  // first output row of the tile
+  int out_col;        // first output column
+  long long out_base; // element offset of the group's output (SCHED_KGROUP)
+};
+
+template <int SCHED, int EPI, bool B_MN>
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* s_ro, int E,
+                                                int n_tiles, int tile) {
+  TileCoord c;
+  if (SCHED == SCHED_ROWS) {
+    int lo = 0, hi = E - 1;  // last expert whose first tile is <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((s_ro[mid] / BM) * n_tiles <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int local = tile - (s_ro[e] / BM) * n_tiles;
+    const int mt = (s_ro[e + 1] - s_ro[e]) / BM;
+    if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
+    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    c.e = e;
+    c.kblocks = p.K / BK;
+    c.a_m = s_ro[e] + c.m * BM;
+    c.a_k = 0;
+    c.out_col = (EPI == EPI_SWIGLU_FWD) ? c.n * (p.BN / 2) : c.n * p.BN;
+    c.b_n = B_MN ? c.out_col : e * p.b_rows_per_expert + c.out_col;
+    c.b_k = B_MN ? e * p.b_k_per_expert : 0;
+    c.out_row = c.a_m;
+    c.out_base = 0;
+  } else {
+    const int mt = p.M / BM;
+    const int per = mt * n_tiles;
+    const int e = tile / per;
+    const int local = tile - e * per;
+    if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
+    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    c.e = e;
+    c.kblocks = (s_ro[e + 1] - s_ro[e]) / BK;
+    c.a_m = c.m * BM;
+    c.a_k = s_ro[e];
+    c.b_n = c.n * p.BN;
+    c.b_k = s_ro[e];
+    c.out_row = c.m * BM;
+    c.out_col = c.n * p.BN;
+    c.out_base = static_cast<long long>(e) * p.M * p.N;
+  }
+  return c;
+}
+
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
+
+template <int SCHED, int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_ro[MAX_EXPERTS + 1];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int E = p.row_offsets ? p.E : 1;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x)
+    s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : (p.M + BM - 1) / BM * BM);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 4); }
+    mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 1) { tmem_alloc(&s_tmem_base, TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+
+  const int BN = p.BN;
+  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t stage_tx = A_STAGE_BYTES + BN * BK * 2;
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          uint64_t* bar = &full_bar[stage];
+          mbar_arrive_expect_tx(bar, stage_tx);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          const int k0 = kb * BK;
+          if (!A_MN) {
+            tma_load_2d(sa, &tmA, bar, c.a_k + k0, c.a_m);
+          } else {
+            tma_load_2d(sa, &tmA, bar, c.a_m, c.a_k + k0);
+            tma_load_2d(sa + 8192, &tmA, bar, c.a_m + 64, c.a_k + k0);
+          }
+          if (!B_MN) {
+            if (EPI == EPI_SWIGLU_FWD) {
+              tma_load_2d(sb, &tmB, bar, k0, c.b_n);
+              tma_load_2d(sb + (BN / 2) * 128, &tmB, bar, k0, c.b_n + p.f);
+            } else {
+              tma_load_2d(sb, &tmB, bar, c.b_k + k0, c.b_n);
+            }
+          } else {
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * 8192, &tmB, bar, c.b_n + 64 * i, c.b_k + k0);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // No bulk copy may still be writing shared memory when the CTA exits.
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_drain(&full_bar[s], (armed_parity >> s) & 1u, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+        if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status,
+                               WAIT_LIMIT_CYCLES)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // K-major: the next 16 elements are 32 bytes further along the swizzled row.
+            // MN-major: the next 16 K rows are 16 * 128 bytes further; MN atoms of 64
+            // elements repeat every 8 KB (one TMA box), 8-row K groups every 1 KB.
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);      // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      // Every MMA must be finished before TMEM is released.
+      tc_commit(&drain_bar);
+      mbar_drain(&drain_bar, 0, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES))
+        break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+      const long long row = c.out_row + row_in_tile;
+      const bool row_ok = row < p.row_limit;
+
+      if (EPI == EPI_STORE) {
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          if (c.kblocks > 0) {
+            tmem_ld32(tbase + c0, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + c.out_base + row * p.ldo + c.out_col + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+              o.y = pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+              o.z = pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+              o.w = pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              dst[v] = o;
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_FWD) {
+        // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2
+        const int half = BN / 2;
+        const float w = row_ok ? p.w_rows[row] : 0.0f;
+        const long long ld2 = 2ll * p.f;
+        for (int c0 = 0; c0 < half; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c0, g);
+          tmem_ld32(tbase + half + c0, u);
+          tmem_wait_ld();
+          if (row_ok) {
+            uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + c.out_col + c0);
+            uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + c.out_col + c0);
+            uint4* hdst = reinterpret_cast<uint4*>(p.h_out + row * p.f + c.out_col + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float hv[8], gv[8], uv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                gv[i] = __uint_as_float(g[8 * v + i]);
+                uv[i] = __uint_as_float(u[8 * v + i]);
+                hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
+              }
+              gdst[v] = make_uint4(pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
+                                   pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
+              udst[v] = make_uint4(pack_bf16(uv[0], uv[1]), pack_bf16(uv[2], uv[3]),
+                                   pack_bf16(uv[4], uv[5]), pack_bf16(uv[6], uv[7]));
+              hdst[v] = make_uint4(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
+                                   pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
+            }
+          }
+        }
+      } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN
+        const float w = row_ok ? p.w_rows[row] : 0.0f;
+        const long long ld2 = 2ll * p.f;
+        float dwp = 0.0f;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_wait_ld();
+          if (row_ok) {
+            const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
+            const uint4* usrc =
+                reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
+            uint4* gdst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + c.out_col + c0);
+            uint4* udst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + p.f + c.out_col + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 g4 = gsrc[v], u4 = usrc[v];
+              const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+              const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+              float dg[8], du[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+                const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
+                const float dh = __uint_as_float(r[8 * v + i]);
+                const float sg = sigmoidf_(g);
+                const float silu = g * sg;
+                const float da = w * dh;
+                dwp += silu * u * dh;
+                dg[i] = da * u * sg * (1.0f + g * (1.0f - sg));
+                du[i] = da * silu;
+              }
+              gdst[v] = make_uint4(pack_bf16(dg[0], dg[1]), pack_bf16(dg[2], dg[3]),
+                                   pack_bf16(dg[4], dg[5]), pack_bf16(dg[6], dg[7]));
+              udst[v] = make_uint4(pack_bf16(du[0], du[1]), pack_bf16(du[2], du[3]),
+                                   pack_bf16(du[4], du[5]), pack_bf16(du[6], du[7]));
+            }
+          }
+        }
+        if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace moe

@@ -1,0 +1,74 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+#include "gemm.cuh"
+
+namespace moe {
+
+constexpr int ROUTE_TOKENS = 256;  // tokens per routing block
+constexpr int ROW_ALIGN = MOE_ROW_ALIGN;
+
+inline int route_blocks(int T) { return T > 0 ? (T + ROUTE_TOKENS - 1) / ROUTE_TOKENS : 1; }
+
+// Scratch of moe_route_topk that moe_permute reads back.
+struct RouteScratch {
+  int32_t* counter;     // 1 int, reset by the call
+  int32_t* block_hist;  // [blocks][E] tokens of each routing block per expert
+  int32_t* block_base;  // [blocks][E] rows of expert e taken by earlier blocks
+  int32_t* local_rank;  // [T][k] rank of (t, j) among the block's tokens of its expert
+};
+
+void count_launch();
+int num_sms();
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int score, int32_t* topk_idx,
+                              float* topk_w, int32_t* split_sizes, int32_t* offsets,
+                              int32_t* row_offsets, const RouteScratch& ws, int32_t* status,
+                              cudaStream_t stream);
+cudaError_t launch_permute(const void* x, int T, int d, int E, int k, const int32_t* topk_idx,
+                           const float* topk_w, const int32_t* split_sizes, const int32_t* row_offsets,
+                           const RouteScratch& ws, void* xp, int32_t* row_to_token,
+                           int32_t* token_to_row, float* w_rows, int rows_cap, int32_t* status,
+                           cudaStream_t stream);
+cudaError_t launch_combine_bwd(const void* dy, int T, int d, int E, int k, const int32_t* token_to_row,
+                               const int32_t* split_sizes, const int32_t* row_offsets, void* dy_rows,
+                               int rows_cap, cudaStream_t stream);
+cudaError_t launch_combine(const void* rows, int T, int d, int k, const int32_t* token_to_row,
+                           const void* shared, void* out, int rows_cap, cudaStream_t stream);
+cudaError_t launch_dw_reduce(const float* part, int stride, const int32_t* row_offsets, int E,
+                             float* dw_rows, int max_rows, cudaStream_t stream);
+cudaError_t launch_route_bwd(const float* logits, int T, int E, int k, int score,
+                             const int32_t* topk_idx, const float* topk_w, const float* dw_rows,
+                             const int32_t* token_to_row, float* d_logits, int rows_cap,
+                             cudaStream_t stream);
+
+// Grouped-GEMM variants (scheduling, epilogue, A/B majorness).
+enum GemmKind {
+  GEMM_ROWS_SWIGLU_FWD = 0,  // ragged rows, K-major A and B, SwiGLU*w epilogue
+  GEMM_ROWS_STORE = 1,       // ragged rows (or dense), K-major A and B
+  GEMM_ROWS_STORE_BMN = 2,   // ragged rows (or dense), K-major A, MN-major B
+  GEMM_ROWS_SWIGLU_BWD = 3,  // ragged rows, K-major A, MN-major B, SwiGLU' epilogue
+  GEMM_KGROUP_STORE = 4,     // ragged K (weight gradients), MN-major A and B
+  GEMM_DENSE_AMN_BK = 5,     // dense, MN-major A, K-major B (test hook)
+  GEMM_DENSE_AMN_BMN = 6     // dense, MN-major A and B (test hook)
+};
+
+cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, cudaStream_t stream);
+
+template <int SCHED, int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                          cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<SCHED, EPI, A_MN, B_MN>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms(), GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(a, b, p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,96 @@
+"""One dropless MoE layer step through the C ABI: buffers and the call sequence.
+
+PyTorch only allocates device memory and provides the stream; every step runs in
+libmoe.so's kernels.  Forward: route -> permute -> grouped MLP -> combine.
+Backward: combine_bwd -> grouped MLP backward -> un-permute (combine of dXp) ->
+route backward.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding as B
+
+
+@dataclass
+class Buffers:
+    dims: B.moe_dims
+    rows: int
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    split_sizes: torch.Tensor
+    offsets: torch.Tensor
+    row_offsets: torch.Tensor
+    xp: torch.Tensor
+    row_to_token: torch.Tensor
+    token_to_row: torch.Tensor
+    w_rows: torch.Tensor
+    gu: torch.Tensor
+    h: torch.Tensor
+    y_rows: torch.Tensor
+    y: torch.Tensor
+    dy_rows: torch.Tensor
+    dgu: torch.Tensor
+    dxp: torch.Tensor
+    dw_gu: torch.Tensor
+    dw_d: torch.Tensor
+    dw_rows: torch.Tensor
+    dx: torch.Tensor
+    d_logits: torch.Tensor
+    workspace: torch.Tensor
+    status: torch.Tensor
+
+
+def dims_of(T, d, f, E, k, f_shared=0, score="softmax", prec="bf16") -> B.moe_dims:
+    dims = B.make_dims(T, d, f, E, k, f_shared, score, prec)
+    st = B.moe_check_dims(dims)
+    if st != B.MOE_OK:
+        raise B.MoeError("moe_check_dims", st)
+    return dims
+
+
+def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
+    T, d, f, E, k = dims.T, dims.d, dims.f, dims.E, dims.k
+    rows = B.moe_row_capacity(dims)
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
+    return Buffers(
+        dims=dims, rows=rows,
+        topk_idx=e(T, k, dt=i32), topk_w=e(T, k, dt=f32), split_sizes=e(E, dt=i32),
+        offsets=e(E + 1, dt=i32), row_offsets=e(E + 1, dt=i32),
+        xp=e(rows, d), row_to_token=e(rows, dt=i32), token_to_row=e(T, k, dt=i32), w_rows=e(rows, dt=f32),
+        gu=e(rows, 2 * f), h=e(rows, f), y_rows=e(rows, d), y=e(T, d),
+        dy_rows=e(rows, d), dgu=e(rows, 2 * f), dxp=e(rows, d),
+        dw_gu=e(E, 2 * f, d), dw_d=e(E, d, f), dw_rows=e(rows, dt=f32), dx=e(T, d), d_logits=e(T, E, dt=f32),
+        workspace=torch.empty(max(1, B.moe_workspace_size(dims)), dtype=torch.uint8, device=device),
+        status=torch.zeros(1, dtype=i32, device=device),
+    )
+
+
+def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, shared_out=None):
+    dm = b.dims
+    B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
+                     b.workspace, b.status, stream)
+    B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
+                  b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
+    B.moe_grouped_mlp_fwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.y_rows, b.status, stream)
+    B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, shared_out, b.y, stream)
+    return b.y
+
+
+def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, shared_dx=None):
+    dm = b.dims
+    B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
+    B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu, b.dxp,
+                          b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)
+    B.moe_combine_fwd(dm, b.dxp, b.token_to_row, shared_dx, b.dx, stream)
+    B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
+    return b.dx
+
+
+def check(b: Buffers, stream=None):
+    st = B.moe_check_status(b.status, stream)
+    if st != B.MOE_OK:
+        raise B.MoeError("device status", st)

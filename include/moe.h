@@ -1,0 +1,273 @@
+/*
+ * Dropless mixture-of-experts layer, forward and backward, on one GB300 (sm_103a).
+ *
+ * C ABI of libmoe.so.  Plain pointers and sizes only.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Ownership: every pointer argument is caller-owned memory; the library keeps
+ *    no pointer after a call returns and allocates no device memory.  Pointers
+ *    named like tensors are DEVICE pointers; `dims` is a HOST pointer.
+ *  - Execution: work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream) and runs asynchronously; no call synchronises the host except
+ *    moe_check_status.
+ *  - Errors: argument problems are found on the host and returned synchronously
+ *    (nothing is enqueued then).  Problems found while kernels run (a broken
+ *    invariant, a pipeline wait that gave up) are written to the caller's
+ *    `dev_status` word (int32, device memory, must start at 0; the first error
+ *    sticks) and are read back by moe_check_status.  No kernel traps.
+ *  - Layouts are row-major.  bf16 tensors are passed as moe_bf16 bit patterns.
+ *    Weights follow the [out, in] convention: W_gu[E][2f][d] holds the gate rows
+ *    [0,f) then the up rows [f,2f) of every expert; W_d[E][d][f].
+ *  - Routed rows live in a padded, expert-contiguous row space of
+ *    moe_row_capacity() rows: expert e owns rows [row_offsets[e], row_offsets[e+1]),
+ *    row_offsets[e] being a multiple of MOE_ROW_ALIGN; its first split_sizes[e]
+ *    rows hold its tokens (in token order) and the rest are padding rows that the
+ *    library fills with zeros where they are read.
+ *  - Alignment: all device pointers 16-byte aligned; d a multiple of 128 and f a
+ *    multiple of 64 (tensor-memory tiles; 32-element MX blocks); 1 <= k <= min(E,32);
+ *    E <= 1024; T >= 0.
+ *
+ * Sources (web pages describing the method; quoted by title and section):
+ *  [DROPLESS] NVIDIA dropless MoE in JAX: "Az NVIDIA szerint tízszer gyorsabb lett a
+ *             dropless MoE tanítása JAX-ban".
+ *  [BIO]      NVIDIA MoE training for biology models: "NVIDIA מציגה דרך יעילה לאמן
+ *             מודלי MoE בביולוגיה".
+ *  [MEGA]     DeepGEMM Mega MoE article (itsolotime.com, Thai).
+ *  [PRIME]    "Prime Mega MoE: tanításra is jó a DeepSeek MoE kernele".
+ */
+#ifndef DROPLESS_MOE_H
+#define DROPLESS_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* bfloat16 bit pattern */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad size, NULL pointer, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but not supported (d % 128, f % 64, E > 1024, ...) */
+  MOE_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 4,   /* workspace NULL while needed */
+  MOE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 6,     /* a bounded device wait gave up (written to dev_status) */
+  MOE_ERR_INVARIANT = 7    /* sum(split_sizes) != T*k seen on the device */
+} moe_status;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 };
+enum { MOE_ROW_ALIGN = 128 };
+
+typedef struct moe_dims {
+  int32_t T;        /* tokens */
+  int32_t d;        /* hidden size */
+  int32_t f;        /* expert intermediate size */
+  int32_t E;        /* routed experts */
+  int32_t k;        /* experts per token */
+  int32_t f_shared; /* shared-expert width, 0 = none */
+  int32_t score;    /* MOE_SCORE_* */
+  int32_t prec;     /* MOE_PREC_* */
+} moe_dims;
+
+/* Library version of this ABI (increments on any signature change). */
+int32_t moe_abi_version(void);
+
+/* Text of a status code; never NULL. */
+const char* moe_status_string(int32_t status);
+
+/* Validates dims against the limits above.  Host only. */
+moe_status moe_check_dims(const moe_dims* dims);
+
+/* Rows of the padded routed-row space: roundup(T*k,128) + 128*E.  Every [rows, .]
+ * routed buffer (xp, gu, h, y_rows, dy_rows, dgu, dxp, w_rows, row_to_token) has
+ * this many rows.  Returns -1 for invalid dims. */
+int64_t moe_row_capacity(const moe_dims* dims);
+
+/* Bytes of scratch the route and backward calls need (one buffer may serve both;
+ * the route scratch must survive from moe_route_topk to moe_permute). */
+size_t moe_workspace_size(const moe_dims* dims);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t moe_launch_count(void);
+
+/*
+ * Step 1 -- learned top-k routing [DROPLESS "A dropless MoE minden tokent
+ * feldolgoz": each token is processed only by its top-K experts] and the per-expert
+ * token counts handed to the grouped GEMM as split_sizes [BIO "מומחים מקובצים
+ * במקום לולאת Python"].
+ *   logits      [T][E] fp32   router logits (input)
+ *   topk_idx    [T][k] int32  selected experts, best first; ties go to the lower index
+ *   topk_w      [T][k] fp32   routing weights: softmax (or sigmoid) of the logits,
+ *                             renormalised over the k selected experts
+ *   split_sizes [E]    int32  tokens routed to each expert (dropless: sum = T*k)
+ *   offsets     [E+1]  int32  exclusive prefix sum of split_sizes
+ *   row_offsets [E+1]  int32  exclusive prefix sum of split_sizes rounded up to 128
+ *   workspace   >= moe_workspace_size bytes; keeps per-block ranks for moe_permute
+ * dev_status gets MOE_ERR_INVARIANT if the counts do not add up to T*k.
+ */
+moe_status moe_route_topk(const moe_dims* dims, const float* logits, int32_t* topk_idx,
+                          float* topk_w, int32_t* split_sizes, int32_t* offsets,
+                          int32_t* row_offsets, void* workspace, int32_t* dev_status,
+                          void* stream);
+
+/*
+ * Step 2 -- dispatch: copy every token to one row per selected expert, experts
+ * contiguous, tokens of one expert in token order [DROPLESS "Az egyenetlen terhelés
+ * lassítja a tanítást": ragged per-expert tensors; MEGA "Mega MoE คืออะไร?":
+ * dispatch step].  Row of (t, j) = row_offsets[e] + number of tokens t' < t that
+ * also chose e.
+ *   x            [T][d] bf16            token activations
+ *   topk_idx, topk_w, split_sizes, row_offsets: from moe_route_topk
+ *   workspace    the one given to moe_route_topk (read only)
+ *   xp           [rows][d] bf16         permuted rows; padding rows set to 0
+ *   row_to_token [rows] int32           token of each row, -1 for padding rows
+ *   token_to_row [T][k] int32           row of each (token, slot)
+ *   w_rows       [rows] fp32            routing weight of each row, 0 for padding
+ * (rows = moe_row_capacity; entries at or beyond row_offsets[E] are not written.)
+ * dev_status gets MOE_ERR_INVARIANT if a computed row falls outside the row space
+ * (stale or foreign workspace); such a row is skipped, never written.
+ */
+moe_status moe_permute(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx,
+                       const float* topk_w, const int32_t* split_sizes,
+                       const int32_t* row_offsets, const void* workspace, moe_bf16* xp,
+                       int32_t* row_to_token, int32_t* token_to_row, float* w_rows,
+                       int32_t* dev_status, void* stream);
+
+/*
+ * Steps 3-5 -- grouped GEMM gate/up, SwiGLU scaled by the routing weight, grouped
+ * GEMM down, each expert using its actual token count [DROPLESS "Csoportosított
+ * mátrixszorzás és összevont adatmozgatás": one grouped GEMM call for all experts,
+ * no padding to a maximum capacity; BIO "צמצום הזיכרון ותקורות הכימות":
+ * GroupedLinear -> ScaledSwiGLU -> GroupedLinear as one fused operation].
+ * For each row r of expert e:
+ *   G = xp[r] W_gate[e]^T, U = xp[r] W_up[e]^T, h = w_rows[r] * silu(G) * U,
+ *   y_rows[r] = h W_d[e]^T                       (fp32 accumulation, bf16 outputs)
+ *   xp [rows][d], w_gu [E][2f][d], w_d [E][d][f]  (inputs, bf16)
+ *   gu [rows][2f] bf16  saved G (cols [0,f)) and U (cols [f,2f)) for the backward
+ *   h  [rows][f]  bf16  saved scaled activation
+ *   y_rows [rows][d] bf16
+ * Tiles are scheduled on the device from row_offsets (no host synchronisation).
+ */
+moe_status moe_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* xp,
+                               const int32_t* row_offsets, const float* w_rows,
+                               const moe_bf16* w_gu, const moe_bf16* w_d, moe_bf16* gu,
+                               moe_bf16* h, moe_bf16* y_rows, int32_t* dev_status,
+                               void* stream);
+
+/*
+ * The two GEMMs of moe_grouped_mlp_fwd as separate calls (same kernels, same
+ * results; lets a caller time or interleave them):
+ *   moe_gemm_gate_up: gu and h from xp (steps 3-4);  moe_gemm_down: y_rows from h (step 5).
+ */
+moe_status moe_gemm_gate_up(const moe_dims* dims, const moe_bf16* xp,
+                            const int32_t* row_offsets, const float* w_rows,
+                            const moe_bf16* w_gu, moe_bf16* gu, moe_bf16* h,
+                            int32_t* dev_status, void* stream);
+moe_status moe_gemm_down(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets,
+                         const moe_bf16* w_d, moe_bf16* y_rows, int32_t* dev_status, void* stream);
+
+/*
+ * Step 6 -- combine back to token order [MEGA "Mega MoE คืออะไร?": combine step;
+ * DROPLESS "Az egyenetlen terhelés lassítja a tanítást": restore the original
+ * order]:  out[t] = sum_{j<k} rows[token_to_row[t][j]]  (+ shared[t] if given),
+ * summed in fp32 in slot order, rounded once to bf16.  The routing weight was
+ * already applied in the SwiGLU step, so the sum is unweighted.  Also serves as
+ * the un-permute of the backward (dX from dXp).
+ *   rows [rows][d] bf16, token_to_row [T][k], shared [T][d] bf16 or NULL, out [T][d].
+ */
+moe_status moe_combine_fwd(const moe_dims* dims, const moe_bf16* rows,
+                           const int32_t* token_to_row, const moe_bf16* shared,
+                           moe_bf16* out, void* stream);
+
+/*
+ * Backward of step 6 (the adjoint of the combine sum): dy_rows[r] = dY[token of r],
+ * padding rows set to 0.
+ *   dy [T][d] bf16, token_to_row [T][k], split_sizes, row_offsets, dy_rows [rows][d].
+ */
+moe_status moe_combine_bwd(const moe_dims* dims, const moe_bf16* dy,
+                           const int32_t* token_to_row, const int32_t* split_sizes,
+                           const int32_t* row_offsets, moe_bf16* dy_rows, void* stream);
+
+/*
+ * Backward of steps 3-5 [BIO "צמצום הזיכרון ותקורות הכימות": the fused grouped MLP
+ * has a backward counterpart; PRIME "Mit csinált a Prime Intellect?": a backward
+ * pass for the fused MoE kernel].  Per expert e, rows r of e:
+ *   dH = dy_rows[r] W_d[e]; dw_rows[r] = sum_n silu(G)U dH; dA = w dH;
+ *   dG = dA U silu'(G); dU = dA silu(G)               -> dgu[r] = [dG | dU]
+ *   dxp[r] = dgu[r] W_gu[e]
+ *   dW_d[e] = sum_r dy_rows[r]^T h[r];  dW_gu[e] = sum_r dgu[r]^T xp[r]
+ * Experts with no rows get dW = 0.  Sums over rows run in a fixed order (no atomics).
+ *   inputs: xp, row_offsets, w_rows, w_gu, w_d, gu, h (saved by the forward), dy_rows
+ *   dgu [rows][2f] bf16 (output, also consumed internally), dxp [rows][d] bf16,
+ *   dw_gu [E][2f][d] bf16, dw_d [E][d][f] bf16, dw_rows [rows] fp32,
+ *   workspace >= moe_workspace_size bytes.
+ */
+moe_status moe_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* xp,
+                               const int32_t* row_offsets, const float* w_rows,
+                               const moe_bf16* w_gu, const moe_bf16* w_d,
+                               const moe_bf16* gu, const moe_bf16* h,
+                               const moe_bf16* dy_rows, moe_bf16* dgu, moe_bf16* dxp,
+                               moe_bf16* dw_gu, moe_bf16* dw_d, float* dw_rows,
+                               void* workspace, int32_t* dev_status, void* stream);
+
+/*
+ * The four GEMMs of moe_grouped_mlp_bwd as separate calls, in the order the
+ * composite runs them:
+ *   moe_gemm_down_dgrad     dH = dy_rows W_d[e] with the SwiGLU' epilogue -> dgu, dw_rows
+ *                           (workspace holds the per-tile dw partials)
+ *   moe_gemm_down_wgrad     dW_d[e]  = dy_rows_e^T h_e
+ *   moe_gemm_gate_up_dgrad  dxp      = dgu W_gu[e]
+ *   moe_gemm_gate_up_wgrad  dW_gu[e] = dgu_e^T xp_e
+ */
+moe_status moe_gemm_down_dgrad(const moe_dims* dims, const moe_bf16* dy_rows,
+                               const int32_t* row_offsets, const float* w_rows,
+                               const moe_bf16* w_d, const moe_bf16* gu, moe_bf16* dgu,
+                               float* dw_rows, void* workspace, int32_t* dev_status,
+                               void* stream);
+moe_status moe_gemm_down_wgrad(const moe_dims* dims, const moe_bf16* dy_rows, const moe_bf16* h,
+                               const int32_t* row_offsets, moe_bf16* dw_d, int32_t* dev_status,
+                               void* stream);
+moe_status moe_gemm_gate_up_dgrad(const moe_dims* dims, const moe_bf16* dgu,
+                                  const int32_t* row_offsets, const moe_bf16* w_gu, moe_bf16* dxp,
+                                  int32_t* dev_status, void* stream);
+moe_status moe_gemm_gate_up_wgrad(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
+                                  const int32_t* row_offsets, moe_bf16* dw_gu, int32_t* dev_status,
+                                  void* stream);
+
+/*
+ * Backward of step 1: router-logit gradient from the routing-weight gradient.
+ * dw[t][j] = dw_rows[token_to_row[t][j]];  c = sum_j w dw;
+ *   softmax: dl[e_j] = w_j (dw_j - c)
+ *   sigmoid: dl[e_j] = (dw_j - c) / sum_j s_j * s_j (1 - s_j),  s = sigmoid(logit)
+ * and dl = 0 for experts not selected.  d_logits [T][E] fp32.
+ */
+moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
+                              const int32_t* topk_idx, const float* topk_w,
+                              const float* dw_rows, const int32_t* token_to_row,
+                              float* d_logits, void* stream);
+
+/* Synchronises `stream`, then returns the status word written by the kernels
+ * (MOE_OK if none failed) or MOE_ERR_CUDA if the stream itself failed. */
+moe_status moe_check_status(const int32_t* dev_status, void* stream);
+
+/*
+ * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the
+ * tensor-core core: C[m][n] = sum_k A(m,k) B(n,k), fp32 accumulation, bf16 out.
+ *   a_layout 0: A stored [M][K];  1: A stored [K][M]
+ *   b_layout 0: B stored [N][K];  1: B stored [K][N]
+ *   C [M][N].  N % 64 == 0, K % 64 == 0, M >= 1.
+ */
+moe_status moe_gemm_bf16(const moe_bf16* A, const moe_bf16* B, moe_bf16* C, int32_t M,
+                         int32_t N, int32_t K, int32_t a_layout, int32_t b_layout,
+                         int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DROPLESS_MOE_H */

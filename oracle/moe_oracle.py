@@ -82,7 +82,8 @@ def route(logits: np.ndarray, k: int, score: str = SOFTMAX, dtype=np.float64):
         z = np.exp(l - l.max(axis=1, keepdims=True))
         p = z / z.sum(axis=1, keepdims=True)
     elif score == SIGMOID:
-        p = 1.0 / (1.0 + np.exp(-l))
+        with np.errstate(over="ignore"):      # exp(-l) = inf for very negative l gives s = 0
+            p = 1.0 / (1.0 + np.exp(-l))
     else:
         raise ValueError(score)
     ps = np.take_along_axis(p, idx, axis=1)
@@ -135,7 +136,8 @@ def combine_rows(rows: np.ndarray, token_to_row: np.ndarray, dtype=np.float64) -
 # ----------------------------------------------------------------------------------
 
 def _sigmoid(v):
-    return 1.0 / (1.0 + np.exp(-v))
+    with np.errstate(over="ignore"):          # exp(-v) = inf for very negative v gives 0
+        return 1.0 / (1.0 + np.exp(-v))
 
 
 def _silu(v):
