@@ -45,7 +45,8 @@ def workload_name(cfg) -> str:
     names = {"tiny": "tiny MoE layer", "mixtral": "Mixtral-8x7B-shaped MoE layer",
              "qwen30b": "Qwen3-30B-A3B-shaped MoE layer", "qwen235b": "Qwen3-235B-A22B-shaped MoE layer",
              "qwen235b-zipf": "Qwen3-235B-A22B-shaped MoE layer (Zipf routing)",
-             "dsv3": "DeepSeek-V3-shaped routed-expert layer"}
+             "dsv3": "DeepSeek-V3-shaped routed-expert layer",
+             "mixtral-e2": "Mixtral-8x7B-shaped experts (2 of them) MoE layer"}
     return names.get(cfg.name, cfg.name) + " fwd+bwd"
 
 
@@ -209,7 +210,9 @@ def run_native(args, cfg):
     inp = synth.torch_inputs(cfg, dev, seed=cfg.seed + 7919 * rank)
     dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
     bufs = layer.allocate(dims, dev)
-    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    # one explicit stream carries every library call, copy and timing event
+    stream = torch.cuda.Stream(dev)
     x, logits, dy, w_gu, w_d = inp["x"], inp["logits"], inp["dy"], inp["w_gu"], inp["w_d"]
     R = cfg.T * cfg.k
     unit = R * cfg.d * cfg.f
@@ -278,8 +281,12 @@ def run_native(args, cfg):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    gemm_ms = {g: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
-               for i, g in enumerate(GEMMS)}
+    # event windows: mark 0 after permute, 1 after gate_up, 2 after down, 3 after combine_bwd,
+    # 4..7 after each backward GEMM call
+    windows = {"gate_up": (0, 1), "down": (1, 2), "down_dgrad": (3, 4), "down_wgrad": (4, 5),
+               "gate_up_dgrad": (5, 6), "gate_up_wgrad": (6, 7)}
+    gemm_ms = {g: statistics.mean(evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps))
+               for g, (a, b) in windows.items()}
 
     # end to end through the same calls with host buffers: H2D of this step's inputs,
     # D2H of its results (Y, dX, d_logits), inside the timed region
@@ -296,14 +303,15 @@ def run_native(args, cfg):
         dist.barrier()
     torch.cuda.synchronize(dev)
     start.record(stream)
-    for _ in range(e2e_steps):
-        x.copy_(x_h, non_blocking=True)
-        logits.copy_(lg_h, non_blocking=True)
-        dy.copy_(dy_h, non_blocking=True)
-        step()
-        y_h.copy_(bufs.y, non_blocking=True)
-        dx_h.copy_(bufs.dx, non_blocking=True)
-        dl_h.copy_(bufs.d_logits, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            x.copy_(x_h, non_blocking=True)
+            logits.copy_(lg_h, non_blocking=True)
+            dy.copy_(dy_h, non_blocking=True)
+            step()
+            y_h.copy_(bufs.y, non_blocking=True)
+            dx_h.copy_(bufs.dx, non_blocking=True)
+            dl_h.copy_(bufs.d_logits, non_blocking=True)
     end.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = start.elapsed_time(end) / e2e_steps

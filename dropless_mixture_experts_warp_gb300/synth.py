@@ -71,6 +71,10 @@ CONFIGS: Dict[str, MoEConfig] = {
                           bias="zero", seed=1003),
     "qwen235b-zipf": MoEConfig("qwen235b-zipf", T=16384, d=4096, f=1536, E=128, k=8,
                                score=SOFTMAX, bias="zipf", bias_param=1.2, seed=1004),
+    # profiling case: the Mixtral per-expert GEMM shapes (about 2048 rows per expert)
+    # with two experts, so an ncu capture stays near 2 GB of device memory
+    "mixtral-e2": MoEConfig("mixtral-e2", T=4096, d=4096, f=14336, E=2, k=1, score=SOFTMAX,
+                            bias="normal", bias_param=0.1, seed=1006),
     "dsv3": MoEConfig("dsv3", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
                       bias="zipf", bias_param=1.0, forced_empty=4, f_shared=2048, seed=1005),
 }

@@ -18,4 +18,5 @@ from .moe_oracle import (  # noqa: F401
     moe_backward,
     route_backward,
     expert_wgrad,
+    expert_wgrad_sampled,
 )

@@ -308,3 +308,43 @@ def expert_wgrad(x, logits, dy, w_gu_e, w_d_e, e: int, k: int, score: str = SOFT
     du = da * g * sg
     return {"dW_gu": np.concatenate([dg.T @ xe, du.T @ xe], axis=0),
             "dW_d": dye.T @ (we * a), "n": int(t_sel.size)}
+
+
+def expert_wgrad_sampled(x, logits, dy, w_gu_e, w_d_e, e: int, k: int, gu_rows, d_cols,
+                         score: str = SOFTMAX, dtype=np.float32) -> Dict[str, np.ndarray]:
+    """Selected entries of expert e's weight gradients, for sampled checks on large layers.
+
+    Returns dW_gu[e][gu_rows, :] (full rows; row j < f is a gate row, j >= f an up row)
+    and dW_d[e][:, d_cols] (full columns).  Same per-row formulas as moe_backward,
+    evaluated only for the intermediate columns those entries depend on.
+    """
+    idx, w = route(logits, k, score, dtype)
+    t_sel, j_sel = np.nonzero(idx == e)
+    f = w_d_e.shape[1]
+    d = w_d_e.shape[0]
+    gu_rows = np.asarray(gu_rows)
+    d_cols = np.asarray(d_cols)
+    if t_sel.size == 0:
+        return {"dW_gu_rows": np.zeros((gu_rows.size, d), dtype),
+                "dW_d_cols": np.zeros((d, d_cols.size), dtype), "n": 0}
+    xe = np.asarray(x[t_sel], dtype)
+    dye = np.asarray(dy[t_sel], dtype)
+    wg = np.asarray(w_gu_e, dtype)
+    wd = np.asarray(w_d_e, dtype)
+    we = w[t_sel, j_sel][:, None]
+    # rows of dW_gu: need columns c = j mod f of G, U and dH
+    cols = gu_rows % f
+    g = xe @ wg[cols].T
+    u = xe @ wg[f + cols].T
+    sg = _sigmoid(g)
+    dh = dye @ wd[:, cols]
+    da = we * dh
+    dg = da * u * sg * (1.0 + g * (1.0 - sg))
+    du = da * g * sg
+    sel = np.where((gu_rows < f)[None, :], dg, du)          # [n_e, len(gu_rows)]
+    dw_gu_rows = sel.T @ xe
+    # columns of dW_d: need columns c of H = w * silu(G) * U
+    g2 = xe @ wg[d_cols].T
+    u2 = xe @ wg[f + d_cols].T
+    h2 = we * g2 * _sigmoid(g2) * u2
+    return {"dW_gu_rows": dw_gu_rows, "dW_d_cols": dye.T @ h2, "n": int(t_sel.size)}

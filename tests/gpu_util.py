@@ -32,3 +32,21 @@ def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     den = float(np.abs(ref).max()) if ref.size else 0.0
     num = float(np.abs(np.asarray(gpu, np.float64) - ref).max()) if ref.size else 0.0
     return num / den if den > 0 else num
+
+
+class LazyExperts:
+    """Expert weights left on the device; ``[e]`` returns expert e as a float32 host array.
+
+    Lets the oracle's per-expert loop touch only the experts a sampled check needs,
+    one at a time, instead of copying tens of GB to the host.
+    """
+
+    def __init__(self, dev_tensor: torch.Tensor):
+        self.t = dev_tensor
+        self.shape = tuple(dev_tensor.shape)
+
+    def __getitem__(self, e):
+        return self.t[e].float().cpu().numpy()
+
+    def __len__(self):
+        return self.shape[0]

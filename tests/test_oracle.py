@@ -241,6 +241,18 @@ def test_expert_wgrad_matches_full_backward():
         np.testing.assert_allclose(r["dW_d"], bwd["dW_d"][e], rtol=1e-12, atol=1e-12)
 
 
+def test_sampled_wgrad_entries_match_full_wgrad():
+    x, logits, w_gu, w_d, dy, _ = _small_problem(42, E=6, k=3, d=20, f=12)
+    rows = np.array([0, 5, 11, 12, 17, 23])          # gate and up rows
+    cols = np.array([0, 3, 11])
+    for e in range(6):
+        full = om.expert_wgrad(x, logits, dy, w_gu[e], w_d[e], e, 3, om.SOFTMAX)
+        s = om.expert_wgrad_sampled(x, logits, dy, w_gu[e], w_d[e], e, 3, rows, cols, om.SOFTMAX,
+                                    dtype=np.float64)
+        np.testing.assert_allclose(s["dW_gu_rows"], full["dW_gu"][rows], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(s["dW_d_cols"], full["dW_d"][:, cols], rtol=1e-12, atol=1e-12)
+
+
 def test_token_subset_equals_full_batch():
     """Rows of Y, dX and d_logits depend on their own token only (used by sampled checks)."""
     x, logits, w_gu, w_d, dy, _ = _small_problem(51)
