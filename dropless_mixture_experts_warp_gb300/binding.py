@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
-                4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_INVARIANT"}
+                4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_INVARIANT",
+                8: "MOE_ERR_SCRATCH_LIMIT"}
 SCORE = {"softmax": 0, "sigmoid": 1}
 PREC = {"bf16": 0, "mxfp8": 1}
 
@@ -66,6 +67,8 @@ SIGNATURES = {
     "moe_gemm_down_wgrad": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_gemm_gate_up_dgrad": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_gemm_gate_up_wgrad": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P]),
+    "moe_gemm_down_dgrad_noalloc": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -219,3 +222,14 @@ def moe_gemm_gate_up_dgrad(dims, dgu, row_offsets, w_gu, dxp, dev_status, stream
 def moe_gemm_gate_up_wgrad(dims, dgu, xp, row_offsets, dw_gu, dev_status, stream=None):
     return _call("moe_gemm_gate_up_wgrad", _d(dims), _ptr(dgu), _ptr(xp), _ptr(row_offsets), _ptr(dw_gu),
                  _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_down_dgrad_noalloc(dims, dy_rows, row_offsets, w_rows, w_d, gu, dgu, dw_rows, dev_status,
+                                stream=None):
+    """moe_gemm_down_dgrad without a workspace: the dw partials live in the library's static array."""
+    return _call("moe_gemm_down_dgrad_noalloc", _d(dims), _ptr(dy_rows), _ptr(row_offsets), _ptr(w_rows),
+                 _ptr(w_d), _ptr(gu), _ptr(dgu), _ptr(dw_rows), _ptr(dev_status), _stream(stream))
+
+
+def moe_noalloc_scratch_bytes() -> int:
+    return lib().moe_noalloc_scratch_bytes()

@@ -55,6 +55,12 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same encoder, for the other translation units of the library.
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                          uint32_t box_inner, uint32_t box_outer) {
+  return make_map(m, base, inner, outer, box_inner, box_outer);
+}
+
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -123,6 +129,7 @@ const char* moe_status_string(int32_t s) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_INVARIANT: return "routing counts do not sum to T*k";
+    case MOE_ERR_SCRATCH_LIMIT: return "problem too large for the static scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

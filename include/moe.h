@@ -56,7 +56,8 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE = 4,   /* workspace NULL while needed */
   MOE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
   MOE_ERR_TIMEOUT = 6,     /* a bounded device wait gave up (written to dev_status) */
-  MOE_ERR_INVARIANT = 7    /* sum(split_sizes) != T*k seen on the device */
+  MOE_ERR_INVARIANT = 7,   /* sum(split_sizes) != T*k seen on the device */
+  MOE_ERR_SCRATCH_LIMIT = 8 /* too large for moe_gemm_down_dgrad_noalloc's static scratch */
 } moe_status;
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
@@ -250,6 +251,34 @@ moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
                               const int32_t* topk_idx, const float* topk_w,
                               const float* dw_rows, const int32_t* token_to_row,
                               float* d_logits, void* stream);
+
+/*
+ * moe_gemm_down_dgrad without a workspace, for callers that cannot allocate device
+ * memory (a host program that owns all device memory through its own pool and gives
+ * plugins no allocator, or a latency-critical loop where cudaMalloc/cudaFree and the
+ * synchronisation they may bring are not allowed).  The pages have no counterpart:
+ * this is an interface convenience, not a step of the method.
+ *
+ * Same arguments, results and kernels as moe_gemm_down_dgrad minus `workspace`: the
+ * per-tile partial sums of dw go to a static device array of
+ * moe_noalloc_scratch_bytes() bytes (8 MiB) that every GPU loading the library holds
+ * until the process exits.  Requires moe_row_capacity(dims) * (f / BN) <= 2^21,
+ * BN = 256, 128 or 64 (the largest dividing f); larger problems get
+ * MOE_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  All
+ * calls share the one array, which keeps the last call's contents (nothing in it has
+ * to start at zero); calls that overlap on the GPU race on it and give wrong dw_rows.
+ */
+moe_status moe_gemm_down_dgrad_noalloc(const moe_dims* dims, const moe_bf16* dy_rows,
+                                       const int32_t* row_offsets, const float* w_rows,
+                                       const moe_bf16* w_d, const moe_bf16* gu, moe_bf16* dgu,
+                                       float* dw_rows, int32_t* dev_status, void* stream);
+
+/* Bytes of the static array moe_gemm_down_dgrad_noalloc uses. */
+size_t moe_noalloc_scratch_bytes(void);
 
 /* Synchronises `stream`, then returns the status word written by the kernels
  * (MOE_OK if none failed) or MOE_ERR_CUDA if the stream itself failed. */
