@@ -208,7 +208,7 @@ def run_native(args, cfg):
 
     dev = torch.device("cuda", local)
     inp = synth.torch_inputs(cfg, dev, seed=cfg.seed + 7919 * rank)
-    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score)
     bufs = layer.allocate(dims, dev)
     torch.cuda.synchronize(dev)
     # one explicit stream carries every library call, copy and timing event
@@ -232,7 +232,9 @@ def run_native(args, cfg):
         mark(1)
         B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
         mark(2)
-        B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, None, b.y, stream)
+        if cfg.f_shared:
+            B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
+        B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
         B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         mark(3)
         B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
@@ -244,7 +246,10 @@ def run_native(args, cfg):
         mark(6)
         B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
         mark(7)
-        B.moe_combine_fwd(dm, b.dxp, b.token_to_row, None, b.dx, stream)
+        if cfg.f_shared:
+            B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
+                                 b.dw_gu_s, b.dw_d_s, b.status, stream)
+        B.moe_combine_fwd(dm, b.dxp, b.token_to_row, b.dx_s, b.dx, stream)
         B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
 
     for _ in range(args.warmup):

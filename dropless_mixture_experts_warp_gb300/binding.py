@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_gemm_gate_up_wgrad": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_gemm_down_dgrad_noalloc": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "moe_shared_mlp_fwd": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_shared_mlp_bwd": (ctypes.c_int32, [_D] + [_P] * 12),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -233,3 +235,15 @@ def moe_gemm_down_dgrad_noalloc(dims, dy_rows, row_offsets, w_rows, w_d, gu, dgu
 
 def moe_noalloc_scratch_bytes() -> int:
     return lib().moe_noalloc_scratch_bytes()
+
+
+def moe_shared_mlp_fwd(dims, x, w_gu_s, w_d_s, gu_s, h_s, y_s, dev_status, stream=None):
+    return _call("moe_shared_mlp_fwd", _d(dims), _ptr(x), _ptr(w_gu_s), _ptr(w_d_s), _ptr(gu_s), _ptr(h_s),
+                 _ptr(y_s), _ptr(dev_status), _stream(stream))
+
+
+def moe_shared_mlp_bwd(dims, x, w_gu_s, w_d_s, gu_s, h_s, dy, dgu_s, dx_s, dw_gu_s, dw_d_s, dev_status,
+                       stream=None):
+    return _call("moe_shared_mlp_bwd", _d(dims), _ptr(x), _ptr(w_gu_s), _ptr(w_d_s), _ptr(gu_s), _ptr(h_s),
+                 _ptr(dy), _ptr(dgu_s), _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status),
+                 _stream(stream))

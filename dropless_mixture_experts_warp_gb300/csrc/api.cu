@@ -390,6 +390,99 @@ moe_status moe_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* xp,
   return moe_gemm_gate_up_wgrad(dims, dgu, xp, row_offsets, dw_gu, dev_status, stream);
 }
 
+moe_status moe_shared_mlp_fwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_gu_s,
+                              const moe_bf16* w_d_s, moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s,
+                              int32_t* dev_status, void* stream) {
+  moe_status st = moe_check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (d.f_shared <= 0) return MOE_ERR_INVALID_ARG;
+  if (d.T == 0) return MOE_OK;
+  if (!x || !w_gu_s || !w_d_s || !gu_s || !h_s || !y_s || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gu_s) || !aligned16(w_d_s) || !aligned16(gu_s) || !aligned16(h_s) ||
+      !aligned16(y_s))
+    return MOE_ERR_ALIGNMENT;
+  const int fs = d.f_shared;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap ta, tb;
+  // gate/up over all T tokens (one dense group), SwiGLU epilogue with weight 1
+  const int bn1 = (fs % 128 == 0) ? 256 : 128;
+  if (!make_map(&ta, x, d.d, d.T, 64, BM) || !make_map(&tb, w_gu_s, d.d, 2ll * fs, 64, bn1 / 2))
+    return MOE_ERR_CUDA;
+  GemmParams p = gemm_params();
+  p.BN = bn1; p.N = fs; p.K = d.d; p.M = d.T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1;
+  p.f = fs; p.row_limit = d.T; p.gu_out = gu_s; p.h_out = h_s; p.status = dev_status;
+  if (launch_gemm_fwd(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // down
+  const int bn2 = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
+  if (!make_map(&ta, h_s, fs, d.T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, bn2)) return MOE_ERR_CUDA;
+  p = gemm_params();
+  p.BN = bn2; p.N = d.d; p.K = fs; p.M = d.T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.out = y_s; p.ldo = d.d; p.row_limit = d.T; p.status = dev_status;
+  return cuda_status(launch_gemm_fwd(GEMM_ROWS_STORE, ta, tb, p, s));
+}
+
+moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_gu_s,
+                              const moe_bf16* w_d_s, const moe_bf16* gu_s, const moe_bf16* h_s,
+                              const moe_bf16* dy, moe_bf16* dgu_s, moe_bf16* dx_s,
+                              moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
+                              void* stream) {
+  moe_status st = moe_check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (d.f_shared <= 0) return MOE_ERR_INVALID_ARG;
+  if (!w_gu_s || !w_d_s || !dw_gu_s || !dw_d_s || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (!x || !gu_s || !h_s || !dy || !dgu_s || !dx_s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gu_s) || !aligned16(w_d_s) || !aligned16(gu_s) || !aligned16(h_s) ||
+      !aligned16(dy) || !aligned16(dgu_s) || !aligned16(dx_s) || !aligned16(dw_gu_s) || !aligned16(dw_d_s))
+    return MOE_ERR_ALIGNMENT;
+  const int fs = d.f_shared;
+  const int T = d.T;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap ta, tb;
+  GemmParams p;
+  // With T = 0 only the (zero) weight gradients remain; their maps then point at a
+  // weight tensor (never read: the contraction is empty) because a map needs a
+  // non-empty tensor.
+  const uint64_t rows = T > 0 ? static_cast<uint64_t>(T) : 1;
+  const moe_bf16* dy_ = T > 0 ? dy : w_d_s;
+  const moe_bf16* h_ = T > 0 ? h_s : w_d_s;
+  const moe_bf16* x_ = T > 0 ? x : w_gu_s;
+  const moe_bf16* dgu_ = T > 0 ? dgu_s : w_gu_s;
+  if (T > 0) {
+    // dH = dy W_d_s (MN-major B) with the SwiGLU' epilogue, weight 1, no dw
+    if (!make_map(&ta, dy, d.d, T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, 64)) return MOE_ERR_CUDA;
+    p = gemm_params();
+    p.BN = bn_for(fs); p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_k_per_expert = d.d; p.m_fastest = 1;
+    p.f = fs; p.row_limit = T; p.gu_in = gu_s; p.dgu_out = dgu_s; p.status = dev_status;
+    if (launch_gemm_bwd(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // dW_d_s = dy^T h_s  ([d, fs], K = T tokens)
+  if (!make_map(&ta, dy_, d.d, rows, 64, 64) || !make_map(&tb, h_, fs, rows, 64, 64)) return MOE_ERR_CUDA;
+  p = gemm_params();
+  p.BN = bn_for(fs); p.N = fs; p.M = d.d; p.K = T; p.E = 1; p.m_fastest = (d.d <= fs) ? 1 : 0;
+  p.out = dw_d_s; p.ldo = fs; p.row_limit = d.d; p.status = dev_status;
+  if (launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T > 0) {
+    // dx_s = dgu_s W_gu_s (MN-major B)
+    const int bnd = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
+    if (!make_map(&ta, dgu_s, 2ll * fs, T, 64, BM) || !make_map(&tb, w_gu_s, d.d, 2ll * fs, 64, 64))
+      return MOE_ERR_CUDA;
+    p = gemm_params();
+    p.BN = bnd; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_k_per_expert = 2 * fs; p.m_fastest = 1;
+    p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
+    if (launch_gemm_bwd(GEMM_ROWS_STORE_BMN, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // dW_gu_s = dgu_s^T x  ([2fs, d], K = T tokens)
+  if (!make_map(&ta, dgu_, 2ll * fs, rows, 64, 64) || !make_map(&tb, x_, d.d, rows, 64, 64))
+    return MOE_ERR_CUDA;
+  p = gemm_params();
+  p.BN = bn_for(d.d) == 64 ? 128 : bn_for(d.d); p.N = d.d; p.M = 2 * fs; p.K = T; p.E = 1;
+  p.m_fastest = (2 * fs <= d.d) ? 1 : 0; p.out = dw_gu_s; p.ldo = d.d; p.row_limit = 2 * fs;
+  p.status = dev_status;
+  return cuda_status(launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, s));
+}
+
 moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
                               const int32_t* topk_idx, const float* topk_w,
                               const float* dw_rows, const int32_t* token_to_row,

@@ -45,7 +45,7 @@ enum Sched { SCHED_ROWS = 0, SCHED_KGROUP = 1 };
 struct GemmParams {
   int BN;                       // accumulator width: 64, 128 or 256
   int N;                        // output columns (SWIGLU_FWD: h columns = f)
-  int K;                        // contraction length (SCHED_ROWS)
+  int K;                        // contraction length (SCHED_ROWS; dense SCHED_KGROUP)
   int M;                        // SCHED_KGROUP: output rows per expert; dense mode: rows
   int E;                        // groups
   const int32_t* row_offsets;   // [E+1] padded row offsets; NULL = one group of M rows
@@ -56,12 +56,12 @@ struct GemmParams {
   moe_bf16* out;                // EPI_STORE output
   long long ldo;                // its leading dimension (elements)
   long long row_limit;          // rows >= row_limit are not stored
-  const float* w_rows;          // routing weight per row (SwiGLU epilogues)
+  const float* w_rows;          // routing weight per row (SwiGLU epilogues); NULL = 1
   moe_bf16* gu_out;             // SWIGLU_FWD: saved G|U [rows][2f]
   moe_bf16* h_out;              // SWIGLU_FWD: h [rows][f]
   const moe_bf16* gu_in;        // SWIGLU_BWD: saved G|U
   moe_bf16* dgu_out;            // SWIGLU_BWD: dG|dU [rows][2f]
-  float* dw_part;               // SWIGLU_BWD: per-row partial of dw, one per N tile
+  float* dw_part;               // SWIGLU_BWD: per-row partial of dw, one per N tile (or NULL)
   int dw_stride;                // its row stride (= number of N tiles)
   int32_t* status;              // device status word
 };
@@ -140,9 +140,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
 
+  // Without row_offsets the problem is one dense group: M rows (SCHED_ROWS) or a
+  // K of p.K rows (SCHED_KGROUP, rows past the tensor's end read as zeros).
   const int E = p.row_offsets ? p.E : 1;
+  const int dense_rows = (SCHED == SCHED_KGROUP) ? (p.K + BK - 1) / BK * BK : (p.M + BM - 1) / BM * BM;
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
-    s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : (p.M + BM - 1) / BM * BM);
+    s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 4); }
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       } else if (EPI == EPI_SWIGLU_FWD) {
         // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2
         const int half = BN / 2;
-        const float w = row_ok ? p.w_rows[row] : 0.0f;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
         const long long ld2 = 2ll * p.f;
         for (int c0 = 0; c0 < half; c0 += 32) {
           uint32_t g[32], u[32];
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN
-        const float w = row_ok ? p.w_rows[row] : 0.0f;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
         const long long ld2 = 2ll * p.f;
         float dwp = 0.0f;
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         }
-        if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp;
+        if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
       }
       tc_fence_before();
       __syncwarp();

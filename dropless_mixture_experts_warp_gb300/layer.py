@@ -41,6 +41,14 @@ class Buffers:
     d_logits: torch.Tensor
     workspace: torch.Tensor
     status: torch.Tensor
+    # shared expert (dims.f_shared > 0), else None
+    gu_s: torch.Tensor = None
+    h_s: torch.Tensor = None
+    y_s: torch.Tensor = None
+    dgu_s: torch.Tensor = None
+    dx_s: torch.Tensor = None
+    dw_gu_s: torch.Tensor = None
+    dw_d_s: torch.Tensor = None
 
 
 def dims_of(T, d, f, E, k, f_shared=0, score="softmax", prec="bf16") -> B.moe_dims:
@@ -56,7 +64,12 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
     rows = B.moe_row_capacity(dims)
     i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
     e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
-    return Buffers(
+    shared = {}
+    if dims.f_shared:
+        fs = dims.f_shared
+        shared = dict(gu_s=e(T, 2 * fs), h_s=e(T, fs), y_s=e(T, d), dgu_s=e(T, 2 * fs), dx_s=e(T, d),
+                      dw_gu_s=e(2 * fs, d), dw_d_s=e(d, fs))
+    return Buffers(**shared,
         dims=dims, rows=rows,
         topk_idx=e(T, k, dt=i32), topk_w=e(T, k, dt=f32), split_sizes=e(E, dt=i32),
         offsets=e(E + 1, dt=i32), row_offsets=e(E + 1, dt=i32),
@@ -69,8 +82,12 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
     )
 
 
-def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, shared_out=None):
+def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None):
     dm = b.dims
+    shared_out = None
+    if dm.f_shared:
+        B.moe_shared_mlp_fwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
+        shared_out = b.y_s
     B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
                      b.workspace, b.status, stream)
     B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
@@ -80,8 +97,13 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, shared_out=None):
     return b.y
 
 
-def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, shared_dx=None):
+def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None, w_d_s=None):
     dm = b.dims
+    shared_dx = None
+    if dm.f_shared:
+        B.moe_shared_mlp_bwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s, b.dw_d_s,
+                             b.status, stream)
+        shared_dx = b.dx_s
     B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
     B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu, b.dxp,
                           b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)

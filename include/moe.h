@@ -241,6 +241,27 @@ moe_status moe_gemm_gate_up_wgrad(const moe_dims* dims, const moe_bf16* dgu, con
                                   void* stream);
 
 /*
+ * The always-on shared expert of the DeepSeek-V3-shaped layer (dims->f_shared > 0):
+ * a dense SwiGLU MLP on every token with weight 1, whose output is added in the
+ * combine after the k routed terms (pass y_s as `shared` to moe_combine_fwd, and dx_s
+ * as `shared` to the un-permute).  It runs through the same tcgen05 grouped-GEMM
+ * kernel with one dense group of T rows.  Not a step the pages describe: the layer
+ * shape comes from DeepSeek-V3, whose training the pages report.
+ *   fwd: gu_s [T][2fs] = x W_gu_s^T (saved G|U), h_s [T][fs] = silu(G) U, y_s [T][d] = h_s W_d_s^T
+ *   bwd: dgu_s = [dG|dU] from dH = dy W_d_s; dx_s [T][d] = dgu_s W_gu_s;
+ *        dw_d_s [d][fs] = dy^T h_s; dw_gu_s [2fs][d] = dgu_s^T x   (zero when T = 0)
+ * W_gu_s [2fs][d] (gate rows first), W_d_s [d][fs]; all bf16, fp32 accumulation.
+ */
+moe_status moe_shared_mlp_fwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_gu_s,
+                              const moe_bf16* w_d_s, moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s,
+                              int32_t* dev_status, void* stream);
+moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_gu_s,
+                              const moe_bf16* w_d_s, const moe_bf16* gu_s, const moe_bf16* h_s,
+                              const moe_bf16* dy, moe_bf16* dgu_s, moe_bf16* dx_s,
+                              moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
+                              void* stream);
+
+/*
  * Backward of step 1: router-logit gradient from the routing-weight gradient.
  * dw[t][j] = dw_rows[token_to_row[t][j]];  c = sum_j w dw;
  *   softmax: dl[e_j] = w_j (dw_j - c)

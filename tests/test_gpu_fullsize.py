@@ -21,16 +21,17 @@ N_TOKENS = 96
 N_ENTRIES = 12
 
 
-@pytest.mark.parametrize("name", ["mixtral", "qwen30b", "qwen235b", "qwen235b-zipf"])
+@pytest.mark.parametrize("name", ["mixtral", "qwen30b", "qwen235b", "qwen235b-zipf", "dsv3"])
 def test_full_size_layer(name):
     need_gpu()
     from dropless_mixture_experts_warp_gb300 import layer
     cfg = synth.CONFIGS[name]
     inp = synth.torch_inputs(cfg, torch.device("cuda"))
-    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score)
     bufs = layer.allocate(dims)
-    layer.forward(bufs, inp["x"], inp["logits"], inp["w_gu"], inp["w_d"])
-    layer.backward(bufs, inp["dy"], inp["logits"], inp["w_gu"], inp["w_d"])
+    sh = {"w_gu_s": inp["w_gu_s"], "w_d_s": inp["w_d_s"]} if cfg.f_shared else {}
+    layer.forward(bufs, inp["x"], inp["logits"], inp["w_gu"], inp["w_d"], **sh)
+    layer.backward(bufs, inp["dy"], inp["logits"], inp["w_gu"], inp["w_d"], x=inp["x"], **sh)
     layer.check(bufs)
 
     # ---- routing and permutation, in full, bit for bit
@@ -47,14 +48,18 @@ def test_full_size_layer(name):
 
     # ---- sampled tokens: Y, dX, d_logits
     rng = np.random.default_rng(cfg.seed)
-    sub = np.sort(rng.choice(cfg.T, size=N_TOKENS, replace=False))
+    n_tok = N_TOKENS if cfg.E <= 128 else 32     # each sampled token pulls k experts to the host
+    sub = np.sort(rng.choice(cfg.T, size=n_tok, replace=False))
     sub_t = torch.from_numpy(sub).cuda()
     xs = host(inp["x"][sub_t])
     dys = host(inp["dy"][sub_t])
     w_gu = LazyExperts(inp["w_gu"])
     w_d = LazyExperts(inp["w_d"])
-    fwd = om.moe_forward(xs, logits[sub], w_gu, w_d, cfg.k, cfg.score, dtype=np.float32)
-    bwd = om.moe_backward(xs, logits[sub], w_gu, w_d, dys, fwd, cfg.k, cfg.score, dtype=np.float32)
+    skw = {}
+    if cfg.f_shared:
+        skw = {"w_gu_s": host(inp["w_gu_s"]), "w_d_s": host(inp["w_d_s"])}
+    fwd = om.moe_forward(xs, logits[sub], w_gu, w_d, cfg.k, cfg.score, dtype=np.float32, **skw)
+    bwd = om.moe_backward(xs, logits[sub], w_gu, w_d, dys, fwd, cfg.k, cfg.score, dtype=np.float32, **skw)
     errs = {"Y": rel_err(host(bufs.y[sub_t]), fwd["Y"]),
             "dX": rel_err(host(bufs.dx[sub_t]), bwd["dX"]),
             "d_logits": rel_err(host(bufs.d_logits[sub_t]), bwd["d_logits"])}
@@ -73,6 +78,17 @@ def test_full_size_layer(name):
                                     e, cfg.k, rows, cols, cfg.score, dtype=np.float32)
         errs[f"dW_gu[{e}]"] = rel_err(host(bufs.dw_gu[e][torch.from_numpy(rows).cuda()]), s["dW_gu_rows"])
         errs[f"dW_d[{e}]"] = rel_err(host(bufs.dw_d[e][:, torch.from_numpy(cols).cuda()]), s["dW_d_cols"])
+    if cfg.f_shared:
+        # the shared expert is one dense group of all T tokens with weight 1: the
+        # oracle's sampled single-expert formula with a one-expert router gives it
+        fs = cfg.f_shared
+        rows = rng.choice(2 * fs, size=N_ENTRIES, replace=False)
+        cols = rng.choice(fs, size=N_ENTRIES, replace=False)
+        s = om.expert_wgrad_sampled(host(x_all), np.zeros((cfg.T, 1), np.float32), host(dy_all),
+                                    skw["w_gu_s"], skw["w_d_s"], 0, 1, rows, cols, om.SOFTMAX,
+                                    dtype=np.float32)
+        errs["dW_gu_s"] = rel_err(host(bufs.dw_gu_s[torch.from_numpy(rows).cuda()]), s["dW_gu_rows"])
+        errs["dW_d_s"] = rel_err(host(bufs.dw_d_s[:, torch.from_numpy(cols).cuda()]), s["dW_d_cols"])
     bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
     assert not bad, errs
     for e in np.nonzero(split == 0)[0]:

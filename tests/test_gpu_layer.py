@@ -23,6 +23,9 @@ CASES = {
                                   bias="zipf", bias_param=1.0, forced_empty=2, seed=12),
     "many": synth.small_config("many", T=512, d=128, f=128, E=64, k=8, bias="zipf", bias_param=1.1,
                                forced_empty=3, seed=13),
+    # DeepSeek-V3-like: sigmoid scores, Zipf load, forced-empty experts, shared expert
+    "shared": synth.small_config("shared", T=300, d=256, f=128, E=16, k=4, score=synth.SIGMOID,
+                                 bias="zipf", bias_param=1.0, forced_empty=2, f_shared=192, seed=14),
 }
 
 
@@ -30,18 +33,24 @@ def run_layer(cfg, inp=None, weights=None, repeat=1):
     from dropless_mixture_experts_warp_gb300 import layer
     inp = inp or synth.token_inputs(cfg)
     w_gu_b, w_d_b = weights or synth.all_expert_weights(cfg)
-    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score)
     bufs = layer.allocate(dims)
     x, dy, logits = bf16_dev(inp["x"]), bf16_dev(inp["dy"]), f32_dev(inp["logits"])
     w_gu, w_d = bf16_dev(w_gu_b), bf16_dev(w_d_b)
+    sh = {}
+    if cfg.f_shared:
+        s_gu, s_d = synth.shared_weights(cfg)
+        sh = {"w_gu_s": bf16_dev(s_gu), "w_d_s": bf16_dev(s_d)}
+    keys = ["y", "dx", "dw_gu", "dw_d", "d_logits", "topk_idx", "topk_w", "split_sizes", "offsets",
+            "row_offsets", "token_to_row", "row_to_token", "w_rows", "xp", "dw_rows"]
+    if cfg.f_shared:
+        keys += ["dw_gu_s", "dw_d_s"]
     outs = []
     for _ in range(repeat):
-        layer.forward(bufs, x, logits, w_gu, w_d)
-        layer.backward(bufs, dy, logits, w_gu, w_d)
+        layer.forward(bufs, x, logits, w_gu, w_d, **sh)
+        layer.backward(bufs, dy, logits, w_gu, w_d, x=x, **sh)
         layer.check(bufs)
-        outs.append({k: getattr(bufs, k).clone() for k in
-                     ("y", "dx", "dw_gu", "dw_d", "d_logits", "topk_idx", "topk_w", "split_sizes",
-                      "offsets", "row_offsets", "token_to_row", "row_to_token", "w_rows", "xp", "dw_rows")})
+        outs.append({k: getattr(bufs, k).clone() for k in keys})
     return bufs, outs, (inp, w_gu_b, w_d_b)
 
 
@@ -50,8 +59,13 @@ def oracle_layer(cfg, inp, w_gu_b, w_d_b):
     dy = synth.bf16_to_f32(inp["dy"]).astype(np.float64)
     w_gu = synth.bf16_to_f32(w_gu_b).astype(np.float64)
     w_d = synth.bf16_to_f32(w_d_b).astype(np.float64)
-    fwd = om.moe_forward(x, inp["logits"], w_gu, w_d, cfg.k, cfg.score)
-    bwd = om.moe_backward(x, inp["logits"], w_gu, w_d, dy, fwd, cfg.k, cfg.score)
+    kw = {}
+    if cfg.f_shared:
+        s_gu, s_d = synth.shared_weights(cfg)
+        kw = {"w_gu_s": synth.bf16_to_f32(s_gu).astype(np.float64),
+              "w_d_s": synth.bf16_to_f32(s_d).astype(np.float64)}
+    fwd = om.moe_forward(x, inp["logits"], w_gu, w_d, cfg.k, cfg.score, **kw)
+    bwd = om.moe_backward(x, inp["logits"], w_gu, w_d, dy, fwd, cfg.k, cfg.score, **kw)
     return fwd, bwd
 
 
@@ -115,6 +129,9 @@ def test_layer_fwd_bwd_matches_oracle(name):
         "dW_d": rel_err(host(o["dw_d"]), bwd["dW_d"]),
         "d_logits": rel_err(host(o["d_logits"]), bwd["d_logits"]),
     }
+    if cfg.f_shared:
+        errs["dW_gu_s"] = rel_err(host(o["dw_gu_s"]), bwd["dW_gu_s"])
+        errs["dW_d_s"] = rel_err(host(o["dw_d_s"]), bwd["dW_d_s"])
     assert all(v <= TOL_BF16 for v in errs.values()), errs
     # experts with no token get an exactly zero weight gradient
     split = host(o["split_sizes"])
@@ -173,3 +190,22 @@ def test_single_expert_single_token():
     assert rel_err(host(o["dx"]), bwd["dX"]) <= TOL_BF16
     assert rel_err(host(o["dw_gu"]), bwd["dW_gu"]) <= TOL_BF16
     assert rel_err(host(o["dw_d"]), bwd["dW_d"]) <= TOL_BF16
+
+
+def test_shared_expert_zero_tokens_gives_zero_gradients():
+    need_gpu()
+    from dropless_mixture_experts_warp_gb300 import layer
+    dims = layer.dims_of(0, 128, 64, 4, 2, 64, "sigmoid")
+    bufs = layer.allocate(dims)
+    bufs.dw_gu_s.fill_(1.0)
+    bufs.dw_d_s.fill_(1.0)
+    z = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    lz = torch.empty(0, 4, dtype=torch.float32, device="cuda")
+    w_gu = torch.randn(4, 128, 128, device="cuda").to(torch.bfloat16)
+    w_d = torch.randn(4, 128, 64, device="cuda").to(torch.bfloat16)
+    s_gu = torch.randn(128, 128, device="cuda").to(torch.bfloat16)
+    s_d = torch.randn(128, 64, device="cuda").to(torch.bfloat16)
+    layer.forward(bufs, z, lz, w_gu, w_d, w_gu_s=s_gu, w_d_s=s_d)
+    layer.backward(bufs, z, lz, w_gu, w_d, x=z, w_gu_s=s_gu, w_d_s=s_d)
+    layer.check(bufs)
+    assert torch.count_nonzero(bufs.dw_gu_s) == 0 and torch.count_nonzero(bufs.dw_d_s) == 0
