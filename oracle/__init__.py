@@ -20,3 +20,4 @@ from .moe_oracle import (  # noqa: F401
     expert_wgrad,
     expert_wgrad_sampled,
 )
+from . import mx  # noqa: F401,E402

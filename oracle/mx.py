@@ -1,0 +1,217 @@
+"""MXFP8 (E4M3 elements, one E8M0 scale per 32 consecutive elements) for the oracle.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The biology-MoE page ("NVIDIA מציגה דרך יעילה לאמן מודלי MoE בביולוגיה", section
+"צמצום הזיכרון ותקורות הכימות") states the format: 8-bit values with one scale
+factor per block of 32 consecutive values, run on Blackwell's block-scaled tensor
+cores; the dropless-MoE page ("Az NVIDIA szerint tízszer gyorsabb lett a dropless
+MoE tanítása JAX-ban", section "Csoportosított mátrixszorzás és összevont
+adatmozgatás") applies it to the expert GEMMs with group-aware quantisation.  The
+pages do not give the rounding or scale rule; the readings taken here:
+
+  * element format E4M3 (bias 7, 3 mantissa bits, no infinities, largest finite
+    448); encoding rounds to the nearest representable value, ties to the even
+    code, and saturates to +-448 (never produces NaN);
+  * scale = 2^(floor(log2(amax)) - 8), 8 being the largest exponent of E4M3, with
+    the exponent clamped to [-127, 127] and stored as the biased byte e + 127
+    (E8M0); an all-zero block gets scale byte 0 and zero codes;
+  * every GEMM operand is quantised along its own contraction axis; blocks of rows
+    start at the first row of each expert's segment (rows past its end count as 0).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+EMAX_E4M3 = 8
+BLOCK = 32
+
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the 128 non-negative codes (0x7F is NaN and excluded by callers)."""
+    vals = np.empty(128, np.float64)
+    for code in range(128):
+        e = code >> 3
+        m = code & 7
+        vals[code] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    vals[0x7F] = np.nan
+    return vals
+
+
+E4M3_VALUES = _e4m3_table()
+_FINITE = E4M3_VALUES[:0x7F]          # codes 0x00..0x7E, increasing
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    mag = E4M3_VALUES[codes & 0x7F]
+    return np.where(codes & 0x80, -mag, mag)
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to the even code, saturating at 448."""
+    v = np.asarray(v, np.float64)
+    if not np.all(np.isfinite(v)):
+        raise ValueError("e4m3_encode: non-finite input")
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.searchsorted(_FINITE, a, side="left")          # first code with value >= a
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _FINITE[lo]
+    d_hi = _FINITE[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(_FINITE[hi] == a, hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    return (code | (np.signbit(v).astype(np.uint8) << 7)).astype(np.uint8)   # sign kept, -0 = 0x80
+
+
+def scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """floor(log2(amax)) - 8, clamped to [-127, 127]; -127 for amax = 0."""
+    amax = np.asarray(amax, np.float64)
+    _, ex = np.frexp(amax)                       # amax = m 2^ex, m in [0.5, 1)
+    e = ex.astype(np.int64) - 1 - EMAX_E4M3
+    e = np.where(amax > 0, e, -127)
+    return np.clip(e, -127, 127)
+
+
+def mx_quantize(x: np.ndarray):
+    """Quantise along the last axis (length a multiple of 32).
+
+    Returns (codes uint8 like x, scale bytes uint8 [..., K/32]).
+    """
+    x = np.asarray(x, np.float64)
+    K = x.shape[-1]
+    if K % BLOCK:
+        raise ValueError("last axis must be a multiple of 32")
+    blocks = x.reshape(*x.shape[:-1], K // BLOCK, BLOCK)
+    e = scale_exponent(np.abs(blocks).max(axis=-1))
+    codes = e4m3_encode(blocks * np.exp2(-e)[..., None])     # exact power-of-two scaling
+    return codes.reshape(x.shape), (e + 127).astype(np.uint8)
+
+
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    K = codes.shape[-1]
+    v = e4m3_decode(codes).reshape(*codes.shape[:-1], K // BLOCK, BLOCK)
+    return (v * np.exp2(scales.astype(np.float64) - 127)[..., None]).reshape(codes.shape)
+
+
+def qdq(x: np.ndarray) -> np.ndarray:
+    """Quantise then dequantise along the last axis, zero-padding it to a multiple of 32."""
+    x = np.asarray(x, np.float64)
+    K = x.shape[-1]
+    pad = (-K) % BLOCK
+    if pad:
+        x = np.concatenate([x, np.zeros((*x.shape[:-1], pad))], axis=-1)
+    return mx_dequantize(*mx_quantize(x))[..., :K]
+
+
+def mx_matmul(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """a [M,K] x b [N,K]^T with both operands MXFP8-quantised along K (the shared axis)."""
+    return (qdq(a) @ qdq(b).T).astype(dtype)
+
+
+# ----------------------------------------------------------------------------------
+# The layer with MXFP8 GEMM operands
+# ----------------------------------------------------------------------------------
+
+def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=None,
+                   dtype=np.float64, matmul=mx_matmul):
+    """Forward of the layer with every GEMM operand quantised along its contraction axis.
+
+    Same steps as moe_oracle.moe_forward; the two GEMMs of each expert become
+    G|U = mx(X_e, W_gu[e]) (both along d) and Y = mx(H_e, W_d[e]) (both along f).
+    ``matmul`` is the GEMM used (identity quantisation gives back the plain forward).
+    """
+    from . import moe_oracle as om
+    x = np.asarray(x, dtype)
+    T, d = x.shape
+    E = w_gu.shape[0]
+    f = w_d.shape[2]
+    idx, w = om.route(logits, k, score, dtype)
+    y_slot = np.zeros((T, k, d), dtype)
+    g_slot = np.zeros((T, k, f), dtype)
+    u_slot = np.zeros((T, k, f), dtype)
+    for e in range(E):
+        t_sel, j_sel = np.nonzero(idx == e)
+        if t_sel.size == 0:
+            continue
+        wg = np.asarray(w_gu[e], dtype)
+        wd = np.asarray(w_d[e], dtype)
+        gu = matmul(x[t_sel], wg, dtype)
+        g, u = gu[:, :f], gu[:, f:]
+        h = w[t_sel, j_sel][:, None] * (g * om._sigmoid(g) * u)
+        y_slot[t_sel, j_sel] = matmul(h, wd, dtype)
+        g_slot[t_sel, j_sel] = g
+        u_slot[t_sel, j_sel] = u
+    y = np.zeros((T, d), dtype)
+    for j in range(k):
+        y += y_slot[:, j]
+    out = {"Y": y, "idx": idx, "w": w, "g": g_slot, "u": u_slot}
+    if w_gu_s is not None:
+        fs = w_d_s.shape[1]
+        gu = matmul(x, np.asarray(w_gu_s, dtype), dtype)
+        g, u = gu[:, :fs], gu[:, fs:]
+        out["Y"] = y + matmul(g * om._sigmoid(g) * u, np.asarray(w_d_s, dtype), dtype)
+        out["g_s"], out["u_s"] = g, u
+    return out
+
+
+def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=None, w_d_s=None,
+                    dtype=np.float64, matmul=mx_matmul):
+    """Backward with MXFP8 GEMM operands (quantisation treated as identity in the chain rule).
+
+    Per expert e, rows in token order (its segment):
+      dH = mx(dY_e, W_d[e]^T)         both along d
+      dX_e = mx(dGU_e, W_gu[e]^T)     both along 2f
+      dW_d[e] = mx(dY_e^T, H_e^T)     both along the rows of e
+      dW_gu[e] = mx(dGU_e^T, X_e^T)   both along the rows of e
+    The SwiGLU' step, dw and the router gradient are as in moe_oracle.moe_backward.
+    """
+    from . import moe_oracle as om
+    x = np.asarray(x, dtype)
+    dy = np.asarray(dy, dtype)
+    T, d = x.shape
+    E = w_gu.shape[0]
+    f = w_d.shape[2]
+    idx, w = fwd["idx"], fwd["w"]
+    dx_slot = np.zeros((T, k, d), dtype)
+    dw = np.zeros((T, k), dtype)
+    dw_gu = np.zeros((E, 2 * f, d), dtype)
+    dw_d = np.zeros((E, d, f), dtype)
+    for e in range(E):
+        t_sel, j_sel = np.nonzero(idx == e)
+        if t_sel.size == 0:
+            continue
+        wg = np.asarray(w_gu[e], dtype)
+        wd = np.asarray(w_d[e], dtype)
+        g = fwd["g"][t_sel, j_sel]
+        u = fwd["u"][t_sel, j_sel]
+        sg = om._sigmoid(g)
+        a = g * sg * u
+        we = w[t_sel, j_sel][:, None]
+        dye = dy[t_sel]
+        dh = matmul(dye, wd.T, dtype)
+        dw[t_sel, j_sel] = (a * dh).sum(axis=1)
+        da = we * dh
+        dgu = np.concatenate([da * u * sg * (1.0 + g * (1.0 - sg)), da * g * sg], axis=1)
+        dx_slot[t_sel, j_sel] = matmul(dgu, wg.T, dtype)
+        dw_d[e] = matmul(dye.T, (we * a).T, dtype)
+        dw_gu[e] = matmul(dgu.T, x[t_sel].T, dtype)
+    dx = np.zeros((T, d), dtype)
+    for j in range(k):
+        dx += dx_slot[:, j]
+    out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw,
+           "d_logits": om.route_backward(logits, idx, w, dw, score, dtype)}
+    if w_gu_s is not None:
+        fs = w_d_s.shape[1]
+        wg = np.asarray(w_gu_s, dtype)
+        wd = np.asarray(w_d_s, dtype)
+        g, u = fwd["g_s"], fwd["u_s"]
+        sg = om._sigmoid(g)
+        dh = matmul(dy, wd.T, dtype)
+        dgu = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg], axis=1)
+        out["dX"] = dx + matmul(dgu, wg.T, dtype)
+        out["dW_d_s"] = matmul(dy.T, (g * sg * u).T, dtype)
+        out["dW_gu_s"] = matmul(dgu.T, x.T, dtype)
+    return out
