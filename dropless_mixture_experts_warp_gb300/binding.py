@@ -71,6 +71,10 @@ SIGNATURES = {
     "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "moe_shared_mlp_fwd": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_shared_mlp_bwd": (ctypes.c_int32, [_D] + [_P] * 12),
+    "moe_test_wait_timeout": (ctypes.c_int32, [_P, ctypes.c_int64, _P]),
+    "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
+    "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
+    "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -247,3 +251,22 @@ def moe_shared_mlp_bwd(dims, x, w_gu_s, w_d_s, gu_s, h_s, dy, dgu_s, dx_s, dw_gu
     return _call("moe_shared_mlp_bwd", _d(dims), _ptr(x), _ptr(w_gu_s), _ptr(w_d_s), _ptr(gu_s), _ptr(h_s),
                  _ptr(dy), _ptr(dgu_s), _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status),
                  _stream(stream))
+
+
+def moe_test_wait_timeout(dev_status, limit_cycles, stream=None):
+    return _call("moe_test_wait_timeout", _ptr(dev_status), limit_cycles, _stream(stream))
+
+
+def moe_mx_quantize_rows(src, rows, C, ld, nrows_dev, codes, scales, stream=None):
+    return _call("moe_mx_quantize_rows", _ptr(src), rows, C, ld, _ptr(nrows_dev), _ptr(codes), _ptr(scales),
+                 _stream(stream))
+
+
+def moe_mx_quantize_cols(src, batch, rows, C, nrows_dev, codes_t, scales, stream=None):
+    return _call("moe_mx_quantize_cols", _ptr(src), batch, rows, C, _ptr(nrows_dev), _ptr(codes_t),
+                 _ptr(scales), _stream(stream))
+
+
+def moe_gemm_mxfp8(a, a_sf, b, b_sf, c, M, N, K, dev_status, stream=None):
+    return _call("moe_gemm_mxfp8", _ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K,
+                 _ptr(dev_status), _stream(stream))

@@ -55,6 +55,20 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D uint8 tensor (E4M3 codes) [outer][inner], 128B swizzle, zero fill.
+bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same encoder, for the other translation units of the library.
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer) {
@@ -504,6 +518,11 @@ moe_status moe_check_status(const int32_t* dev_status, void* stream) {
   if (cudaMemcpy(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   return static_cast<moe_status>(v);
+}
+
+moe_status moe_test_wait_timeout(int32_t* dev_status, int64_t limit_cycles, void* stream) {
+  if (!dev_status || limit_cycles < 1 || limit_cycles > (1ll << 32)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout(dev_status, limit_cycles, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_bf16(const moe_bf16* A, const moe_bf16* B, moe_bf16* C, int32_t M,

@@ -64,6 +64,11 @@ struct GemmParams {
   float* dw_part;               // SWIGLU_BWD: per-row partial of dw, one per N tile (or NULL)
   int dw_stride;                // its row stride (= number of N tiles)
   int32_t* status;              // device status word
+  // block-scaled (MXFP8) operands only: SF tiles and their number of K tiles per 128 rows
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int a_sf_ktiles;
+  int b_sf_ktiles;
 };
 
 struct TileCoord {
@@ -75,7 +80,7 @@ struct TileCoord {
   long long out_base; // element offset of the group's output (SCHED_KGROUP)
 };
 
-template <int SCHED, int EPI, bool B_MN>
+template <int SCHED, int EPI, bool B_MN, int KB = BK>
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* s_ro, int E,
                                                 int n_tiles, int tile) {
   TileCoord c;
@@ -91,7 +96,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
     if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
-    c.kblocks = p.K / BK;
+    c.kblocks = p.K / KB;
     c.a_m = s_ro[e] + c.m * BM;
     c.a_k = 0;
     c.out_col = (EPI == EPI_SWIGLU_FWD) ? c.n * (p.BN / 2) : c.n * p.BN;
@@ -107,7 +112,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
     if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
-    c.kblocks = (s_ro[e + 1] - s_ro[e]) / BK;
+    c.kblocks = (s_ro[e + 1] - s_ro[e]) / KB;
     c.a_m = c.m * BM;
     c.a_k = s_ro[e];
     c.b_n = c.n * p.BN;
@@ -120,6 +125,110 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
 }
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
+
+// Epilogue of one tile for one thread (one accumulator row): reads the fp32
+// accumulator columns from TMEM (32 at a time) and applies the fused EPI step.
+// Every lane of the warp must call it (tcgen05.ld is warp-wide).
+template <int EPI>
+__device__ __forceinline__ void tile_epilogue(const GemmParams& p, const TileCoord& c, uint32_t tbase,
+                                              long long row, bool row_ok, int BN) {
+  if (EPI == EPI_STORE) {
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      if (c.kblocks > 0) {
+        tmem_ld32(tbase + c0, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + c.out_base + row * p.ldo + c.out_col + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+          o.y = pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+          o.z = pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+          o.w = pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+          dst[v] = o;
+        }
+      }
+    }
+  } else if (EPI == EPI_SWIGLU_FWD) {
+    // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2
+    const int half = BN / 2;
+    const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+    const long long ld2 = 2ll * p.f;
+    for (int c0 = 0; c0 < half; c0 += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(tbase + c0, g);
+      tmem_ld32(tbase + half + c0, u);
+      tmem_wait_ld();
+      if (row_ok) {
+        uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + c.out_col + c0);
+        uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + c.out_col + c0);
+        uint4* hdst = reinterpret_cast<uint4*>(p.h_out + row * p.f + c.out_col + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float hv[8], gv[8], uv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            gv[i] = __uint_as_float(g[8 * v + i]);
+            uv[i] = __uint_as_float(u[8 * v + i]);
+            hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
+          }
+          gdst[v] = make_uint4(pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
+                               pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
+          udst[v] = make_uint4(pack_bf16(uv[0], uv[1]), pack_bf16(uv[2], uv[3]),
+                               pack_bf16(uv[4], uv[5]), pack_bf16(uv[6], uv[7]));
+          hdst[v] = make_uint4(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
+                               pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
+        }
+      }
+    }
+  } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN
+    const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+    const long long ld2 = 2ll * p.f;
+    float dwp = 0.0f;
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tbase + c0, r);
+      tmem_wait_ld();
+      if (row_ok) {
+        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
+        const uint4* usrc =
+            reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
+        uint4* gdst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + c.out_col + c0);
+        uint4* udst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + p.f + c.out_col + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 g4 = gsrc[v], u4 = usrc[v];
+          const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+          const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+          float dg[8], du[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+            const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
+            const float dh = __uint_as_float(r[8 * v + i]);
+            const float sg = sigmoidf_(g);
+            const float silu = g * sg;
+            const float da = w * dh;
+            dwp += silu * u * dh;
+            dg[i] = da * u * sg * (1.0f + g * (1.0f - sg));
+            du[i] = da * silu;
+          }
+          gdst[v] = make_uint4(pack_bf16(dg[0], dg[1]), pack_bf16(dg[2], dg[3]),
+                               pack_bf16(dg[4], dg[5]), pack_bf16(dg[6], dg[7]));
+          udst[v] = make_uint4(pack_bf16(du[0], du[1]), pack_bf16(du[2], du[3]),
+                               pack_bf16(du[4], du[5]), pack_bf16(du[6], du[7]));
+        }
+      }
+    }
+    if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
+  }
+}
 
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
@@ -266,102 +375,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const long long row = c.out_row + row_in_tile;
       const bool row_ok = row < p.row_limit;
 
-      if (EPI == EPI_STORE) {
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t r[32];
-          if (c.kblocks > 0) {
-            tmem_ld32(tbase + c0, r);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + c.out_base + row * p.ldo + c.out_col + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              o.y = pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              o.z = pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              o.w = pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-              dst[v] = o;
-            }
-          }
-        }
-      } else if (EPI == EPI_SWIGLU_FWD) {
-        // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2
-        const int half = BN / 2;
-        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
-        const long long ld2 = 2ll * p.f;
-        for (int c0 = 0; c0 < half; c0 += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tbase + c0, g);
-          tmem_ld32(tbase + half + c0, u);
-          tmem_wait_ld();
-          if (row_ok) {
-            uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + c.out_col + c0);
-            uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + c.out_col + c0);
-            uint4* hdst = reinterpret_cast<uint4*>(p.h_out + row * p.f + c.out_col + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float hv[8], gv[8], uv[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                gv[i] = __uint_as_float(g[8 * v + i]);
-                uv[i] = __uint_as_float(u[8 * v + i]);
-                hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
-              }
-              gdst[v] = make_uint4(pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
-                                   pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
-              udst[v] = make_uint4(pack_bf16(uv[0], uv[1]), pack_bf16(uv[2], uv[3]),
-                                   pack_bf16(uv[4], uv[5]), pack_bf16(uv[6], uv[7]));
-              hdst[v] = make_uint4(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
-                                   pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
-            }
-          }
-        }
-      } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN
-        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
-        const long long ld2 = 2ll * p.f;
-        float dwp = 0.0f;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tbase + c0, r);
-          tmem_wait_ld();
-          if (row_ok) {
-            const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
-            const uint4* usrc =
-                reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
-            uint4* gdst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + c.out_col + c0);
-            uint4* udst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + p.f + c.out_col + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 g4 = gsrc[v], u4 = usrc[v];
-              const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-              const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
-              float dg[8], du[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-                const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
-                const float dh = __uint_as_float(r[8 * v + i]);
-                const float sg = sigmoidf_(g);
-                const float silu = g * sg;
-                const float da = w * dh;
-                dwp += silu * u * dh;
-                dg[i] = da * u * sg * (1.0f + g * (1.0f - sg));
-                du[i] = da * silu;
-              }
-              gdst[v] = make_uint4(pack_bf16(dg[0], dg[1]), pack_bf16(dg[2], dg[3]),
-                                   pack_bf16(dg[4], dg[5]), pack_bf16(dg[6], dg[7]));
-              udst[v] = make_uint4(pack_bf16(du[0], du[1]), pack_bf16(du[2], du[3]),
-                                   pack_bf16(du[4], du[5]), pack_bf16(du[6], du[7]));
-            }
-          }
-        }
-        if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
-      }
+      tile_epilogue<EPI>(p, c, tbase, row, row_ok, BN);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);

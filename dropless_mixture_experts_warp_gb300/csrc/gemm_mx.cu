@@ -1,0 +1,29 @@
+// Instantiations of the MXFP8 grouped GEMM.
+#include "gemm_mx.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+template <int SCHED, int EPI>
+static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                               cudaStream_t stream) {
+  auto kern = grouped_gemm_mx_kernel<SCHED, EPI>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MX_SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms(), GEMM_THREADS, MX_SMEM_BYTES, stream>>>(a, b, p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                           cudaStream_t stream) {
+  switch (kind) {
+    case GEMM_ROWS_SWIGLU_FWD: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_FWD>(a, b, p, stream);
+    case GEMM_ROWS_STORE: return launch_mx_t<SCHED_ROWS, EPI_STORE>(a, b, p, stream);
+    case GEMM_ROWS_SWIGLU_BWD: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD>(a, b, p, stream);
+    case GEMM_KGROUP_STORE: return launch_mx_t<SCHED_KGROUP, EPI_STORE>(a, b, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

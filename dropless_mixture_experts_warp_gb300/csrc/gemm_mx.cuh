@@ -1,0 +1,187 @@
+// Persistent grouped GEMM with MXFP8 operands on tcgen05 (kind::mxf8f6f4.block_scale).
+//
+// Same roles and schedule as the bf16 kernel (gemm.cuh): warp 0 loads, warp 1 issues,
+// warps 2..5 run the shared epilogue.  Differences:
+//   * operands are E4M3 codes, both K-major, 128 codes (128 bytes) per stage row;
+//   * each stage also carries the E8M0 scale tiles of its A rows (512 B) and B rows
+//     (512 B per 128 rows), fetched with contiguous bulk copies; the MMA warp moves
+//     them into TMEM with tcgen05.cp (32x128b, replicated to the four lane quarters)
+//     and every MMA (K = 32) selects its byte of the scale words with the
+//     scale-factor id of the instruction descriptor;
+//   * TMEM holds one 256-column accumulator (BN = 256) or two of 128 (BN = 128) in
+//     columns 0..255 and the scale factors of each stage from column 256 on.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace moe {
+
+constexpr int MX_BK = 128;                                  // K elements (= bytes) per stage
+constexpr int MX_A_BYTES = BM * MX_BK;                      // 16 KB
+constexpr int MX_B_BYTES_MAX = 256 * MX_BK;                 // 32 KB
+constexpr int MX_SFA_OFF = MX_A_BYTES + MX_B_BYTES_MAX;     // scale tiles after the codes
+constexpr int MX_SFB_OFF = MX_SFA_OFF + 512;
+constexpr int MX_STAGE_BYTES = 50 * 1024;                   // 48 KB codes + 1.5 KB scales, 1 KB aligned
+constexpr int MX_STAGES = 4;
+constexpr int MX_SMEM_BYTES = MX_STAGES * MX_STAGE_BYTES + 1024;
+constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
+constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
+
+template <int SCHED, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[MX_STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[MX_STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_ro[MAX_EXPERTS + 1];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int E = p.row_offsets ? p.E : 1;
+  const int dense_rows =
+      (SCHED == SCHED_KGROUP) ? (p.K + MX_BK - 1) / MX_BK * MX_BK : (p.M + BM - 1) / BM * BM;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x)
+    s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 4); }
+    mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 1) { tmem_alloc(&s_tmem_base, TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+
+  const int BN = p.BN;                       // 128 or 256
+  const int num_acc = BN <= 128 ? 2 : 1;
+  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t stage_tx = MX_A_BYTES + BN * MX_BK + 512 + (BN / 128) * 512;
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          uint8_t* sa = smem + stage * MX_STAGE_BYTES;
+          uint8_t* sb = sa + MX_A_BYTES;
+          uint64_t* bar = &full_bar[stage];
+          mbar_arrive_expect_tx(bar, stage_tx);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          const int ka = c.a_k + kb * MX_BK;     // K index of A (and of B: b_k == a_k here)
+          const int kbt = ka / MX_BK;
+          tma_load_2d(sa, &tmA, bar, ka, c.a_m);
+          bulk_load(sa + MX_SFA_OFF,
+                    p.sfa + (static_cast<size_t>(c.a_m / 128) * p.a_sf_ktiles + kbt) * 512, 512, bar);
+          const int kbb = c.b_k + kb * MX_BK;
+          const int kbtb = kbb / MX_BK;
+          if (EPI == EPI_SWIGLU_FWD) {           // gate rows then up rows, 128 each
+            tma_load_2d(sb, &tmB, bar, kbb, c.b_n);
+            tma_load_2d(sb + (BN / 2) * MX_BK, &tmB, bar, kbb, c.b_n + p.f);
+            bulk_load(sa + MX_SFB_OFF,
+                      p.sfb + (static_cast<size_t>(c.b_n / 128) * p.b_sf_ktiles + kbtb) * 512, 512, bar);
+            bulk_load(sa + MX_SFB_OFF + 512,
+                      p.sfb + (static_cast<size_t>((c.b_n + p.f) / 128) * p.b_sf_ktiles + kbtb) * 512, 512,
+                      bar);
+          } else {
+            tma_load_2d(sb, &tmB, bar, kbb, c.b_n);
+            for (int i = 0; i < BN / 128; ++i)
+              bulk_load(sa + MX_SFB_OFF + 512 * i,
+                        p.sfb + (static_cast<size_t>(c.b_n / 128 + i) * p.b_sf_ktiles + kbtb) * 512, 512, bar);
+          }
+          if (++stage == MX_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      for (int s = 0; s < MX_STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_drain(&full_bar[s], (armed_parity >> s) & 1u, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+        if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status,
+                               WAIT_LIMIT_CYCLES)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * MX_STAGE_BYTES);
+          const uint32_t sb = sa + MX_A_BYTES;
+          const uint32_t sfa_t = tmem_base + MX_SF_TMEM_COL + stage * MX_SF_COLS_PER_STAGE;
+          const uint32_t sfb_t = sfa_t + 4;
+          // scale tiles: 32 rows x 16 B each, 8-row core matrices 128 B apart
+          tc_cp_32x128b_x4(sfa_t, smem_desc_plain(sa + MX_SFA_OFF, 0, 128));
+          for (int i = 0; i < BN / 128; ++i)
+            tc_cp_32x128b_x4(sfb_t + 4 * i, smem_desc_plain(sa + MX_SFB_OFF + 512 * i, 0, 128));
+#pragma unroll
+          for (int kk = 0; kk < MX_BK / 32; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == MX_STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+        if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
+      }
+      tc_commit(&drain_bar);
+      mbar_drain(&drain_bar, 0, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const long long row = c.out_row + row_in_tile;
+      tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace moe

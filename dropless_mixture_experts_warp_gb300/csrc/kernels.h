@@ -43,6 +43,8 @@ cudaError_t launch_route_bwd(const float* logits, int T, int E, int k, int score
                              const int32_t* token_to_row, float* d_logits, int rows_cap,
                              cudaStream_t stream);
 
+cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t stream);
+
 // Grouped-GEMM variants (scheduling, epilogue, A/B majorness).
 enum GemmKind {
   GEMM_ROWS_SWIGLU_FWD = 0,  // ragged rows, K-major A and B, SwiGLU*w epilogue
@@ -58,6 +60,19 @@ cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
                             const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, cudaStream_t stream);
+
+// MXFP8 variants (both operands K-major E4M3 codes + scale tiles); kind is one of
+// GEMM_ROWS_SWIGLU_FWD, GEMM_ROWS_STORE, GEMM_ROWS_SWIGLU_BWD, GEMM_KGROUP_STORE.
+cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                           cudaStream_t stream);
+cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
+                              uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
+                                uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                          uint32_t box_inner, uint32_t box_outer);
+bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer);
 
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,

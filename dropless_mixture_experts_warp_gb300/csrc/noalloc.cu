@@ -23,9 +23,6 @@ namespace moe {
 constexpr size_t NOALLOC_DW_PART_FLOATS = size_t(2) << 20;  // 8 MiB of fp32 partials
 static __device__ __align__(256) float g_dw_part_scratch[NOALLOC_DW_PART_FLOATS];
 
-bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                          uint32_t box_inner, uint32_t box_outer);
-
 // Device address of the array on the current device.  In host code the array's
 // name is only a host-side stand-in, so the address is looked up once per device
 // (with that device current) and cached.

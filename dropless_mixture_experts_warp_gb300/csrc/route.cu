@@ -362,3 +362,26 @@ cudaError_t launch_route_bwd(const float* logits, int T, int E, int k, int score
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// One thread waits on an mbarrier that nothing ever arrives on, through the same
+// bounded wait the GEMM pipeline uses; it must give up after `limit` cycles and
+// leave MOE_ERR_TIMEOUT in the status word.
+__global__ void wait_timeout_kernel(int32_t* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait_bounded(&bar, 0, &abort_flag, status, limit);
+}
+
+cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(status, limit);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -306,6 +306,45 @@ size_t moe_noalloc_scratch_bytes(void);
 moe_status moe_check_status(const int32_t* dev_status, void* stream);
 
 /*
+ * Test hook for failure detection: one thread waits, through the same bounded
+ * mbarrier wait as the GEMM pipeline, on a barrier that nothing arrives on.  After
+ * limit_cycles (1 .. 2^32) it gives up and writes MOE_ERR_TIMEOUT to dev_status; the
+ * CUDA context stays usable.  Lets a test make a device wait run out on purpose.
+ */
+moe_status moe_test_wait_timeout(int32_t* dev_status, int64_t limit_cycles, void* stream);
+
+/*
+ * MXFP8 building blocks (E4M3 codes, one E8M0 scale per 32 elements along the GEMM's
+ * contraction axis) [BIO "צמצום הזיכרון ותקורות הכימות": one scale per block of 32
+ * consecutive values, block-scaled Blackwell tensor-core instructions; DROPLESS
+ * "Csoportosított mátrixszorzás és összevont adatmozgatás": group-aware MXFP8
+ * quantisation for the expert GEMMs].
+ * Scale rule: e = floor(log2(amax)) - 8 clamped to [-127,127], byte e + 127 (0 for an
+ * all-zero block); codes = E4M3(x * 2^-e), round to nearest even, saturating at 448.
+ * Scale layout ("SF tiles"): for an operand of R rows (M or N) and K columns the
+ * scales form 512-byte tiles, tile (r/128, k/128) at byte (r/128 * K/128 + k/128)*512;
+ * inside, byte ((r%32)*4 + (r%128)/32)*4 + (k%128)/32 is the scale of row r's block k/32.
+ * Scale arrays therefore hold roundup(R,128) * K/32 bytes.
+ *
+ * moe_mx_quantize_rows: src bf16 [rows][ld] (first C columns) -> codes [rows][C] and
+ *   SF tiles with K = C (blocks along each row).  C % 128 == 0.  Rows at or beyond
+ *   *nrows_dev (if not NULL) are skipped.
+ * moe_mx_quantize_cols: src bf16 [batch][rows][C] -> codes_t [batch][C][rows] and, per
+ *   batch, SF tiles of an operand with C rows and K = rows (blocks of 32 rows down each
+ *   column).  rows % 128 == 0, C % 128 == 0; 128-row tiles at or beyond *nrows_dev are
+ *   skipped.  Per batch, scales take C * rows / 32 bytes.
+ * moe_gemm_mxfp8: C[M][N] bf16 = sum_k deq(A)(m,k) deq(B)(n,k) with A codes [M][K],
+ *   B codes [N][K] (both K-major) and their SF tiles; fp32 accumulation on the
+ *   block-scaled tensor cores.  M, N, K multiples of 128.
+ */
+moe_status moe_mx_quantize_rows(const moe_bf16* src, int64_t rows, int32_t C, int64_t ld,
+                                const int32_t* nrows_dev, uint8_t* codes, uint8_t* scales, void* stream);
+moe_status moe_mx_quantize_cols(const moe_bf16* src, int32_t batch, int64_t rows, int32_t C,
+                                const int32_t* nrows_dev, uint8_t* codes_t, uint8_t* scales, void* stream);
+moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                          moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream);
+
+/*
  * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the
  * tensor-core core: C[m][n] = sum_k A(m,k) B(n,k), fp32 accumulation, bf16 out.
  *   a_layout 0: A stored [M][K];  1: A stored [K][M]

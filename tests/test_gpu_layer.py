@@ -209,3 +209,21 @@ def test_shared_expert_zero_tokens_gives_zero_gradients():
     layer.backward(bufs, z, lz, w_gu, w_d, x=z, w_gu_s=s_gu, w_d_s=s_d)
     layer.check(bufs)
     assert torch.count_nonzero(bufs.dw_gu_s) == 0 and torch.count_nonzero(bufs.dw_d_s) == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A device wait on a barrier nothing arrives on gives up and reports MOE_ERR_TIMEOUT."""
+    need_gpu()
+    from dropless_mixture_experts_warp_gb300 import binding as B
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_test_wait_timeout(status, 1 << 24)       # about 8 ms at 2 GHz
+    assert B.moe_check_status(status) == 6         # MOE_ERR_TIMEOUT
+    # the context is still usable: a GEMM after the timeout runs and is right
+    A = torch.randn(128, 64, device="cuda").to(torch.bfloat16)
+    Bm = torch.randn(64, 64, device="cuda").to(torch.bfloat16)
+    C = torch.empty(128, 64, dtype=torch.bfloat16, device="cuda")
+    ok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_gemm_bf16(A, Bm, C, 128, 64, 64, 0, 0, ok)
+    assert B.moe_check_status(ok) == 0
+    ref = A.float() @ Bm.float().T
+    assert rel_err(host(C), host(ref).astype(np.float64)) < 1e-2
