@@ -35,6 +35,10 @@ UNIT = "TFLOP/s"
 GEMMS = ["gate_up", "down", "down_dgrad", "down_wgrad", "gate_up_dgrad", "gate_up_wgrad"]
 GEMM_FLOP_FACTOR = {"gate_up": 4, "down": 2, "down_dgrad": 2, "down_wgrad": 2, "gate_up_dgrad": 4,
                     "gate_up_wgrad": 4}   # x R*d*f
+GEMM_KERNEL_MX = {"gate_up": "grouped_gemm_mx_kernel<0,1>", "down": "grouped_gemm_mx_kernel<0,0>",
+                  "down_dgrad": "grouped_gemm_mx_kernel<0,2> + dw_reduce_kernel",
+                  "down_wgrad": "grouped_gemm_mx_kernel<1,0>", "gate_up_dgrad": "grouped_gemm_mx_kernel<0,0>",
+                  "gate_up_wgrad": "grouped_gemm_mx_kernel<1,0>"}
 GEMM_KERNEL = {"gate_up": "grouped_gemm_kernel<0,1,0,0>", "down": "grouped_gemm_kernel<0,0,0,0>",
                "down_dgrad": "grouped_gemm_kernel<0,2,0,1> + dw_reduce_kernel",
                "down_wgrad": "grouped_gemm_kernel<1,0,1,1>", "gate_up_dgrad": "grouped_gemm_kernel<0,0,0,1>",
@@ -128,10 +132,13 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: float, chunk: int, seed=0):
+def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: float, chunk: int, seed=0,
+                       prec="bf16"):
     """Run the CPU oracle (fp32) on random token chunks for about `seconds`; returns FLOP/s and tokens."""
     import numpy as np
     from oracle import moe_oracle as om
+    from oracle import mx
+    fwd_fn, bwd_fn = (mx.moe_forward_mx, mx.moe_backward_mx) if prec == "mxfp8" else (om.moe_forward, om.moe_backward)
     from dropless_mixture_experts_warp_gb300 import synth
     rng = np.random.default_rng(seed)
     done_tok, t_total = 0, 0.0
@@ -141,8 +148,8 @@ def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: flo
         dy = synth.bf16_to_f32(dy_bits[sub])
         lg = logits[sub]
         t0 = time.perf_counter()
-        fwd = om.moe_forward(x, lg, w_gu32, w_d32, cfg.k, cfg.score, dtype=np.float32)
-        om.moe_backward(x, lg, w_gu32, w_d32, dy, fwd, cfg.k, cfg.score, dtype=np.float32)
+        fwd = fwd_fn(x, lg, w_gu32, w_d32, cfg.k, cfg.score, dtype=np.float32)
+        bwd_fn(x, lg, w_gu32, w_d32, dy, fwd, cfg.k, cfg.score, dtype=np.float32)
         t_total += time.perf_counter() - t0
         done_tok += chunk
     flops = 18.0 * done_tok * cfg.k * cfg.d * cfg.f
@@ -208,7 +215,8 @@ def run_native(args, cfg):
 
     dev = torch.device("cuda", local)
     inp = synth.torch_inputs(cfg, dev, seed=cfg.seed + 7919 * rank)
-    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, args.prec)
+    mx8 = args.prec == "mxfp8"
     bufs = layer.allocate(dims, dev)
     torch.cuda.synchronize(dev)
     # one explicit stream carries every library call, copy and timing event
@@ -227,24 +235,42 @@ def run_native(args, cfg):
                          b.workspace, b.status, stream)
         B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
                       b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
+        if mx8:   # the 16-bit master weights are quantised every step
+            B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
         mark(0)
-        B.moe_gemm_gate_up(dm, b.xp, b.row_offsets, b.w_rows, w_gu, b.gu, b.h, b.status, stream)
+        if mx8:
+            B.moe_gemm_gate_up_mx(dm, b.xp, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.h, b.status, stream)
+        else:
+            B.moe_gemm_gate_up(dm, b.xp, b.row_offsets, b.w_rows, w_gu, b.gu, b.h, b.status, stream)
         mark(1)
-        B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
+        if mx8:
+            B.moe_gemm_down_mx(dm, b.h, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
+        else:
+            B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
         mark(2)
         if cfg.f_shared:
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
         B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
         B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         mark(3)
-        B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
-                              b.workspace, b.status, stream)
-        mark(4)
-        B.moe_gemm_down_wgrad(dm, b.dy_rows, b.h, b.row_offsets, b.dw_d, b.status, stream)
-        mark(5)
-        B.moe_gemm_gate_up_dgrad(dm, b.dgu, b.row_offsets, w_gu, b.dxp, b.status, stream)
-        mark(6)
-        B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
+        if mx8:
+            B.moe_gemm_down_dgrad_mx(dm, b.dy_rows, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dgu,
+                                     b.dw_rows, b.workspace, b.status, stream)
+            mark(4)
+            B.moe_gemm_down_wgrad_mx(dm, b.dy_rows, b.h, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+            mark(5)
+            B.moe_gemm_gate_up_dgrad_mx(dm, b.dgu, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
+            mark(6)
+            B.moe_gemm_gate_up_wgrad_mx(dm, b.dgu, b.xp, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+        else:
+            B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
+                                  b.workspace, b.status, stream)
+            mark(4)
+            B.moe_gemm_down_wgrad(dm, b.dy_rows, b.h, b.row_offsets, b.dw_d, b.status, stream)
+            mark(5)
+            B.moe_gemm_gate_up_dgrad(dm, b.dgu, b.row_offsets, w_gu, b.dxp, b.status, stream)
+            mark(6)
+            B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
         mark(7)
         if cfg.f_shared:
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
@@ -332,18 +358,21 @@ def run_native(args, cfg):
     dom = max(GEMMS, key=lambda g: gemm_ms[g])
     dom_flops = GEMM_FLOP_FACTOR[dom] * unit
     achieved = dom_flops / (gemm_ms[dom] * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # MXFP8 has no measured peak: bf16's measured figure times the nominal 2x ratio
+    peak = peaks["bf16_tflops_sustained"] * (2.0 if mx8 else 1.0)
     traffic = read_traffic(dom)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_json(cfg),
+        "vs_baseline": None, "dtype": "e4m3+e8m0 (MXFP8), fp32 acc" if mx8 else "bf16", "data": "synthetic",
+        "config": config_json(cfg, args.prec),
         "tokens_per_s": world * cfg.T / (ms * 1e-3),
-        "frac_of_bf16_peak": value / world / peak,
-        "roofline": {"bound": "tensor", "kernel": f"{dom} ({GEMM_KERNEL[dom]})", "achieved": achieved,
+        "frac_of_peak": value / world / peak,
+        "roofline": {"bound": "tensor", "kernel": f"{dom} ({(GEMM_KERNEL_MX if mx8 else GEMM_KERNEL)[dom]})", "achieved": achieved,
                      "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (timed inside a long step)",
+                     "peak_source": (f"{peak_src} bf16_tflops_sustained x 2 (nominal MXFP8/bf16 ratio)" if mx8 else
+                                     f"{peak_src} bf16_tflops_sustained (timed inside a long step)"),
                      "flops_per_launch": dom_flops, "ms_per_launch": gemm_ms[dom]},
         "gemm_ms": {g: round(v, 4) for g, v in gemm_ms.items()},
         "gemm_tflops": {g: GEMM_FLOP_FACTOR[g] * unit / (gemm_ms[g] * 1e-3) / 1e12 for g in GEMMS},
@@ -360,7 +389,7 @@ def run_native(args, cfg):
         w_gu32 = w_gu.float().cpu().numpy()
         w_d32 = w_d.float().cpu().numpy()
         rate, ntok, secs = oracle_sample_rate(cfg, ex["x"], ex["logits"], ex["dy"], w_gu32, w_d32,
-                                              args.cpu_seconds, args.ref_tokens)
+                                              args.cpu_seconds, args.ref_tokens, prec=args.prec)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{ntok} random tokens of the {cfg.T}-token batch, fp32 NumPy, "
                                           f"{secs:.1f} s"}
@@ -378,6 +407,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--prec", default="bf16", choices=["bf16", "mxfp8"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")

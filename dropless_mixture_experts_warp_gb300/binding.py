@@ -75,6 +75,15 @@ SIGNATURES = {
     "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
     "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_mx_weights_size": (ctypes.c_size_t, [_D]),
+    "moe_mx_workspace_size": (ctypes.c_size_t, [_D]),
+    "moe_mx_quantize_weights": (ctypes.c_int32, [_D, _P, _P, _P, _P]),
+    "moe_gemm_gate_up_mx": (ctypes.c_int32, [_D] + [_P] * 9),
+    "moe_gemm_down_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_down_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 11),
+    "moe_gemm_down_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_gate_up_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_gate_up_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -270,3 +279,47 @@ def moe_mx_quantize_cols(src, batch, rows, C, nrows_dev, codes_t, scales, stream
 def moe_gemm_mxfp8(a, a_sf, b, b_sf, c, M, N, K, dev_status, stream=None):
     return _call("moe_gemm_mxfp8", _ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K,
                  _ptr(dev_status), _stream(stream))
+
+
+def moe_mx_weights_size(dims) -> int:
+    return lib().moe_mx_weights_size(_d(dims))
+
+
+def moe_mx_workspace_size(dims) -> int:
+    return lib().moe_mx_workspace_size(_d(dims))
+
+
+def moe_mx_quantize_weights(dims, w_gu, w_d, wq, stream=None):
+    return _call("moe_mx_quantize_weights", _d(dims), _ptr(w_gu), _ptr(w_d), _ptr(wq), _stream(stream))
+
+
+def moe_gemm_gate_up_mx(dims, xp, row_offsets, w_rows, wq, mx_ws, gu, h, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_mx", _d(dims), _ptr(xp), _ptr(row_offsets), _ptr(w_rows), _ptr(wq),
+                 _ptr(mx_ws), _ptr(gu), _ptr(h), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_down_mx(dims, h, row_offsets, wq, mx_ws, y_rows, dev_status, stream=None):
+    return _call("moe_gemm_down_mx", _d(dims), _ptr(h), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws), _ptr(y_rows),
+                 _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_down_dgrad_mx(dims, dy_rows, row_offsets, w_rows, wq, mx_ws, gu, dgu, dw_rows, workspace,
+                           dev_status, stream=None):
+    return _call("moe_gemm_down_dgrad_mx", _d(dims), _ptr(dy_rows), _ptr(row_offsets), _ptr(w_rows), _ptr(wq),
+                 _ptr(mx_ws), _ptr(gu), _ptr(dgu), _ptr(dw_rows), _ptr(workspace), _ptr(dev_status),
+                 _stream(stream))
+
+
+def moe_gemm_down_wgrad_mx(dims, dy_rows, h, row_offsets, mx_ws, dw_d, dev_status, stream=None):
+    return _call("moe_gemm_down_wgrad_mx", _d(dims), _ptr(dy_rows), _ptr(h), _ptr(row_offsets), _ptr(mx_ws),
+                 _ptr(dw_d), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_gate_up_dgrad_mx(dims, dgu, row_offsets, wq, mx_ws, dxp, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_dgrad_mx", _d(dims), _ptr(dgu), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws),
+                 _ptr(dxp), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_gate_up_wgrad_mx(dims, dgu, xp, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(dgu), _ptr(xp), _ptr(row_offsets), _ptr(mx_ws),
+                 _ptr(dw_gu), _ptr(dev_status), _stream(stream))

@@ -117,6 +117,9 @@ static Carve carve(const moe_dims& d, void* ws) {
   return c;
 }
 
+// The dw-partials region of a caller workspace (shared by the bf16 and MXFP8 calls).
+float* workspace_dw_part(const moe_dims& d, void* ws) { return carve(d, ws).dw_part; }
+
 static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 static GemmParams gemm_params() {
@@ -156,7 +159,7 @@ moe_status moe_check_dims(const moe_dims* dims) {
   if (d.k > d.E || d.k > 32) return MOE_ERR_INVALID_ARG;
   if (d.score != MOE_SCORE_SOFTMAX && d.score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (d.prec != MOE_PREC_BF16 && d.prec != MOE_PREC_MXFP8) return MOE_ERR_INVALID_ARG;
-  if (d.prec != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
+  if (d.prec == MOE_PREC_MXFP8 && (d.f % 128 != 0 || d.f_shared % 128 != 0)) return MOE_ERR_UNSUPPORTED;
   if (d.E > MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
   if (d.d % 128 != 0 || d.f % 64 != 0 || d.f_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (row_capacity(d) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;

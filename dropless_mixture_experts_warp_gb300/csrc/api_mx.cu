@@ -51,3 +51,285 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
 }
 
 }  // extern "C"
+
+// ============================================================================ layer path
+
+namespace moe {
+
+static inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
+static int bn_mx(int n) { return n % 256 == 0 ? 256 : 128; }
+
+// One MXFP8 operand: codes and their SF tiles.
+struct MxOp {
+  uint8_t* codes;
+  uint8_t* sf;
+};
+
+static size_t op_bytes(size_t elems) { return a256(elems) + a256(elems / 32); }
+
+static MxOp carve_op(uint8_t*& p, size_t elems) {
+  MxOp o;
+  o.codes = p;
+  p += a256(elems);
+  o.sf = p;
+  p += a256(elems / 32);
+  return o;
+}
+
+// Quantised weights: W_gu along d ([E*2f][d]), W_gu along 2f ([E][d][2f]),
+// W_d along f ([E*d][f]), W_d along d ([E][f][d]).
+struct MxWeights {
+  MxOp gu_rows, gu_cols, d_rows, d_cols;
+};
+
+static MxWeights carve_weights(const moe_dims& d, void* base) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t n = static_cast<size_t>(d.E) * 2 * d.f * d.d;
+  const size_t m = static_cast<size_t>(d.E) * d.f * d.d;
+  MxWeights w;
+  w.gu_rows = carve_op(p, n);
+  w.gu_cols = carve_op(p, n);
+  w.d_rows = carve_op(p, m);
+  w.d_cols = carve_op(p, m);
+  return w;
+}
+
+// Quantised activations of one step, each along the contraction axis of its GEMM.
+struct MxActs {
+  MxOp xp_rows, xp_cols, h_rows, h_cols, dy_rows, dy_cols, dgu_rows, dgu_cols;
+};
+
+static MxActs carve_acts(const moe_dims& d, int64_t R_cap, void* base) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t rd = static_cast<size_t>(R_cap) * d.d, rf = static_cast<size_t>(R_cap) * d.f;
+  MxActs a;
+  a.xp_rows = carve_op(p, rd);
+  a.xp_cols = carve_op(p, rd);
+  a.h_rows = carve_op(p, rf);
+  a.h_cols = carve_op(p, rf);
+  a.dy_rows = carve_op(p, rd);
+  a.dy_cols = carve_op(p, rd);
+  a.dgu_rows = carve_op(p, 2 * rf);
+  a.dgu_cols = carve_op(p, 2 * rf);
+  return a;
+}
+
+static moe_status mx_common(const moe_dims* dims) {
+  moe_status st = moe_check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static GemmParams mx_params() {
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  return p;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_mx_weights_size(const moe_dims* dims) {
+  if (mx_common(dims) != MOE_OK) return 0;
+  const size_t n = static_cast<size_t>(dims->E) * 2 * dims->f * dims->d;
+  const size_t m = static_cast<size_t>(dims->E) * dims->f * dims->d;
+  return 2 * op_bytes(n) + 2 * op_bytes(m);
+}
+
+size_t moe_mx_workspace_size(const moe_dims* dims) {
+  if (mx_common(dims) != MOE_OK) return 0;
+  const size_t R = static_cast<size_t>(moe_row_capacity(dims));
+  const size_t rd = R * dims->d, rf = R * dims->f;
+  return 4 * op_bytes(rd) + 2 * op_bytes(rf) + 2 * op_bytes(2 * rf);
+}
+
+moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, const moe_bf16* w_d, void* wq,
+                                   void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!w_gu || !w_d || !wq) return MOE_ERR_INVALID_ARG;
+  if (!al16(w_gu) || !al16(w_d) || !al16(wq)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_weights(d, wq);
+  const long long E = d.E;
+  if (launch_quant_rows(w_gu, E * 2 * d.f, d.d, d.d, nullptr, w.gu_rows.codes, w.gu_rows.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(w_gu, d.E, 2ll * d.f, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s) != cudaSuccess ||
+      launch_quant_rows(w_d, E * d.d, d.f, d.f, nullptr, w.d_rows.codes, w.d_rows.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(w_d, d.E, d.d, d.f, nullptr, w.d_cols.codes, w.d_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const moe_bf16* xp, const int32_t* row_offsets,
+                               const float* w_rows, const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* h,
+                               int32_t* dev_status, void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!xp || !row_offsets || !w_rows || !wq || !mx_ws || !gu || !h || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(xp) || !al16(wq) || !al16(mx_ws) || !al16(gu) || !al16(h)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_weights(d, const_cast<void*>(wq));
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  if (launch_quant_rows(xp, R_cap, d.d, d.d, row_offsets + d.E, a.xp_rows.codes, a.xp_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.xp_rows.codes, d.d, R_cap, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.gu_rows.codes, d.d, 2ll * d.f * d.E, 128, 128))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = 256; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = 2 * d.f;
+  p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
+  p.gu_out = gu; p.h_out = h; p.status = dev_status;
+  p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s));
+}
+
+moe_status moe_gemm_down_mx(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets, const void* wq,
+                            void* mx_ws, moe_bf16* y_rows, int32_t* dev_status, void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!h || !row_offsets || !wq || !mx_ws || !y_rows || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(h) || !al16(wq) || !al16(mx_ws) || !al16(y_rows)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_weights(d, const_cast<void*>(wq));
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  if (launch_quant_rows(h, R_cap, d.f, d.f, row_offsets + d.E, a.h_rows.codes, a.h_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.d);
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.h_rows.codes, d.f, R_cap, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.d_rows.codes, d.f, static_cast<uint64_t>(d.d) * d.E, 128, bn))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
+  p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
+  p.sfa = a.h_rows.sf; p.sfb = w.d_rows.sf; p.a_sf_ktiles = d.f / 128; p.b_sf_ktiles = d.f / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+}
+
+moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const int32_t* row_offsets,
+                                  const float* w_rows, const void* wq, void* mx_ws, const moe_bf16* gu,
+                                  moe_bf16* dgu, float* dw_rows, void* workspace, int32_t* dev_status,
+                                  void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!dy_rows || !row_offsets || !w_rows || !wq || !mx_ws || !gu || !dgu || !dw_rows || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (!al16(dy_rows) || !al16(wq) || !al16(mx_ws) || !al16(gu) || !al16(dgu)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_weights(d, const_cast<void*>(wq));
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  // the dw partials use the same region of the workspace as the bf16 call
+  float* dw_part = workspace_dw_part(d, workspace);
+  if (launch_quant_rows(dy_rows, R_cap, d.d, d.d, row_offsets + d.E, a.dy_rows.codes, a.dy_rows.sf, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.f);
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, R_cap, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.d_cols.codes, d.d, static_cast<uint64_t>(d.f) * d.E, 128, bn))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.f;
+  p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
+  p.dgu_out = dgu; p.dw_part = dw_part; p.dw_stride = d.f / bn; p.status = dev_status;
+  p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_st(launch_dw_reduce(dw_part, d.f / bn, row_offsets, d.E, dw_rows, static_cast<int>(R_cap), s));
+}
+
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const moe_bf16* h,
+                                  const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
+                                  void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!dy_rows || !h || !row_offsets || !mx_ws || !dw_d || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(dy_rows) || !al16(h) || !al16(mx_ws) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  const int32_t* nrows = row_offsets + d.E;
+  if (launch_quant_cols_t(dy_rows, 1, R_cap, d.d, nrows, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(h, 1, R_cap, d.f, nrows, a.h_cols.codes, a.h_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.f);
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.dy_cols.codes, R_cap, d.d, 128, BM) ||
+      !make_tensor_map_u8(&tb, a.h_cols.codes, R_cap, d.f, 128, bn))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = bn; p.N = d.f; p.M = d.d; p.E = d.E; p.row_offsets = row_offsets; p.m_fastest = (d.d <= d.f) ? 1 : 0;
+  p.out = dw_d; p.ldo = d.f; p.row_limit = d.d; p.status = dev_status;
+  p.sfa = a.dy_cols.sf; p.sfb = a.h_cols.sf; p.a_sf_ktiles = static_cast<int>(R_cap / 128);
+  p.b_sf_ktiles = static_cast<int>(R_cap / 128);
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+}
+
+moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const int32_t* row_offsets,
+                                     const void* wq, void* mx_ws, moe_bf16* dxp, int32_t* dev_status,
+                                     void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!dgu || !row_offsets || !wq || !mx_ws || !dxp || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(dgu) || !al16(wq) || !al16(mx_ws) || !al16(dxp)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_weights(d, const_cast<void*>(wq));
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  if (launch_quant_rows(dgu, R_cap, 2 * d.f, 2ll * d.f, row_offsets + d.E, a.dgu_rows.codes, a.dgu_rows.sf, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.d);
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * d.f, R_cap, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.gu_cols.codes, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E, 128, bn))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
+  p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
+  p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * d.f / 128; p.b_sf_ktiles = 2 * d.f / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+}
+
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
+                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu, int32_t* dev_status,
+                                     void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!dgu || !xp || !row_offsets || !mx_ws || !dw_gu || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(dgu) || !al16(xp) || !al16(mx_ws) || !al16(dw_gu)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  const int32_t* nrows = row_offsets + d.E;
+  if (launch_quant_cols_t(dgu, 1, R_cap, 2 * d.f, nrows, a.dgu_cols.codes, a.dgu_cols.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(xp, 1, R_cap, d.d, nrows, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.d);
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_u8(&ta, a.dgu_cols.codes, R_cap, 2ll * d.f, 128, BM) ||
+      !make_tensor_map_u8(&tb, a.xp_cols.codes, R_cap, d.d, 128, bn))
+    return MOE_ERR_CUDA;
+  GemmParams p = mx_params();
+  p.BN = bn; p.N = d.d; p.M = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets;
+  p.m_fastest = (2 * d.f <= d.d) ? 1 : 0; p.out = dw_gu; p.ldo = d.d; p.row_limit = 2 * d.f;
+  p.status = dev_status;
+  p.sfa = a.dgu_cols.sf; p.sfb = a.xp_cols.sf; p.a_sf_ktiles = static_cast<int>(R_cap / 128);
+  p.b_sf_ktiles = static_cast<int>(R_cap / 128);
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+}
+
+}  // extern "C"

@@ -69,6 +69,7 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,

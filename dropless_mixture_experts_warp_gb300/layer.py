@@ -49,6 +49,9 @@ class Buffers:
     dx_s: torch.Tensor = None
     dw_gu_s: torch.Tensor = None
     dw_d_s: torch.Tensor = None
+    # MXFP8 path (dims.prec == mxfp8): quantised weights and activation scratch
+    wq: torch.Tensor = None
+    mx_ws: torch.Tensor = None
 
 
 def dims_of(T, d, f, E, k, f_shared=0, score="softmax", prec="bf16") -> B.moe_dims:
@@ -69,6 +72,9 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
         fs = dims.f_shared
         shared = dict(gu_s=e(T, 2 * fs), h_s=e(T, fs), y_s=e(T, d), dgu_s=e(T, 2 * fs), dx_s=e(T, d),
                       dw_gu_s=e(2 * fs, d), dw_d_s=e(d, fs))
+    if dims.prec == 1:
+        shared["wq"] = torch.empty(B.moe_mx_weights_size(dims), dtype=torch.uint8, device=device)
+        shared["mx_ws"] = torch.empty(B.moe_mx_workspace_size(dims), dtype=torch.uint8, device=device)
     return Buffers(**shared,
         dims=dims, rows=rows,
         topk_idx=e(T, k, dt=i32), topk_w=e(T, k, dt=f32), split_sizes=e(E, dt=i32),
@@ -92,7 +98,14 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
                      b.workspace, b.status, stream)
     B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
                   b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
-    B.moe_grouped_mlp_fwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.y_rows, b.status, stream)
+    if dm.prec == 1:
+        # 16-bit master weights are quantised every step (they change every optimiser step)
+        B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
+        B.moe_gemm_gate_up_mx(dm, b.xp, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.h, b.status, stream)
+        B.moe_gemm_down_mx(dm, b.h, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
+    else:
+        B.moe_grouped_mlp_fwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.y_rows, b.status,
+                              stream)
     B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, shared_out, b.y, stream)
     return b.y
 
@@ -105,8 +118,15 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
                              b.status, stream)
         shared_dx = b.dx_s
     B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
-    B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu, b.dxp,
-                          b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)
+    if dm.prec == 1:
+        B.moe_gemm_down_dgrad_mx(dm, b.dy_rows, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dgu, b.dw_rows,
+                                 b.workspace, b.status, stream)
+        B.moe_gemm_down_wgrad_mx(dm, b.dy_rows, b.h, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+        B.moe_gemm_gate_up_dgrad_mx(dm, b.dgu, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
+        B.moe_gemm_gate_up_wgrad_mx(dm, b.dgu, b.xp, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+    else:
+        B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu,
+                              b.dxp, b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)
     B.moe_combine_fwd(dm, b.dxp, b.token_to_row, shared_dx, b.dx, stream)
     B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
     return b.dx

@@ -51,7 +51,7 @@ typedef uint16_t moe_bf16; /* bfloat16 bit pattern */
 typedef enum moe_status {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* bad size, NULL pointer, k > E, ... */
-  MOE_ERR_UNSUPPORTED = 2, /* valid but not supported (d % 128, f % 64, E > 1024, ...) */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but not supported (d % 128, f % 64 (% 128 for MXFP8), E > 1024, ...) */
   MOE_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
   MOE_ERR_WORKSPACE = 4,   /* workspace NULL while needed */
   MOE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
@@ -343,6 +343,45 @@ moe_status moe_mx_quantize_cols(const moe_bf16* src, int32_t batch, int64_t rows
                                 const int32_t* nrows_dev, uint8_t* codes_t, uint8_t* scales, void* stream);
 moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
                           moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream);
+
+/*
+ * The grouped GEMMs with MXFP8 operands (dims->prec may be either value; f % 128 == 0).
+ * Each call first quantises its activation operands along the contraction axis of
+ * its GEMM (row blocks along d, f or 2f; column blocks of 32 rows inside each
+ * 128-aligned expert segment for the weight gradients) into `mx_ws`, then runs the
+ * block-scaled tcgen05 GEMM with the same fused epilogues and the same bf16 outputs
+ * as the bf16 calls.  The backward treats quantisation as the identity.
+ *   wq:    >= moe_mx_weights_size bytes, filled by moe_mx_quantize_weights from the
+ *          bf16 master weights (W_gu along d and along 2f, W_d along f and along d);
+ *          refill it whenever the weights change.
+ *   mx_ws: >= moe_mx_workspace_size bytes of caller scratch for the quantised
+ *          activations; the calls of one step must share it (the gate/up and down
+ *          weight-gradient calls reuse nothing, each quantises what it reads).
+ * Same arguments otherwise as moe_gemm_gate_up, moe_gemm_down, moe_gemm_down_dgrad,
+ * moe_gemm_down_wgrad, moe_gemm_gate_up_dgrad, moe_gemm_gate_up_wgrad.
+ */
+size_t moe_mx_weights_size(const moe_dims* dims);
+size_t moe_mx_workspace_size(const moe_dims* dims);
+moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, const moe_bf16* w_d, void* wq,
+                                   void* stream);
+moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const moe_bf16* xp, const int32_t* row_offsets,
+                               const float* w_rows, const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* h,
+                               int32_t* dev_status, void* stream);
+moe_status moe_gemm_down_mx(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets, const void* wq,
+                            void* mx_ws, moe_bf16* y_rows, int32_t* dev_status, void* stream);
+moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const int32_t* row_offsets,
+                                  const float* w_rows, const void* wq, void* mx_ws, const moe_bf16* gu,
+                                  moe_bf16* dgu, float* dw_rows, void* workspace, int32_t* dev_status,
+                                  void* stream);
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const moe_bf16* h,
+                                  const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
+                                  void* stream);
+moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const int32_t* row_offsets,
+                                     const void* wq, void* mx_ws, moe_bf16* dxp, int32_t* dev_status,
+                                     void* stream);
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
+                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu,
+                                     int32_t* dev_status, void* stream);
 
 /*
  * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the

@@ -1,0 +1,93 @@
+"""The MXFP8 layer path through the C ABI against the MXFP8 oracle.
+
+Weight codes and scales are compared bit for bit; layer outputs and gradients by
+max|gpu - oracle| / max|oracle| <= 6e-2.  The GPU quantises the bf16-stored h and
+dG|dU while the oracle quantises its fp32/fp64 values, and accumulation orders
+differ, so intermediate codes may differ by one step; the tolerance covers that.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bf16_dev, f32_dev, host, need_gpu, rel_err
+from oracle import mx
+from dropless_mixture_experts_warp_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_MXFP8 = 6e-2
+
+CASES = {
+    "mx-ragged": synth.small_config("mx-ragged", T=1000, d=256, f=128, E=8, k=2, bias_param=0.7, seed=41),
+    "mx-zipf": synth.small_config("mx-zipf", T=777, d=384, f=256, E=16, k=4, score=synth.SIGMOID, bias="zipf",
+                                  bias_param=1.0, forced_empty=2, seed=42),
+}
+
+
+def _run(cfg):
+    from dropless_mixture_experts_warp_gb300 import layer
+    inp = synth.token_inputs(cfg)
+    w_gu_b, w_d_b = synth.all_expert_weights(cfg)
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score, "mxfp8")
+    b = layer.allocate(dims)
+    w_gu, w_d = bf16_dev(w_gu_b), bf16_dev(w_d_b)
+    logits = f32_dev(inp["logits"])
+    layer.forward(b, bf16_dev(inp["x"]), logits, w_gu, w_d)
+    layer.backward(b, bf16_dev(inp["dy"]), logits, w_gu, w_d)
+    layer.check(b)
+    return b, inp, w_gu_b, w_d_b
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_mx_layer_matches_mx_oracle(name):
+    need_gpu()
+    cfg = CASES[name]
+    b, inp, w_gu_b, w_d_b = _run(cfg)
+    f64 = lambda a: synth.bf16_to_f32(a).astype(np.float64)  # noqa: E731
+    fwd = mx.moe_forward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), cfg.k, cfg.score)
+    bwd = mx.moe_backward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), f64(inp["dy"]), fwd,
+                             cfg.k, cfg.score)
+    errs = {"Y": rel_err(host(b.y), fwd["Y"]), "dX": rel_err(host(b.dx), bwd["dX"]),
+            "dW_gu": rel_err(host(b.dw_gu), bwd["dW_gu"]), "dW_d": rel_err(host(b.dw_d), bwd["dW_d"]),
+            "d_logits": rel_err(host(b.d_logits), bwd["d_logits"])}
+    assert all(v <= TOL_MXFP8 for v in errs.values()), errs
+    split = host(b.split_sizes)
+    for e in np.nonzero(split == 0)[0]:
+        assert torch.count_nonzero(b.dw_gu[int(e)]) == 0 and torch.count_nonzero(b.dw_d[int(e)]) == 0
+
+
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_mx_weight_codes_and_scales_bit_exact():
+    need_gpu()
+    from test_gpu_mx import scales_from_tiles
+    cfg = CASES["mx-ragged"]
+    b, inp, w_gu_b, w_d_b = _run(cfg)
+    wq = host(b.wq)
+    E, f, d = cfg.E, cfg.f, cfg.d
+    n, m = E * 2 * f * d, E * f * d
+    regions = []
+    off = 0
+    for elems in (n, n, m, m):
+        regions.append((wq[off:off + elems], wq[off + _a256(elems):off + _a256(elems) + elems // 32]))
+        off += _a256(elems) + _a256(elems // 32)
+    w_gu = synth.bf16_to_f32(w_gu_b).astype(np.float64)
+    w_d = synth.bf16_to_f32(w_d_b).astype(np.float64)
+    # W_gu along d, rows [E*2f]
+    c, s = mx.mx_quantize(w_gu.reshape(E * 2 * f, d))
+    assert np.array_equal(regions[0][0].reshape(E * 2 * f, d), c)
+    assert np.array_equal(scales_from_tiles(regions[0][1], E * 2 * f, d), s)
+    # W_gu along 2f, stored [E][d][2f]
+    c, s = mx.mx_quantize(np.swapaxes(w_gu, 1, 2).reshape(E * d, 2 * f))
+    assert np.array_equal(regions[1][0].reshape(E * d, 2 * f), c)
+    assert np.array_equal(scales_from_tiles(regions[1][1], E * d, 2 * f), s)
+    # W_d along f, rows [E*d]
+    c, s = mx.mx_quantize(w_d.reshape(E * d, f))
+    assert np.array_equal(regions[2][0].reshape(E * d, f), c)
+    assert np.array_equal(scales_from_tiles(regions[2][1], E * d, f), s)
+    # W_d along d, stored [E][f][d]
+    c, s = mx.mx_quantize(np.swapaxes(w_d, 1, 2).reshape(E * f, d))
+    assert np.array_equal(regions[3][0].reshape(E * f, d), c)
+    assert np.array_equal(scales_from_tiles(regions[3][1], E * f, d), s)
