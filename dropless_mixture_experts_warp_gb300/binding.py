@@ -72,6 +72,7 @@ SIGNATURES = {
     "moe_shared_mlp_fwd": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_shared_mlp_bwd": (ctypes.c_int32, [_D] + [_P] * 12),
     "moe_test_wait_timeout": (ctypes.c_int32, [_P, ctypes.c_int64, _P]),
+    "moe_gemm_bf16_pair": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
     "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -323,3 +324,8 @@ def moe_gemm_gate_up_dgrad_mx(dims, dgu, row_offsets, wq, mx_ws, dxp, dev_status
 def moe_gemm_gate_up_wgrad_mx(dims, dgu, xp, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
     return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(dgu), _ptr(xp), _ptr(row_offsets), _ptr(mx_ws),
                  _ptr(dw_gu), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_bf16_pair(A, B, C, M, N, K, a_layout, b_layout, dev_status, stream=None):
+    return _call("moe_gemm_bf16_pair", _ptr(A), _ptr(B), _ptr(C), M, N, K, a_layout, b_layout,
+                 _ptr(dev_status), _stream(stream))

@@ -122,6 +122,20 @@ float* workspace_dw_part(const moe_dims& d, void* ws) { return carve(d, ws).dw_p
 
 static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The CTA-pair kernel serves every product whose tile is at least 128 columns wide
+// (and, for the weight gradients, whose output rows come in 256-row pairs).
+static bool pair_ok(GemmKind kind, const GemmParams& p) {
+  if (p.BN < 128) return false;
+  if (kind == GEMM_KGROUP_STORE && p.M % 256 != 0) return false;
+  return true;
+}
+
+static cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
+                               const GemmParams& p, cudaStream_t s) {
+  if (pair_ok(kind, p)) return launch_gemm_pair(kind, a, b, p, s);
+  return bwd ? launch_gemm_bwd(kind, a, b, p, s) : launch_gemm_fwd(kind, a, b, p, s);
+}
+
 static GemmParams gemm_params() {
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -233,7 +247,7 @@ moe_status moe_gemm_gate_up(const moe_dims* dims, const moe_bf16* xp,
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets;
   p.b_rows_per_expert = 2 * d.f; p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_out = gu; p.h_out = h; p.status = dev_status;
-  return cuda_status(launch_gemm_fwd(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_best(GEMM_ROWS_SWIGLU_FWD, false, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_down(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets,
@@ -248,13 +262,13 @@ moe_status moe_gemm_down(const moe_dims* dims, const moe_bf16* h, const int32_t*
   const int bn = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
   CUtensorMap ta, tb;
   if (!make_map(&ta, h, d.f, R_cap, 64, BM) ||
-      !make_map(&tb, w_d, d.f, static_cast<uint64_t>(d.d) * d.E, 64, bn))
+      !make_map(&tb, w_d, d.f, static_cast<uint64_t>(d.d) * d.E, 64, bn / 2))   // CTA-pair boxes
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets;
   p.b_rows_per_expert = d.d; p.m_fastest = (R / d.E <= d.d) ? 1 : 0;
   p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
-  return cuda_status(launch_gemm_fwd(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_gemm_pair(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* xp,
@@ -322,7 +336,7 @@ moe_status moe_gemm_down_dgrad(const moe_dims* dims, const moe_bf16* dy_rows,
   p.b_k_per_expert = d.d; p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu; p.dgu_out = dgu; p.dw_part = c.dw_part;
   p.dw_stride = d.f / bn; p.status = dev_status;
-  if (launch_gemm_bwd(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_best(GEMM_ROWS_SWIGLU_BWD, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(launch_dw_reduce(c.dw_part, d.f / bn, row_offsets, d.E, dw_rows,
                                       static_cast<int>(R_cap), s));
 }
@@ -344,7 +358,7 @@ moe_status moe_gemm_down_wgrad(const moe_dims* dims, const moe_bf16* dy_rows, co
   p.BN = bn_for(d.f); p.N = d.f; p.M = d.d; p.E = d.E; p.row_offsets = row_offsets;
   p.m_fastest = (d.d <= d.f) ? 1 : 0; p.out = dw_d; p.ldo = d.f; p.row_limit = d.d;
   p.status = dev_status;
-  return cuda_status(launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_best(GEMM_KGROUP_STORE, true, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_gate_up_dgrad(const moe_dims* dims, const moe_bf16* dgu,
@@ -366,7 +380,7 @@ moe_status moe_gemm_gate_up_dgrad(const moe_dims* dims, const moe_bf16* dgu,
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets;
   p.b_k_per_expert = 2 * d.f; p.m_fastest = (R / d.E <= d.d) ? 1 : 0;
   p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
-  return cuda_status(launch_gemm_bwd(GEMM_ROWS_STORE_BMN, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_best(GEMM_ROWS_STORE_BMN, true, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_gate_up_wgrad(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
@@ -386,7 +400,7 @@ moe_status moe_gemm_gate_up_wgrad(const moe_dims* dims, const moe_bf16* dgu, con
   p.BN = bn_for(d.d) == 64 ? 128 : bn_for(d.d); p.N = d.d; p.M = 2 * d.f; p.E = d.E;
   p.row_offsets = row_offsets; p.m_fastest = (2 * d.f <= d.d) ? 1 : 0; p.out = dw_gu; p.ldo = d.d;
   p.row_limit = 2 * d.f; p.status = dev_status;
-  return cuda_status(launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_best(GEMM_KGROUP_STORE, true, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* xp,
@@ -429,14 +443,14 @@ moe_status moe_shared_mlp_fwd(const moe_dims* dims, const moe_bf16* x, const moe
   GemmParams p = gemm_params();
   p.BN = bn1; p.N = fs; p.K = d.d; p.M = d.T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1;
   p.f = fs; p.row_limit = d.T; p.gu_out = gu_s; p.h_out = h_s; p.status = dev_status;
-  if (launch_gemm_fwd(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_best(GEMM_ROWS_SWIGLU_FWD, false, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // down
   const int bn2 = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
-  if (!make_map(&ta, h_s, fs, d.T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, bn2)) return MOE_ERR_CUDA;
+  if (!make_map(&ta, h_s, fs, d.T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, bn2 / 2)) return MOE_ERR_CUDA;
   p = gemm_params();
   p.BN = bn2; p.N = d.d; p.K = fs; p.M = d.T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
   p.out = y_s; p.ldo = d.d; p.row_limit = d.T; p.status = dev_status;
-  return cuda_status(launch_gemm_fwd(GEMM_ROWS_STORE, ta, tb, p, s));
+  return cuda_status(launch_gemm_pair(GEMM_ROWS_STORE, ta, tb, p, s));
 }
 
 moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_gu_s,
@@ -472,14 +486,14 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
     p = gemm_params();
     p.BN = bn_for(fs); p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_k_per_expert = d.d; p.m_fastest = 1;
     p.f = fs; p.row_limit = T; p.gu_in = gu_s; p.dgu_out = dgu_s; p.status = dev_status;
-    if (launch_gemm_bwd(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_best(GEMM_ROWS_SWIGLU_BWD, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // dW_d_s = dy^T h_s  ([d, fs], K = T tokens)
   if (!make_map(&ta, dy_, d.d, rows, 64, 64) || !make_map(&tb, h_, fs, rows, 64, 64)) return MOE_ERR_CUDA;
   p = gemm_params();
   p.BN = bn_for(fs); p.N = fs; p.M = d.d; p.K = T; p.E = 1; p.m_fastest = (d.d <= fs) ? 1 : 0;
   p.out = dw_d_s; p.ldo = fs; p.row_limit = d.d; p.status = dev_status;
-  if (launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_best(GEMM_KGROUP_STORE, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (T > 0) {
     // dx_s = dgu_s W_gu_s (MN-major B)
     const int bnd = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
@@ -488,7 +502,7 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
     p = gemm_params();
     p.BN = bnd; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_k_per_expert = 2 * fs; p.m_fastest = 1;
     p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
-    if (launch_gemm_bwd(GEMM_ROWS_STORE_BMN, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_best(GEMM_ROWS_STORE_BMN, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // dW_gu_s = dgu_s^T x  ([2fs, d], K = T tokens)
   if (!make_map(&ta, dgu_, 2ll * fs, rows, 64, 64) || !make_map(&tb, x_, d.d, rows, 64, 64))
@@ -497,7 +511,7 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
   p.BN = bn_for(d.d) == 64 ? 128 : bn_for(d.d); p.N = d.d; p.M = 2 * fs; p.K = T; p.E = 1;
   p.m_fastest = (2 * fs <= d.d) ? 1 : 0; p.out = dw_gu_s; p.ldo = d.d; p.row_limit = 2 * fs;
   p.status = dev_status;
-  return cuda_status(launch_gemm_bwd(GEMM_KGROUP_STORE, ta, tb, p, s));
+  return cuda_status(launch_best(GEMM_KGROUP_STORE, true, ta, tb, p, s));
 }
 
 moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
@@ -521,6 +535,26 @@ moe_status moe_check_status(const int32_t* dev_status, void* stream) {
   if (cudaMemcpy(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
   return static_cast<moe_status>(v);
+}
+
+moe_status moe_gemm_bf16_pair(const moe_bf16* A, const moe_bf16* B, moe_bf16* C, int32_t M, int32_t N,
+                              int32_t K, int32_t a_layout, int32_t b_layout, int32_t* dev_status, void* stream) {
+  if (!A || !B || !C || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (M < 1 || N < 128 || K < 64 || N % 128 || K % 64) return MOE_ERR_UNSUPPORTED;
+  if ((a_layout != 0 && a_layout != 1) || (b_layout != 0 && b_layout != 1)) return MOE_ERR_INVALID_ARG;
+  if (a_layout == 1 && M % 8) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MOE_ERR_ALIGNMENT;
+  const int bn = N % 256 == 0 ? 256 : 128;
+  CUtensorMap ta, tb;
+  bool ok = a_layout == 0 ? make_map(&ta, A, K, M, 64, BM) : make_map(&ta, A, M, K, 64, 64);
+  ok = ok && (b_layout == 0 ? make_map(&tb, B, K, N, 64, bn / 2) : make_map(&tb, B, N, K, 64, 64));
+  if (!ok) return MOE_ERR_CUDA;
+  GemmParams p = gemm_params();
+  p.BN = bn; p.N = N; p.K = K; p.M = M; p.E = 1; p.row_offsets = nullptr;
+  p.m_fastest = 1; p.out = C; p.ldo = N; p.row_limit = M; p.status = dev_status;
+  GemmKind kind = a_layout == 0 ? (b_layout == 0 ? GEMM_ROWS_STORE : GEMM_ROWS_STORE_BMN)
+                                : (b_layout == 0 ? GEMM_DENSE_AMN_BK : GEMM_DENSE_AMN_BMN);
+  return cuda_status(launch_gemm_pair(kind, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_test_wait_timeout(int32_t* dev_status, int64_t limit_cycles, void* stream) {

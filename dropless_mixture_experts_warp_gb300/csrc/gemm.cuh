@@ -4,8 +4,9 @@
 //   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage ring
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator;
 //               owns the TMEM allocation (two accumulators of 256 fp32 columns)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU / SwiGLU'
-//               arithmetic, bf16 stores.  Warp w reads TMEM lanes 32*(w%4)..+31.
+//   warps 2..    epilogue (4 warps, 8 for the SwiGLU' epilogue): tcgen05.ld of the
+//               accumulator, fused SwiGLU / SwiGLU' arithmetic, bf16 stores.  Warp w
+//               reads TMEM lanes 32*(w%4)..+31; with 8 warps, w and w+4 split the columns.
 // The two accumulators let the epilogue of one tile overlap the mainloop of the
 // next.  Work tiles come from a device-side schedule derived from row_offsets, so
 // the host never waits for the per-expert counts.
@@ -35,7 +36,10 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES_MAX;
 constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_STRIDE = 256;
-constexpr int GEMM_THREADS = 192;
+// Epilogue warps: 8 for the SwiGLU' epilogue (two per TMEM lane quarter, splitting
+// the columns), 4 otherwise.  Block = producer warp + MMA warp + epilogue warps.
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == 2 ? 8 : 4; }
+__host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int MAX_EXPERTS = 1024;
 constexpr long long WAIT_LIMIT_CYCLES = 1ll << 31;  // about one second
 
@@ -124,16 +128,30 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
   return c;
 }
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoidf_(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
-// Epilogue of one tile for one thread (one accumulator row): reads the fp32
-// accumulator columns from TMEM (32 at a time) and applies the fused EPI step.
-// Every lane of the warp must call it (tcgen05.ld is warp-wide).
-template <int EPI>
-__device__ __forceinline__ void tile_epilogue(const GemmParams& p, const TileCoord& c, uint32_t tbase,
-                                              long long row, bool row_ok, int BN) {
+// Hand-off of the dw partials between the two epilogue warps of a TMEM lane
+// quarter (second half -> first half), through mbarriers so every wait is bounded.
+struct DwHandoff {
+  float* s_dw;             // [BM] partials of the second half
+  uint64_t* full;          // [4] second half has written s_dw
+  uint64_t* empty;         // [4] first half has read it
+  uint32_t* phase;         // this thread's phase bit
+  volatile int* abort_flag;
+};
+
+// Epilogue of one tile for one thread (one accumulator row, half of the columns):
+// reads fp32 accumulator columns from TMEM (32 at a time) and applies the fused EPI
+// step.  The two epilogue warps of a TMEM lane quarter split the tile's columns
+// (`half` 0 or 1).  Every lane of both warps must call it (tcgen05.ld and the named
+// barrier are collective).
+template <int EPI, int NH = epi_warps(EPI) / 4>
+__device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoord& c, uint32_t tbase,
+                                              long long row, bool row_ok, int BN, int half, int quarter,
+                                              int row_in_tile, const DwHandoff& hand) {
   if (EPI == EPI_STORE) {
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    const int cb = half * (BN / NH);
+    for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
       uint32_t r[32];
       if (c.kblocks > 0) {
         tmem_ld32(tbase + c0, r);
@@ -156,14 +174,16 @@ __device__ __forceinline__ void tile_epilogue(const GemmParams& p, const TileCoo
       }
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
-    // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2
-    const int half = BN / 2;
+    // columns [0, BN/2) hold G, [BN/2, BN) hold U for h columns out_col .. +BN/2;
+    // this half takes h columns [half*BN/4, (half+1)*BN/4)
+    const int hw = BN / 2;
     const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
     const long long ld2 = 2ll * p.f;
-    for (int c0 = 0; c0 < half; c0 += 32) {
+    const int cb = half * (hw / NH);
+    for (int c0 = cb; c0 < cb + hw / NH; c0 += 32) {
       uint32_t g[32], u[32];
       tmem_ld32(tbase + c0, g);
-      tmem_ld32(tbase + half + c0, u);
+      tmem_ld32(tbase + hw + c0, u);
       tmem_wait_ld();
       if (row_ok) {
         uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + c.out_col + c0);
@@ -187,25 +207,30 @@ __device__ __forceinline__ void tile_epilogue(const GemmParams& p, const TileCoo
         }
       }
     }
-  } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN
+  } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN; this half: BN/2 of them
     const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
     const long long ld2 = 2ll * p.f;
     float dwp = 0.0f;
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    const int cb = half * (BN / NH);
+    for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
+      // the saved G and U are fetched before the accumulator so both latencies overlap
+      uint4 g4[4], u4[4];
+      if (row_ok) {
+        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
+        const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) { g4[v] = gsrc[v]; u4[v] = usrc[v]; }
+      }
       uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_wait_ld();
       if (row_ok) {
-        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
-        const uint4* usrc =
-            reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
         uint4* gdst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + c.out_col + c0);
         uint4* udst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + p.f + c.out_col + c0);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 g4 = gsrc[v], u4 = usrc[v];
-          const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-          const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+          const uint32_t gw[4] = {g4[v].x, g4[v].y, g4[v].z, g4[v].w};
+          const uint32_t uw[4] = {u4[v].x, u4[v].y, u4[v].z, u4[v].w};
           float dg[8], du[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -226,12 +251,33 @@ __device__ __forceinline__ void tile_epilogue(const GemmParams& p, const TileCoo
         }
       }
     }
-    if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
+    if (NH == 1) {
+      if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
+    } else if (p.dw_part) {
+      // the two halves' partials, combined in a fixed order: first half + second half
+      const int lane = row_in_tile & 31;
+      const uint32_t ph = *hand.phase;
+      *hand.phase ^= 1u;
+      if (half == 1) {
+        if (!mbar_wait_bounded(&hand.empty[quarter], ph ^ 1, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+          return false;
+        hand.s_dw[row_in_tile] = dwp;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hand.full[quarter]);
+      } else {
+        if (!mbar_wait_bounded(&hand.full[quarter], ph, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+          return false;
+        if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp + hand.s_dw[row_in_tile];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hand.empty[quarter]);
+      }
+    }
   }
+  return true;
 }
 
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
@@ -240,6 +286,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t dw_full_bar[4];
+  __shared__ __align__(8) uint64_t dw_empty_bar[4];
+  __shared__ float s_dw[BM];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
@@ -257,8 +306,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
+    for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
     s_abort = 0;
     fence_mbar_init();
   }
@@ -365,7 +415,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, dw_phase = 0;
+    const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES))
@@ -375,7 +426,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const long long row = c.out_row + row_in_tile;
       const bool row_ok = row < p.row_limit;
 
-      tile_epilogue<EPI>(p, c, tbase, row, row_ok, BN);
+      if (!tile_epilogue<EPI>(p, c, tbase, row, row_ok, BN, (warp - 2) >> 2, q, row_in_tile, hand)) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);

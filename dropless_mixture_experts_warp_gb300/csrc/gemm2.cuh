@@ -1,0 +1,250 @@
+// Persistent grouped GEMM over CTA pairs (tcgen05 cta_group::2, M = 256 per MMA).
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256 x BN tile: each CTA
+// holds 128 rows of A and half of B's BN rows in its shared memory and receives its
+// 128 rows of the accumulator in its own TMEM.  Compared with the single-CTA kernel
+// each SM stages half as many B bytes per FLOP, so a stage is 32 KB and six of them
+// fit, which hides more load latency.
+//   warp 0 (both CTAs)  TMA producer for this CTA's halves; completions are counted on
+//                       the leader CTA's full barrier (.cta_group::2 loads)
+//   warp 1 (leader)     issues the pair's MMAs; commits multicast to both CTAs
+//   warps 2..           epilogue on this CTA's 128 accumulator rows (shared epilogue)
+// Row tiles of the grouped (ragged-M) mode stay inside an expert: an expert with an
+// odd number of 128-row tiles ends with a pair whose second half is discarded, so
+// the epilogue never writes past the expert's segment.  For the gate/up GEMM the
+// leader holds the gate rows and the peer the up rows of W_gu, so the accumulator's
+// columns are [G | U] as in the single-CTA kernel.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace moe {
+
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;                // 16 KB
+constexpr int P_B_BYTES_MAX = 128 * BK * 2;           // half of a 256-row B tile
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024;
+
+struct PairTile {
+  TileCoord c;
+  long long row_end;  // rows at or beyond this are not stored
+};
+
+// s_pt[e]: first pair tile of expert e (SCHED_ROWS); rank: 0 (leader) or 1.
+template <int SCHED, int EPI, bool B_MN>
+__device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_ro, const int* s_pt, int E,
+                                              int n_tiles, int tile, int rank) {
+  PairTile t;
+  TileCoord& c = t.c;
+  const int half_n = p.BN / 2;
+  if (SCHED == SCHED_ROWS) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pt[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int local = tile - s_pt[e];
+    const int mt2 = ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2;
+    if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
+    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    c.e = e;
+    c.kblocks = p.K / BK;
+    c.a_m = s_ro[e] + c.m * 2 * BM + rank * BM;
+    c.a_k = 0;
+    c.out_col = (EPI == EPI_SWIGLU_FWD) ? c.n * half_n : c.n * p.BN;
+    if (EPI == EPI_SWIGLU_FWD)  // leader: gate rows, peer: up rows
+      c.b_n = e * p.b_rows_per_expert + c.out_col + rank * p.f;
+    else
+      c.b_n = (B_MN ? 0 : e * p.b_rows_per_expert) + c.out_col + rank * half_n;
+    c.b_k = B_MN ? e * p.b_k_per_expert : 0;
+    c.out_row = c.a_m;
+    c.out_base = 0;
+    t.row_end = s_ro[e + 1] < p.row_limit ? s_ro[e + 1] : p.row_limit;
+  } else {
+    const int mt2 = p.M / (2 * BM);
+    const int per = mt2 * n_tiles;
+    const int e = tile / per;
+    const int local = tile - e * per;
+    if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
+    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    c.e = e;
+    c.kblocks = (s_ro[e + 1] - s_ro[e]) / BK;
+    c.a_m = c.m * 2 * BM + rank * BM;
+    c.a_k = s_ro[e];
+    c.out_col = c.n * p.BN;
+    c.b_n = c.out_col + rank * half_n;
+    c.b_k = s_ro[e];
+    c.out_row = c.a_m;
+    c.out_base = static_cast<long long>(e) * p.M * p.N;
+    t.row_end = p.row_limit;
+  }
+  return t;
+}
+
+template <int SCHED, int EPI, bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const GemmParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[P_STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[P_STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t dw_full_bar[4];
+  __shared__ __align__(8) uint64_t dw_empty_bar[4];
+  __shared__ float s_dw[BM];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_ro[MAX_EXPERTS + 1];
+  __shared__ int s_pt[MAX_EXPERTS + 1];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int E = p.row_offsets ? p.E : 1;
+  const int dense_rows = (SCHED == SCHED_KGROUP) ? (p.K + BK - 1) / BK * BK : (p.M + BM - 1) / BM * BM;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x)
+    s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
+  const int BN = p.BN;  // 128 or 256
+  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // pair tiles per expert, exclusive prefix (E <= 1024, once per launch)
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      s_pt[e] = run;
+      run += ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2 * n_tiles;
+    }
+    s_pt[E] = run;
+    for (int s = 0; s < P_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 2 * epi_warps(EPI)); }
+    mbar_init(&drain_bar, 1);
+    for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 1) { tmem_alloc_pair(&s_tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int total = (SCHED == SCHED_ROWS) ? s_pt[E] : E * (p.M / (2 * BM)) * n_tiles;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t cta_tx = P_A_BYTES + (BN / 2) * BK * 2;
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
+        const TileCoord& c = t.c;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          uint8_t* sa = smem + stage * P_STAGE_BYTES;
+          uint8_t* sb = sa + P_A_BYTES;
+          const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);  // the leader's
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&full_bar[stage], 2 * cta_tx);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          const int k0 = kb * BK;
+          if (!A_MN) {
+            tma_load_2d_pair(sa, &tmA, bar, c.a_k + k0, c.a_m);
+          } else {
+            tma_load_2d_pair(sa, &tmA, bar, c.a_m, c.a_k + k0);
+            tma_load_2d_pair(sa + 8192, &tmA, bar, c.a_m + 64, c.a_k + k0);
+          }
+          if (!B_MN) {
+            tma_load_2d_pair(sb, &tmB, bar, c.b_k + k0, c.b_n);
+          } else {
+            for (int i = 0; i < BN / 128; ++i)
+              tma_load_2d_pair(sb + i * 8192, &tmB, bar, c.b_n + 64 * i, c.b_k + k0);
+          }
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (rank == 0)
+        for (int s = 0; s < P_STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_drain(&full_bar[s], (armed_parity >> s) & 1u, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_bf16(2 * BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, 0);
+        if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = 0; kb < t.c.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, p.status,
+                                 WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * P_STAGE_BYTES);
+          const uint32_t sb = sa + P_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
+          if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&tfull_bar[acc], 0x3);      // both halves of the accumulator ready
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      tc_commit_pair(&drain_bar);
+      mbar_drain(&drain_bar, 0, WAIT_LIMIT_CYCLES);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0, dw_phase = 0;
+    const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
+    for (int tile = pair; tile < total; tile += npairs) {
+      const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
+      const long long row = t.c.out_row + row_in_tile;
+      if (!tile_epilogue<EPI>(p, t.c, tbase, row, row < t.row_end, BN, (warp - 2) >> 2, q, row_in_tile, hand))
+        break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while the other may still signal its barriers
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+}  // namespace moe

@@ -10,7 +10,7 @@ static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const
   auto kern = grouped_gemm_mx_kernel<SCHED, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MX_SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), GEMM_THREADS, MX_SMEM_BYTES, stream>>>(a, b, p);
+  kern<<<num_sms(), gemm_threads(EPI), MX_SMEM_BYTES, stream>>>(a, b, p);
   count_launch();
   return cudaGetLastError();
 }

@@ -1,7 +1,7 @@
 // Persistent grouped GEMM with MXFP8 operands on tcgen05 (kind::mxf8f6f4.block_scale).
 //
 // Same roles and schedule as the bf16 kernel (gemm.cuh): warp 0 loads, warp 1 issues,
-// warps 2..5 run the shared epilogue.  Differences:
+// the warps after them run the shared epilogue.  Differences:
 //   * operands are E4M3 codes, both K-major, 128 codes (128 bytes) per stage row;
 //   * each stage also carries the E8M0 scale tiles of its A rows (512 B) and B rows
 //     (512 B per 128 rows), fetched with contiguous bulk copies; the MMA warp moves
@@ -28,7 +28,7 @@ constexpr int MX_SF_TMEM_COL = 256;                         // first scale-facto
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
 
 template <int SCHED, int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
@@ -37,6 +37,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t dw_full_bar[4];
+  __shared__ __align__(8) uint64_t dw_empty_bar[4];
+  __shared__ float s_dw[BM];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
@@ -53,8 +56,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   if (threadIdx.x == 0) {
     for (int s = 0; s < MX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
+    for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
     s_abort = 0;
     fence_mbar_init();
   }
@@ -163,14 +167,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, dw_phase = 0;
+    const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const long long row = c.out_row + row_in_tile;
-      tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN);
+      if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile, hand))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);

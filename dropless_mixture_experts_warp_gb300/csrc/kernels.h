@@ -3,6 +3,7 @@
 
 #include "common.cuh"
 #include "gemm.cuh"
+#include "gemm2.cuh"
 
 namespace moe {
 
@@ -60,6 +61,22 @@ cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
                             const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, cudaStream_t stream);
+// The same products on CTA pairs (M = 256 per MMA; K-major B tensor maps with boxes of
+// BN/2 rows; BN 128 or 256; SCHED_KGROUP needs p.M % 256 == 0).
+cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                             const GemmParams& p, cudaStream_t stream);
+
+template <int SCHED, int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                               cudaStream_t stream) {
+  auto kern = grouped_gemm_pair_kernel<SCHED, EPI, A_MN, B_MN>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  const int grid = num_sms() & ~1;  // whole CTA pairs
+  kern<<<grid, gemm_threads(EPI), P_SMEM_BYTES, stream>>>(a, b, p);
+  count_launch();
+  return cudaGetLastError();
+}
 
 // MXFP8 variants (both operands K-major E4M3 codes + scale tiles); kind is one of
 // GEMM_ROWS_SWIGLU_FWD, GEMM_ROWS_STORE, GEMM_ROWS_SWIGLU_BWD, GEMM_KGROUP_STORE.
@@ -82,7 +99,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const Gemm
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(a, b, p);
+  kern<<<num_sms(), gemm_threads(EPI), GEMM_SMEM_BYTES, stream>>>(a, b, p);
   count_launch();
   return cudaGetLastError();
 }

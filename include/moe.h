@@ -306,6 +306,14 @@ size_t moe_noalloc_scratch_bytes(void);
 moe_status moe_check_status(const int32_t* dev_status, void* stream);
 
 /*
+ * The same dense GEMM as moe_gemm_bf16 on the CTA-pair kernel (tcgen05 cta_group::2,
+ * M = 256 per MMA across two SMs), which the layer uses where shapes allow.
+ * N % 128 == 0, K % 64 == 0.
+ */
+moe_status moe_gemm_bf16_pair(const moe_bf16* A, const moe_bf16* B, moe_bf16* C, int32_t M, int32_t N,
+                              int32_t K, int32_t a_layout, int32_t b_layout, int32_t* dev_status, void* stream);
+
+/*
  * Test hook for failure detection: one thread waits, through the same bounded
  * mbarrier wait as the GEMM pipeline, on a barrier that nothing arrives on.  After
  * limit_cycles (1 .. 2^32) it gives up and writes MOE_ERR_TIMEOUT to dev_status; the
