@@ -248,7 +248,10 @@ def run_native(args, cfg):
         else:
             B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
         mark(2)
-        if cfg.f_shared:
+        if cfg.f_shared and mx8:
+            B.moe_mx_quantize_shared_weights(dm, inp["w_gu_s"], inp["w_d_s"], b.wq_s, stream)
+            B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
+        elif cfg.f_shared:
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
         B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
         B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
@@ -272,7 +275,10 @@ def run_native(args, cfg):
             mark(6)
             B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
         mark(7)
-        if cfg.f_shared:
+        if cfg.f_shared and mx8:
+            B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s,
+                                    b.dw_d_s, b.status, stream)
+        elif cfg.f_shared:
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
                                  b.dw_gu_s, b.dw_d_s, b.status, stream)
         B.moe_combine_fwd(dm, b.dxp, b.token_to_row, b.dx_s, b.dx, stream)

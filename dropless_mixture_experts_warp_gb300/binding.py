@@ -73,6 +73,11 @@ SIGNATURES = {
     "moe_shared_mlp_bwd": (ctypes.c_int32, [_D] + [_P] * 12),
     "moe_test_wait_timeout": (ctypes.c_int32, [_P, ctypes.c_int64, _P]),
     "moe_gemm_bf16_pair": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_mx_shared_weights_size": (ctypes.c_size_t, [_D]),
+    "moe_mx_shared_workspace_size": (ctypes.c_size_t, [_D]),
+    "moe_mx_quantize_shared_weights": (ctypes.c_int32, [_D, _P, _P, _P, _P]),
+    "moe_shared_mlp_fwd_mx": (ctypes.c_int32, [_D] + [_P] * 8),
+    "moe_shared_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 12),
     "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
     "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -329,3 +334,28 @@ def moe_gemm_gate_up_wgrad_mx(dims, dgu, xp, row_offsets, mx_ws, dw_gu, dev_stat
 def moe_gemm_bf16_pair(A, B, C, M, N, K, a_layout, b_layout, dev_status, stream=None):
     return _call("moe_gemm_bf16_pair", _ptr(A), _ptr(B), _ptr(C), M, N, K, a_layout, b_layout,
                  _ptr(dev_status), _stream(stream))
+
+
+def moe_mx_shared_weights_size(dims) -> int:
+    return lib().moe_mx_shared_weights_size(_d(dims))
+
+
+def moe_mx_shared_workspace_size(dims) -> int:
+    return lib().moe_mx_shared_workspace_size(_d(dims))
+
+
+def moe_mx_quantize_shared_weights(dims, w_gu_s, w_d_s, wq_s, stream=None):
+    return _call("moe_mx_quantize_shared_weights", _d(dims), _ptr(w_gu_s), _ptr(w_d_s), _ptr(wq_s),
+                 _stream(stream))
+
+
+def moe_shared_mlp_fwd_mx(dims, x, wq_s, mx_ws_s, gu_s, h_s, y_s, dev_status, stream=None):
+    return _call("moe_shared_mlp_fwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(h_s),
+                 _ptr(y_s), _ptr(dev_status), _stream(stream))
+
+
+def moe_shared_mlp_bwd_mx(dims, x, wq_s, mx_ws_s, gu_s, h_s, dy, dgu_s, dx_s, dw_gu_s, dw_d_s, dev_status,
+                          stream=None):
+    return _call("moe_shared_mlp_bwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(h_s),
+                 _ptr(dy), _ptr(dgu_s), _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status),
+                 _stream(stream))

@@ -333,3 +333,193 @@ moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, 
 }
 
 }  // extern "C"
+
+// ============================================================================ shared expert
+
+namespace moe {
+
+// Quantised shared-expert weights: W_gu_s along d ([2fs][d]) and along 2fs ([d][2fs]),
+// W_d_s along fs ([d][fs]) and along d ([fs][d]).
+static MxWeights carve_shared_weights(const moe_dims& d, void* base) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t n = 2ull * d.f_shared * d.d, m = static_cast<size_t>(d.f_shared) * d.d;
+  MxWeights w;
+  w.gu_rows = carve_op(p, n);
+  w.gu_cols = carve_op(p, n);
+  w.d_rows = carve_op(p, m);
+  w.d_cols = carve_op(p, m);
+  return w;
+}
+
+// Quantised shared-expert activations over the T tokens.
+static MxActs carve_shared_acts(const moe_dims& d, void* base) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  const size_t td = static_cast<size_t>(d.T) * d.d, tf = static_cast<size_t>(d.T) * d.f_shared;
+  MxActs a;
+  a.xp_rows = carve_op(p, td);
+  a.xp_cols = carve_op(p, td);
+  a.h_rows = carve_op(p, tf);
+  a.h_cols = carve_op(p, tf);
+  a.dy_rows = carve_op(p, td);
+  a.dy_cols = carve_op(p, td);
+  a.dgu_rows = carve_op(p, 2 * tf);
+  a.dgu_cols = carve_op(p, 2 * tf);
+  return a;
+}
+
+static moe_status mx_shared_common(const moe_dims* dims) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  if (dims->f_shared <= 0) return MOE_ERR_INVALID_ARG;
+  if (dims->f_shared % 128 != 0 || dims->T % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_mx_shared_weights_size(const moe_dims* dims) {
+  if (mx_shared_common(dims) != MOE_OK) return 0;
+  const size_t n = 2ull * dims->f_shared * dims->d, m = static_cast<size_t>(dims->f_shared) * dims->d;
+  return 2 * op_bytes(n) + 2 * op_bytes(m);
+}
+
+size_t moe_mx_shared_workspace_size(const moe_dims* dims) {
+  if (mx_shared_common(dims) != MOE_OK) return 0;
+  const size_t td = static_cast<size_t>(dims->T) * dims->d, tf = static_cast<size_t>(dims->T) * dims->f_shared;
+  return 4 * op_bytes(td) + 2 * op_bytes(tf) + 2 * op_bytes(2 * tf);
+}
+
+moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* w_gu_s, const moe_bf16* w_d_s,
+                                          void* wq_s, void* stream) {
+  moe_status st = mx_shared_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!w_gu_s || !w_d_s || !wq_s) return MOE_ERR_INVALID_ARG;
+  if (!al16(w_gu_s) || !al16(w_d_s) || !al16(wq_s)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_shared_weights(d, wq_s);
+  const int fs = d.f_shared;
+  if (launch_quant_rows(w_gu_s, 2ll * fs, d.d, d.d, nullptr, w.gu_rows.codes, w.gu_rows.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(w_gu_s, 1, 2ll * fs, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s) != cudaSuccess ||
+      launch_quant_rows(w_d_s, d.d, fs, fs, nullptr, w.d_rows.codes, w.d_rows.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(w_d_s, 1, d.d, fs, nullptr, w.d_cols.codes, w.d_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
+                                 moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s, int32_t* dev_status, void* stream) {
+  moe_status st = mx_shared_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (d.T == 0) return MOE_OK;
+  if (!x || !wq_s || !mx_ws_s || !gu_s || !h_s || !y_s || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(h_s) || !al16(y_s))
+    return MOE_ERR_ALIGNMENT;
+  const int fs = d.f_shared, T = d.T;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
+  MxActs a = carve_shared_acts(d, mx_ws_s);
+  CUtensorMap ta, tb;
+  GemmParams p;
+  if (launch_quant_rows(x, T, d.d, d.d, nullptr, a.xp_rows.codes, a.xp_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!make_tensor_map_u8(&ta, a.xp_rows.codes, d.d, T, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.gu_rows.codes, d.d, 2ll * fs, 128, 128))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1; p.f = fs;
+  p.row_limit = T; p.gu_out = gu_s; p.h_out = h_s; p.status = dev_status;
+  p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_quant_rows(h_s, T, fs, fs, nullptr, a.h_rows.codes, a.h_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int bn = bn_mx(d.d);
+  if (!make_tensor_map_u8(&ta, a.h_rows.codes, fs, T, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.d_rows.codes, fs, d.d, 128, bn))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = bn; p.N = d.d; p.K = fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.out = y_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
+  p.sfa = a.h_rows.sf; p.sfb = w.d_rows.sf; p.a_sf_ktiles = fs / 128; p.b_sf_ktiles = fs / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+}
+
+moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
+                                 const moe_bf16* gu_s, const moe_bf16* h_s, const moe_bf16* dy, moe_bf16* dgu_s,
+                                 moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
+                                 void* stream) {
+  moe_status st = mx_shared_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const int fs = d.f_shared, T = d.T;
+  if (!wq_s || !dw_gu_s || !dw_d_s || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {  // no token: the shared weights get zero gradients
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dw_gu_s, 0, 2ull * fs * d.d * 2, s) != cudaSuccess ||
+        cudaMemsetAsync(dw_d_s, 0, static_cast<size_t>(fs) * d.d * 2, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (!x || !mx_ws_s || !gu_s || !h_s || !dy || !dgu_s || !dx_s) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(h_s) || !al16(dy) || !al16(dgu_s) ||
+      !al16(dx_s) || !al16(dw_gu_s) || !al16(dw_d_s))
+    return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
+  MxActs a = carve_shared_acts(d, mx_ws_s);
+  CUtensorMap ta, tb;
+  GemmParams p;
+  // dH = dy W_d_s with the SwiGLU' epilogue (weight 1, no dw)
+  if (launch_quant_rows(dy, T, d.d, d.d, nullptr, a.dy_rows.codes, a.dy_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int bn = bn_mx(fs);
+  if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, T, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.d_cols.codes, d.d, fs, 128, bn))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = 1; p.f = fs;
+  p.row_limit = T; p.gu_in = gu_s; p.dgu_out = dgu_s; p.status = dev_status;
+  p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dW_d_s = dy^T h_s (K = T)
+  if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(h_s, 1, T, fs, nullptr, a.h_cols.codes, a.h_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!make_tensor_map_u8(&ta, a.dy_cols.codes, T, d.d, 128, BM) ||
+      !make_tensor_map_u8(&tb, a.h_cols.codes, T, fs, 128, bn))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = bn; p.N = fs; p.M = d.d; p.K = T; p.E = 1; p.m_fastest = (d.d <= fs) ? 1 : 0;
+  p.out = dw_d_s; p.ldo = fs; p.row_limit = d.d; p.status = dev_status;
+  p.sfa = a.dy_cols.sf; p.sfb = a.h_cols.sf; p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
+  if (launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dx_s = dgu_s W_gu_s (K = 2fs)
+  if (launch_quant_rows(dgu_s, T, 2 * fs, 2ll * fs, nullptr, a.dgu_rows.codes, a.dgu_rows.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  bn = bn_mx(d.d);
+  if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * fs, T, 128, BM) ||
+      !make_tensor_map_u8(&tb, w.gu_cols.codes, 2ll * fs, d.d, 128, bn))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = bn; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
+  p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
+  if (launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dW_gu_s = dgu_s^T x (K = T)
+  if (launch_quant_cols_t(dgu_s, 1, T, 2 * fs, nullptr, a.dgu_cols.codes, a.dgu_cols.sf, s) != cudaSuccess ||
+      launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!make_tensor_map_u8(&ta, a.dgu_cols.codes, T, 2ll * fs, 128, BM) ||
+      !make_tensor_map_u8(&tb, a.xp_cols.codes, T, d.d, 128, bn))
+    return MOE_ERR_CUDA;
+  p = mx_params();
+  p.BN = bn; p.N = d.d; p.M = 2 * fs; p.K = T; p.E = 1; p.m_fastest = (2 * fs <= d.d) ? 1 : 0;
+  p.out = dw_gu_s; p.ldo = d.d; p.row_limit = 2 * fs; p.status = dev_status;
+  p.sfa = a.dgu_cols.sf; p.sfb = a.xp_cols.sf; p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+}
+
+}  // extern "C"

@@ -52,6 +52,8 @@ class Buffers:
     # MXFP8 path (dims.prec == mxfp8): quantised weights and activation scratch
     wq: torch.Tensor = None
     mx_ws: torch.Tensor = None
+    wq_s: torch.Tensor = None
+    mx_ws_s: torch.Tensor = None
 
 
 def dims_of(T, d, f, E, k, f_shared=0, score="softmax", prec="bf16") -> B.moe_dims:
@@ -75,6 +77,10 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
     if dims.prec == 1:
         shared["wq"] = torch.empty(B.moe_mx_weights_size(dims), dtype=torch.uint8, device=device)
         shared["mx_ws"] = torch.empty(B.moe_mx_workspace_size(dims), dtype=torch.uint8, device=device)
+        if dims.f_shared:
+            shared["wq_s"] = torch.empty(B.moe_mx_shared_weights_size(dims), dtype=torch.uint8, device=device)
+            shared["mx_ws_s"] = torch.empty(max(1, B.moe_mx_shared_workspace_size(dims)), dtype=torch.uint8,
+                                            device=device)
     return Buffers(**shared,
         dims=dims, rows=rows,
         topk_idx=e(T, k, dt=i32), topk_w=e(T, k, dt=f32), split_sizes=e(E, dt=i32),
@@ -91,7 +97,11 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
 def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None):
     dm = b.dims
     shared_out = None
-    if dm.f_shared:
+    if dm.f_shared and dm.prec == 1:
+        B.moe_mx_quantize_shared_weights(dm, w_gu_s, w_d_s, b.wq_s, stream)
+        B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
+        shared_out = b.y_s
+    elif dm.f_shared:
         B.moe_shared_mlp_fwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
         shared_out = b.y_s
     B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
@@ -113,7 +123,11 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
 def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None, w_d_s=None):
     dm = b.dims
     shared_dx = None
-    if dm.f_shared:
+    if dm.f_shared and dm.prec == 1:
+        B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s,
+                                b.dw_d_s, b.status, stream)
+        shared_dx = b.dx_s
+    elif dm.f_shared:
         B.moe_shared_mlp_bwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s, b.dw_d_s,
                              b.status, stream)
         shared_dx = b.dx_s

@@ -392,6 +392,24 @@ moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, 
                                      int32_t* dev_status, void* stream);
 
 /*
+ * The shared expert with MXFP8 GEMM operands (DeepSeek-V3 shape in MXFP8; f_shared and
+ * T multiples of 128).  wq_s (>= moe_mx_shared_weights_size bytes) holds W_gu_s and
+ * W_d_s quantised along both of their axes, filled by moe_mx_quantize_shared_weights;
+ * mx_ws_s (>= moe_mx_shared_workspace_size bytes) is scratch for the quantised
+ * activations.  Otherwise as moe_shared_mlp_fwd / moe_shared_mlp_bwd.
+ */
+size_t moe_mx_shared_weights_size(const moe_dims* dims);
+size_t moe_mx_shared_workspace_size(const moe_dims* dims);
+moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* w_gu_s, const moe_bf16* w_d_s,
+                                          void* wq_s, void* stream);
+moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
+                                 moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s, int32_t* dev_status, void* stream);
+moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
+                                 const moe_bf16* gu_s, const moe_bf16* h_s, const moe_bf16* dy, moe_bf16* dgu_s,
+                                 moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
+                                 void* stream);
+
+/*
  * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the
  * tensor-core core: C[m][n] = sum_k A(m,k) B(n,k), fp32 accumulation, bf16 out.
  *   a_layout 0: A stored [M][K];  1: A stored [K][M]

@@ -96,19 +96,44 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return (v * np.exp2(scales.astype(np.float64) - 127)[..., None]).reshape(codes.shape)
 
 
+def e4m3_round(a: np.ndarray) -> np.ndarray:
+    """Value of e4m3_encode, computed arithmetically: |a| rounded to the E4M3 grid.
+
+    For |a| >= 2^-6 the grid step is 2^(floor(log2|a|) - 3), below it 2^-9; np.rint
+    rounds half to even, which is the even code; the result saturates at 448.
+    """
+    a = np.asarray(a)
+    if a.dtype not in (np.float32, np.float64):
+        a = a.astype(np.float64)
+    mag = np.minimum(np.abs(a), a.dtype.type(E4M3_MAX))
+    _, ex = np.frexp(mag)                         # mag = m 2^ex, m in [0.5, 1)
+    step = np.ldexp(a.dtype.type(1), np.maximum(ex - 1, -6) - 3)
+    r = np.minimum(np.rint(mag / step) * step, a.dtype.type(E4M3_MAX))
+    return np.copysign(r, a)
+
+
 def qdq(x: np.ndarray) -> np.ndarray:
-    """Quantise then dequantise along the last axis, zero-padding it to a multiple of 32."""
-    x = np.asarray(x, np.float64)
+    """Quantise then dequantise along the last axis, zero-padding it to a multiple of 32.
+
+    Equal to mx_dequantize(*mx_quantize(x)) (checked in the tests), computed without
+    the code table so large operands stay cheap.
+    """
+    x = np.asarray(x)
+    if x.dtype != np.float32:        # fp32 stays fp32: every E4M3 code times 2^[-127,119] is an fp32
+        x = x.astype(np.float64)
     K = x.shape[-1]
     pad = (-K) % BLOCK
     if pad:
-        x = np.concatenate([x, np.zeros((*x.shape[:-1], pad))], axis=-1)
-    return mx_dequantize(*mx_quantize(x))[..., :K]
+        x = np.concatenate([x, np.zeros((*x.shape[:-1], pad), x.dtype)], axis=-1)
+    blocks = x.reshape(*x.shape[:-1], x.shape[-1] // BLOCK, BLOCK)
+    e = scale_exponent(np.abs(blocks).max(axis=-1).astype(np.float64))
+    scale = np.ldexp(x.dtype.type(1), e)[..., None]
+    return (e4m3_round(blocks / scale) * scale).reshape(x.shape)[..., :K]
 
 
 def mx_matmul(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:
     """a [M,K] x b [N,K]^T with both operands MXFP8-quantised along K (the shared axis)."""
-    return (qdq(a) @ qdq(b).T).astype(dtype)
+    return qdq(a).astype(dtype) @ qdq(b).astype(dtype).T
 
 
 # ----------------------------------------------------------------------------------
@@ -215,3 +240,48 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
         out["dW_d_s"] = matmul(dy.T, (g * sg * u).T, dtype)
         out["dW_gu_s"] = matmul(dgu.T, x.T, dtype)
     return out
+
+
+def expert_wgrad_sampled_mx(x, logits, dy, w_gu_e, w_d_e, e, k, gu_rows, d_cols, score="softmax",
+                            dtype=np.float64):
+    """Selected entries of expert e's weight gradients in the MXFP8 layer.
+
+    dW_gu[e][gu_rows, :] and dW_d[e][:, d_cols], by the formulas of moe_backward_mx
+    restricted to the intermediate columns those entries need (each quantisation
+    block lies inside one row or one column, so the restriction is exact).
+    """
+    from . import moe_oracle as om
+    idx, w = om.route(logits, k, score, dtype)
+    t_sel, j_sel = np.nonzero(idx == e)
+    f = w_d_e.shape[1]
+    d = w_d_e.shape[0]
+    gu_rows = np.asarray(gu_rows)
+    d_cols = np.asarray(d_cols)
+    if t_sel.size == 0:
+        return {"dW_gu_rows": np.zeros((gu_rows.size, d), dtype), "dW_d_cols": np.zeros((d, d_cols.size), dtype)}
+    xe = np.asarray(x[t_sel], dtype)
+    dye = np.asarray(dy[t_sel], dtype)
+    wg = np.asarray(w_gu_e, dtype)
+    wd = np.asarray(w_d_e, dtype)
+    we = w[t_sel, j_sel][:, None]
+    qx = qdq(xe)                      # X_e along d (forward)
+    qdy = qdq(dye)                    # dY_e along d (dgrad)
+
+    def gu_cols(cols):                # columns of G and U = mx(X_e, W_gu[e])
+        return qx @ qdq(wg[cols]).T, qx @ qdq(wg[f + cols]).T
+
+    # dW_d[:, c] = mx(dY_e^T, H_e^T): both along the rows of e
+    g2, u2 = gu_cols(d_cols)
+    h2 = we * g2 * om._sigmoid(g2) * u2
+    dw_d_cols = qdq(dye.T) @ qdq(h2.T).T
+    # dW_gu[j, :] = mx(dGU_e^T, X_e^T)
+    cols = gu_rows % f
+    g, u = gu_cols(cols)
+    sg = om._sigmoid(g)
+    dh = qdy @ qdq(wd.T[cols]).T       # dH = mx(dY_e, W_d[e]^T), columns `cols`
+    da = we * dh
+    dg = da * u * sg * (1.0 + g * (1.0 - sg))
+    du = da * g * sg
+    sel = np.where((gu_rows < f)[None, :], dg, du)
+    dw_gu_rows = qdq(sel.T) @ qdq(xe.T).T
+    return {"dW_gu_rows": dw_gu_rows.astype(dtype), "dW_d_cols": dw_d_cols.astype(dtype)}

@@ -21,6 +21,9 @@ CASES = {
     "mx-ragged": synth.small_config("mx-ragged", T=1000, d=256, f=128, E=8, k=2, bias_param=0.7, seed=41),
     "mx-zipf": synth.small_config("mx-zipf", T=777, d=384, f=256, E=16, k=4, score=synth.SIGMOID, bias="zipf",
                                   bias_param=1.0, forced_empty=2, seed=42),
+    # DeepSeek-V3-like with the shared expert (T a multiple of 128 for its row blocks)
+    "mx-shared": synth.small_config("mx-shared", T=384, d=256, f=128, E=16, k=4, score=synth.SIGMOID,
+                                    bias="zipf", bias_param=1.0, forced_empty=2, f_shared=128, seed=43),
 }
 
 
@@ -28,12 +31,17 @@ def _run(cfg):
     from dropless_mixture_experts_warp_gb300 import layer
     inp = synth.token_inputs(cfg)
     w_gu_b, w_d_b = synth.all_expert_weights(cfg)
-    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score, "mxfp8")
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, "mxfp8")
     b = layer.allocate(dims)
     w_gu, w_d = bf16_dev(w_gu_b), bf16_dev(w_d_b)
     logits = f32_dev(inp["logits"])
-    layer.forward(b, bf16_dev(inp["x"]), logits, w_gu, w_d)
-    layer.backward(b, bf16_dev(inp["dy"]), logits, w_gu, w_d)
+    sh = {}
+    if cfg.f_shared:
+        s_gu, s_d = synth.shared_weights(cfg)
+        sh = {"w_gu_s": bf16_dev(s_gu), "w_d_s": bf16_dev(s_d)}
+    x = bf16_dev(inp["x"])
+    layer.forward(b, x, logits, w_gu, w_d, **sh)
+    layer.backward(b, bf16_dev(inp["dy"]), logits, w_gu, w_d, x=x, **sh)
     layer.check(b)
     return b, inp, w_gu_b, w_d_b
 
@@ -44,12 +52,19 @@ def test_mx_layer_matches_mx_oracle(name):
     cfg = CASES[name]
     b, inp, w_gu_b, w_d_b = _run(cfg)
     f64 = lambda a: synth.bf16_to_f32(a).astype(np.float64)  # noqa: E731
-    fwd = mx.moe_forward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), cfg.k, cfg.score)
+    kw = {}
+    if cfg.f_shared:
+        s_gu, s_d = synth.shared_weights(cfg)
+        kw = {"w_gu_s": f64(s_gu), "w_d_s": f64(s_d)}
+    fwd = mx.moe_forward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), cfg.k, cfg.score, **kw)
     bwd = mx.moe_backward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), f64(inp["dy"]), fwd,
-                             cfg.k, cfg.score)
+                             cfg.k, cfg.score, **kw)
     errs = {"Y": rel_err(host(b.y), fwd["Y"]), "dX": rel_err(host(b.dx), bwd["dX"]),
             "dW_gu": rel_err(host(b.dw_gu), bwd["dW_gu"]), "dW_d": rel_err(host(b.dw_d), bwd["dW_d"]),
             "d_logits": rel_err(host(b.d_logits), bwd["d_logits"])}
+    if cfg.f_shared:
+        errs["dW_gu_s"] = rel_err(host(b.dw_gu_s), bwd["dW_gu_s"])
+        errs["dW_d_s"] = rel_err(host(b.dw_d_s), bwd["dW_d_s"])
     assert all(v <= TOL_MXFP8 for v in errs.values()), errs
     split = host(b.split_sizes)
     for e in np.nonzero(split == 0)[0]:

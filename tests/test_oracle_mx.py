@@ -138,3 +138,33 @@ def test_weight_gradient_row_blocks_start_at_the_segment():
         h = f1["w"][t, 0][:, None] * g * (1 / (1 + np.exp(-g))) * u
         ref = mx.qdq(dy[t].T) @ mx.qdq(h.T).T
         np.testing.assert_allclose(b1["dW_d"][e], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sampled_mx_wgrad_entries_match_full_mx_backward():
+    x, logits, w_gu, w_d, dy, _ = _small(seed=8, T=90, E=3, k=2)
+    f1 = mx.moe_forward_mx(x, logits, w_gu, w_d, 2)
+    b1 = mx.moe_backward_mx(x, logits, w_gu, w_d, dy, f1, 2)
+    rows = np.array([0, 7, 31, 32, 50, 63])
+    cols = np.array([1, 17, 30])
+    for e in range(3):
+        s = mx.expert_wgrad_sampled_mx(x, logits, dy, w_gu[e], w_d[e], e, 2, rows, cols)
+        np.testing.assert_allclose(s["dW_gu_rows"], b1["dW_gu"][e][rows], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(s["dW_d_cols"], b1["dW_d"][e][:, cols], rtol=1e-10, atol=1e-12)
+
+
+def test_fast_qdq_equals_code_table_path():
+    rng = np.random.default_rng(9)
+    v = _all_bf16_finite()
+    x = np.concatenate([v, rng.standard_normal(4096) * 1e-3, np.zeros(64), -np.zeros(32)])
+    x = np.concatenate([x, np.zeros((-x.size) % 32)]).reshape(-1, 32)
+    ref = mx.mx_dequantize(*mx.mx_quantize(x))
+    got = mx.qdq(x)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+    y = rng.standard_normal((50, 96)) * np.exp2(rng.integers(-30, 30, (50, 1)))
+    assert np.array_equal(mx.qdq(y), mx.mx_dequantize(*mx.mx_quantize(y)))
+    # the fp32 path gives the same values as the fp64 one
+    x32 = x.astype(np.float32)
+    assert np.array_equal(mx.qdq(x32).astype(np.float64), mx.qdq(x32.astype(np.float64)))
+    y32 = y.astype(np.float32)
+    assert np.array_equal(mx.qdq(y32).astype(np.float64), mx.qdq(y32.astype(np.float64)))
