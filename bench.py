@@ -233,38 +233,45 @@ def run_native(args, cfg):
                 ev[i].record(stream)
         B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
                          b.workspace, b.status, stream)
-        B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
-                      b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
-        if mx8:   # the 16-bit master weights are quantised every step
+        if mx8:
+            # the 16-bit master weights are quantised every step; x is quantised in the dispatch
             B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
+            B.moe_permute_mx(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.mx_ws,
+                             b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
+        else:
+            B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
+                          b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
         mark(0)
         if mx8:
-            B.moe_gemm_gate_up_mx(dm, b.xp, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.h, b.status, stream)
+            B.moe_gemm_gate_up_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.status, stream)
         else:
             B.moe_gemm_gate_up(dm, b.xp, b.row_offsets, b.w_rows, w_gu, b.gu, b.h, b.status, stream)
         mark(1)
         if mx8:
-            B.moe_gemm_down_mx(dm, b.h, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
+            B.moe_gemm_down_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
         else:
             B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
         mark(2)
         if cfg.f_shared and mx8:
             B.moe_mx_quantize_shared_weights(dm, inp["w_gu_s"], inp["w_d_s"], b.wq_s, stream)
-            B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
+            B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.y_s, b.status, stream)
         elif cfg.f_shared:
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
         B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
-        B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
+        if mx8:
+            B.moe_combine_bwd_mx(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.mx_ws, stream)
+        else:
+            B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         mark(3)
         if mx8:
-            B.moe_gemm_down_dgrad_mx(dm, b.dy_rows, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dgu,
-                                     b.dw_rows, b.workspace, b.status, stream)
+            B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace,
+                                     b.status, stream)
             mark(4)
-            B.moe_gemm_down_wgrad_mx(dm, b.dy_rows, b.h, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+            B.moe_gemm_down_wgrad_mx(dm, dy, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
             mark(5)
-            B.moe_gemm_gate_up_dgrad_mx(dm, b.dgu, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
+            B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
             mark(6)
-            B.moe_gemm_gate_up_wgrad_mx(dm, b.dgu, b.xp, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+            B.moe_gemm_gate_up_wgrad_mx(dm, x, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
         else:
             B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
                                   b.workspace, b.status, stream)
@@ -276,8 +283,8 @@ def run_native(args, cfg):
             B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
         mark(7)
         if cfg.f_shared and mx8:
-            B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s,
-                                    b.dw_d_s, b.status, stream)
+            B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
+                                    stream)
         elif cfg.f_shared:
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
                                  b.dw_gu_s, b.dw_d_s, b.status, stream)

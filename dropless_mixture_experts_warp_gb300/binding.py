@@ -76,19 +76,21 @@ SIGNATURES = {
     "moe_mx_shared_weights_size": (ctypes.c_size_t, [_D]),
     "moe_mx_shared_workspace_size": (ctypes.c_size_t, [_D]),
     "moe_mx_quantize_shared_weights": (ctypes.c_int32, [_D, _P, _P, _P, _P]),
-    "moe_shared_mlp_fwd_mx": (ctypes.c_int32, [_D] + [_P] * 8),
-    "moe_shared_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 12),
+    "moe_shared_mlp_fwd_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_shared_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 10),
     "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
     "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_mx_weights_size": (ctypes.c_size_t, [_D]),
     "moe_mx_workspace_size": (ctypes.c_size_t, [_D]),
     "moe_mx_quantize_weights": (ctypes.c_int32, [_D, _P, _P, _P, _P]),
-    "moe_gemm_gate_up_mx": (ctypes.c_int32, [_D] + [_P] * 9),
-    "moe_gemm_down_mx": (ctypes.c_int32, [_D] + [_P] * 7),
-    "moe_gemm_down_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 11),
+    "moe_permute_mx": (ctypes.c_int32, [_D] + [_P] * 12),
+    "moe_combine_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 6),
+    "moe_gemm_gate_up_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_down_mx": (ctypes.c_int32, [_D] + [_P] * 6),
+    "moe_gemm_down_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 9),
     "moe_gemm_down_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
-    "moe_gemm_gate_up_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_gate_up_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 6),
     "moe_gemm_gate_up_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
 }
 
@@ -299,42 +301,47 @@ def moe_mx_quantize_weights(dims, w_gu, w_d, wq, stream=None):
     return _call("moe_mx_quantize_weights", _d(dims), _ptr(w_gu), _ptr(w_d), _ptr(wq), _stream(stream))
 
 
-def moe_gemm_gate_up_mx(dims, xp, row_offsets, w_rows, wq, mx_ws, gu, h, dev_status, stream=None):
-    return _call("moe_gemm_gate_up_mx", _d(dims), _ptr(xp), _ptr(row_offsets), _ptr(w_rows), _ptr(wq),
-                 _ptr(mx_ws), _ptr(gu), _ptr(h), _ptr(dev_status), _stream(stream))
+def moe_permute_mx(dims, x, topk_idx, topk_w, split_sizes, row_offsets, workspace, mx_ws, row_to_token,
+                   token_to_row, w_rows, dev_status, stream=None):
+    return _call("moe_permute_mx", _d(dims), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(split_sizes),
+                 _ptr(row_offsets), _ptr(workspace), _ptr(mx_ws), _ptr(row_to_token), _ptr(token_to_row),
+                 _ptr(w_rows), _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_down_mx(dims, h, row_offsets, wq, mx_ws, y_rows, dev_status, stream=None):
-    return _call("moe_gemm_down_mx", _d(dims), _ptr(h), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws), _ptr(y_rows),
+def moe_combine_bwd_mx(dims, dy, token_to_row, split_sizes, row_offsets, mx_ws, stream=None):
+    return _call("moe_combine_bwd_mx", _d(dims), _ptr(dy), _ptr(token_to_row), _ptr(split_sizes),
+                 _ptr(row_offsets), _ptr(mx_ws), _stream(stream))
+
+
+def moe_gemm_gate_up_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_mx", _d(dims), _ptr(row_offsets), _ptr(w_rows), _ptr(wq), _ptr(mx_ws),
+                 _ptr(gu), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_down_mx(dims, row_offsets, wq, mx_ws, y_rows, dev_status, stream=None):
+    return _call("moe_gemm_down_mx", _d(dims), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws), _ptr(y_rows),
                  _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_down_dgrad_mx(dims, dy_rows, row_offsets, w_rows, wq, mx_ws, gu, dgu, dw_rows, workspace,
-                           dev_status, stream=None):
-    return _call("moe_gemm_down_dgrad_mx", _d(dims), _ptr(dy_rows), _ptr(row_offsets), _ptr(w_rows), _ptr(wq),
-                 _ptr(mx_ws), _ptr(gu), _ptr(dgu), _ptr(dw_rows), _ptr(workspace), _ptr(dev_status),
-                 _stream(stream))
+def moe_gemm_down_dgrad_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dw_rows, workspace, dev_status,
+                           stream=None):
+    return _call("moe_gemm_down_dgrad_mx", _d(dims), _ptr(row_offsets), _ptr(w_rows), _ptr(wq), _ptr(mx_ws),
+                 _ptr(gu), _ptr(dw_rows), _ptr(workspace), _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_down_wgrad_mx(dims, dy_rows, h, row_offsets, mx_ws, dw_d, dev_status, stream=None):
-    return _call("moe_gemm_down_wgrad_mx", _d(dims), _ptr(dy_rows), _ptr(h), _ptr(row_offsets), _ptr(mx_ws),
-                 _ptr(dw_d), _ptr(dev_status), _stream(stream))
+def moe_gemm_down_wgrad_mx(dims, dy, row_to_token, row_offsets, mx_ws, dw_d, dev_status, stream=None):
+    return _call("moe_gemm_down_wgrad_mx", _d(dims), _ptr(dy), _ptr(row_to_token), _ptr(row_offsets),
+                 _ptr(mx_ws), _ptr(dw_d), _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_gate_up_dgrad_mx(dims, dgu, row_offsets, wq, mx_ws, dxp, dev_status, stream=None):
-    return _call("moe_gemm_gate_up_dgrad_mx", _d(dims), _ptr(dgu), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws),
-                 _ptr(dxp), _ptr(dev_status), _stream(stream))
-
-
-def moe_gemm_gate_up_wgrad_mx(dims, dgu, xp, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
-    return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(dgu), _ptr(xp), _ptr(row_offsets), _ptr(mx_ws),
-                 _ptr(dw_gu), _ptr(dev_status), _stream(stream))
-
-
-def moe_gemm_bf16_pair(A, B, C, M, N, K, a_layout, b_layout, dev_status, stream=None):
-    return _call("moe_gemm_bf16_pair", _ptr(A), _ptr(B), _ptr(C), M, N, K, a_layout, b_layout,
+def moe_gemm_gate_up_dgrad_mx(dims, row_offsets, wq, mx_ws, dxp, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_dgrad_mx", _d(dims), _ptr(row_offsets), _ptr(wq), _ptr(mx_ws), _ptr(dxp),
                  _ptr(dev_status), _stream(stream))
 
+
+def moe_gemm_gate_up_wgrad_mx(dims, x, row_to_token, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(x), _ptr(row_to_token), _ptr(row_offsets),
+                 _ptr(mx_ws), _ptr(dw_gu), _ptr(dev_status), _stream(stream))
 
 def moe_mx_shared_weights_size(dims) -> int:
     return lib().moe_mx_shared_weights_size(_d(dims))
@@ -349,13 +356,16 @@ def moe_mx_quantize_shared_weights(dims, w_gu_s, w_d_s, wq_s, stream=None):
                  _stream(stream))
 
 
-def moe_shared_mlp_fwd_mx(dims, x, wq_s, mx_ws_s, gu_s, h_s, y_s, dev_status, stream=None):
-    return _call("moe_shared_mlp_fwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(h_s),
-                 _ptr(y_s), _ptr(dev_status), _stream(stream))
+def moe_shared_mlp_fwd_mx(dims, x, wq_s, mx_ws_s, gu_s, y_s, dev_status, stream=None):
+    return _call("moe_shared_mlp_fwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(y_s),
+                 _ptr(dev_status), _stream(stream))
 
 
-def moe_shared_mlp_bwd_mx(dims, x, wq_s, mx_ws_s, gu_s, h_s, dy, dgu_s, dx_s, dw_gu_s, dw_d_s, dev_status,
-                          stream=None):
-    return _call("moe_shared_mlp_bwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(h_s),
-                 _ptr(dy), _ptr(dgu_s), _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status),
-                 _stream(stream))
+def moe_shared_mlp_bwd_mx(dims, x, wq_s, mx_ws_s, gu_s, dy, dx_s, dw_gu_s, dw_d_s, dev_status, stream=None):
+    return _call("moe_shared_mlp_bwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(dy),
+                 _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_bf16_pair(A, B, C, M, N, K, a_layout, b_layout, dev_status, stream=None):
+    return _call("moe_gemm_bf16_pair", _ptr(A), _ptr(B), _ptr(C), M, N, K, a_layout, b_layout,
+                 _ptr(dev_status), _stream(stream))

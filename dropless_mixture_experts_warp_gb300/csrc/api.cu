@@ -117,6 +117,8 @@ static Carve carve(const moe_dims& d, void* ws) {
   return c;
 }
 
+RouteScratch route_scratch(const moe_dims& d, void* ws) { return carve(d, ws).route; }
+
 // The dw-partials region of a caller workspace (shared by the bf16 and MXFP8 calls).
 float* workspace_dw_part(const moe_dims& d, void* ws) { return carve(d, ws).dw_part; }
 

@@ -154,29 +154,60 @@ moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, c
   if (!al16(w_gu) || !al16(w_d) || !al16(wq)) return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, wq);
-  const long long E = d.E;
-  if (launch_quant_rows(w_gu, E * 2 * d.f, d.d, d.d, nullptr, w.gu_rows.codes, w.gu_rows.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(w_gu, d.E, 2ll * d.f, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s) != cudaSuccess ||
-      launch_quant_rows(w_d, E * d.d, d.f, d.f, nullptr, w.d_rows.codes, w.d_rows.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(w_d, d.E, d.d, d.f, nullptr, w.d_cols.codes, w.d_cols.sf, s) != cudaSuccess)
+  // one read of each weight: column-wise codes per expert and row-wise codes of the same tiles
+  if (launch_quant_cols_t(w_gu, d.E, 2ll * d.f, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s, nullptr,
+                          w.gu_rows.codes, w.gu_rows.sf) != cudaSuccess ||
+      launch_quant_cols_t(w_d, d.E, d.d, d.f, nullptr, w.d_cols.codes, w.d_cols.sf, s, nullptr, w.d_rows.codes,
+                          w.d_rows.sf) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
-moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const moe_bf16* xp, const int32_t* row_offsets,
-                               const float* w_rows, const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* h,
-                               int32_t* dev_status, void* stream) {
+moe_status moe_permute_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, const float* topk_w,
+                          const int32_t* split_sizes, const int32_t* row_offsets, const void* workspace,
+                          void* mx_ws, int32_t* row_to_token, int32_t* token_to_row, float* w_rows,
+                          int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!xp || !row_offsets || !w_rows || !wq || !mx_ws || !gu || !h || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(xp) || !al16(wq) || !al16(mx_ws) || !al16(gu) || !al16(h)) return MOE_ERR_ALIGNMENT;
+  if (!split_sizes || !row_offsets || !mx_ws || !row_to_token || !w_rows || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (!x || !topk_idx || !topk_w || !token_to_row)) return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  if (!al16(x) || !al16(mx_ws)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims);
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  RouteScratch rs = route_scratch(d, const_cast<void*>(workspace));
+  return cuda_st(launch_scatter_quant(true, x, d.T, d.d, d.E, d.k, topk_idx, topk_w, split_sizes, row_offsets, &rs,
+                                      a.xp_rows.codes, a.xp_rows.sf, row_to_token, token_to_row, w_rows,
+                                      static_cast<int>(R_cap), dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* token_to_row,
+                              const int32_t* split_sizes, const int32_t* row_offsets, void* mx_ws, void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!split_sizes || !row_offsets || !mx_ws) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (!dy || !token_to_row)) return MOE_ERR_INVALID_ARG;
+  if (!al16(dy) || !al16(mx_ws)) return MOE_ERR_ALIGNMENT;
+  const int64_t R_cap = moe_row_capacity(dims);
+  MxActs a = carve_acts(d, R_cap, mx_ws);
+  return cuda_st(launch_scatter_quant(false, dy, d.T, d.d, d.E, d.k, nullptr, nullptr, split_sizes, row_offsets,
+                                      nullptr, a.dy_rows.codes, a.dy_rows.sf, nullptr,
+                                      const_cast<int32_t*>(token_to_row), nullptr, static_cast<int>(R_cap),
+                                      nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                               const void* wq, void* mx_ws, moe_bf16* gu, int32_t* dev_status, void* stream) {
+  moe_status st = mx_common(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!row_offsets || !w_rows || !wq || !mx_ws || !gu || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  if (launch_quant_rows(xp, R_cap, d.d, d.d, row_offsets + d.E, a.xp_rows.codes, a.xp_rows.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   CUtensorMap ta, tb;
   if (!make_tensor_map_u8(&ta, a.xp_rows.codes, d.d, R_cap, 128, BM) ||
       !make_tensor_map_u8(&tb, w.gu_rows.codes, d.d, 2ll * d.f * d.E, 128, 128))
@@ -184,24 +215,23 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const moe_bf16* xp, const i
   GemmParams p = mx_params();
   p.BN = 256; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = 2 * d.f;
   p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
-  p.gu_out = gu; p.h_out = h; p.status = dev_status;
+  p.gu_out = gu; p.status = dev_status;
   p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s));
+  p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
+  p.q_cols_ld = R_cap; p.q_cols_ktiles = static_cast<int>(R_cap / 128);
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_gemm_down_mx(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets, const void* wq,
-                            void* mx_ws, moe_bf16* y_rows, int32_t* dev_status, void* stream) {
+moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq, void* mx_ws,
+                            moe_bf16* y_rows, int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!h || !row_offsets || !wq || !mx_ws || !y_rows || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(h) || !al16(wq) || !al16(mx_ws) || !al16(y_rows)) return MOE_ERR_ALIGNMENT;
+  if (!row_offsets || !wq || !mx_ws || !y_rows || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(wq) || !al16(mx_ws) || !al16(y_rows)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  if (launch_quant_rows(h, R_cap, d.f, d.f, row_offsets + d.E, a.h_rows.codes, a.h_rows.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   CUtensorMap ta, tb;
   if (!make_tensor_map_u8(&ta, a.h_rows.codes, d.f, R_cap, 128, BM) ||
@@ -211,29 +241,23 @@ moe_status moe_gemm_down_mx(const moe_dims* dims, const moe_bf16* h, const int32
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   p.sfa = a.h_rows.sf; p.sfb = w.d_rows.sf; p.a_sf_ktiles = d.f / 128; p.b_sf_ktiles = d.f / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const int32_t* row_offsets,
-                                  const float* w_rows, const void* wq, void* mx_ws, const moe_bf16* gu,
-                                  moe_bf16* dgu, float* dw_rows, void* workspace, int32_t* dev_status,
-                                  void* stream) {
+moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, const moe_bf16* gu, float* dw_rows, void* workspace,
+                                  int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!dy_rows || !row_offsets || !w_rows || !wq || !mx_ws || !gu || !dgu || !dw_rows || !dev_status)
-    return MOE_ERR_INVALID_ARG;
+  if (!row_offsets || !w_rows || !wq || !mx_ws || !gu || !dw_rows || !dev_status) return MOE_ERR_INVALID_ARG;
   if (!workspace) return MOE_ERR_WORKSPACE;
-  if (!al16(dy_rows) || !al16(wq) || !al16(mx_ws) || !al16(gu) || !al16(dgu)) return MOE_ERR_ALIGNMENT;
+  if (!al16(wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  // the dw partials use the same region of the workspace as the bf16 call
   float* dw_part = workspace_dw_part(d, workspace);
-  if (launch_quant_rows(dy_rows, R_cap, d.d, d.d, row_offsets + d.E, a.dy_rows.codes, a.dy_rows.sf, s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
   const int bn = bn_mx(d.f);
   CUtensorMap ta, tb;
   if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, R_cap, 128, BM) ||
@@ -242,26 +266,29 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows,
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.f;
   p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
-  p.dgu_out = dgu; p.dw_part = dw_part; p.dw_stride = d.f / bn; p.status = dev_status;
+  p.dw_part = dw_part; p.dw_stride = d.f / bn; p.status = dev_status;
   p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
+  p.q_cols_sf = a.dgu_cols.sf; p.q_cols_ld = R_cap; p.q_cols_ktiles = static_cast<int>(R_cap / 128);
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_st(launch_dw_reduce(dw_part, d.f / bn, row_offsets, d.E, dw_rows, static_cast<int>(R_cap), s));
 }
 
-moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const moe_bf16* h,
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
                                   const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
                                   void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!dy_rows || !h || !row_offsets || !mx_ws || !dw_d || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(dy_rows) || !al16(h) || !al16(mx_ws) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
+  if (!row_to_token || !row_offsets || !mx_ws || !dw_d || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && !dy) return MOE_ERR_INVALID_ARG;
+  if (!al16(dy) || !al16(mx_ws) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  const int32_t* nrows = row_offsets + d.E;
-  if (launch_quant_cols_t(dy_rows, 1, R_cap, d.d, nrows, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(h, 1, R_cap, d.f, nrows, a.h_cols.codes, a.h_cols.sf, s) != cudaSuccess)
+  // column-wise codes of dY's routed rows, gathered from dY through row_to_token
+  if (launch_quant_cols_t(dy, 1, R_cap, d.d, row_offsets + d.E, a.dy_cols.codes, a.dy_cols.sf, s, row_to_token) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   const int bn = bn_mx(d.f);
   CUtensorMap ta, tb;
@@ -276,21 +303,16 @@ moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows,
   return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
 }
 
-moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const int32_t* row_offsets,
-                                     const void* wq, void* mx_ws, moe_bf16* dxp, int32_t* dev_status,
-                                     void* stream) {
+moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq,
+                                     void* mx_ws, moe_bf16* dxp, int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!dgu || !row_offsets || !wq || !mx_ws || !dxp || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(dgu) || !al16(wq) || !al16(mx_ws) || !al16(dxp)) return MOE_ERR_ALIGNMENT;
+  if (!row_offsets || !wq || !mx_ws || !dxp || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(wq) || !al16(mx_ws) || !al16(dxp)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  if (launch_quant_rows(dgu, R_cap, 2 * d.f, 2ll * d.f, row_offsets + d.E, a.dgu_rows.codes, a.dgu_rows.sf, s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   CUtensorMap ta, tb;
   if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * d.f, R_cap, 128, BM) ||
@@ -300,23 +322,24 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const moe_bf16* dgu, 
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * d.f / 128; p.b_sf_ktiles = 2 * d.f / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* row_to_token,
                                      const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu, int32_t* dev_status,
                                      void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!dgu || !xp || !row_offsets || !mx_ws || !dw_gu || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(dgu) || !al16(xp) || !al16(mx_ws) || !al16(dw_gu)) return MOE_ERR_ALIGNMENT;
+  if (!row_to_token || !row_offsets || !mx_ws || !dw_gu || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && !x) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(mx_ws) || !al16(dw_gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  const int32_t* nrows = row_offsets + d.E;
-  if (launch_quant_cols_t(dgu, 1, R_cap, 2 * d.f, nrows, a.dgu_cols.codes, a.dgu_cols.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(xp, 1, R_cap, d.d, nrows, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
+  // column-wise codes of the permuted rows, gathered from x through row_to_token
+  if (launch_quant_cols_t(x, 1, R_cap, d.d, row_offsets + d.E, a.xp_cols.codes, a.xp_cols.sf, s, row_to_token) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   CUtensorMap ta, tb;
@@ -401,23 +424,22 @@ moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, wq_s);
   const int fs = d.f_shared;
-  if (launch_quant_rows(w_gu_s, 2ll * fs, d.d, d.d, nullptr, w.gu_rows.codes, w.gu_rows.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(w_gu_s, 1, 2ll * fs, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s) != cudaSuccess ||
-      launch_quant_rows(w_d_s, d.d, fs, fs, nullptr, w.d_rows.codes, w.d_rows.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(w_d_s, 1, d.d, fs, nullptr, w.d_cols.codes, w.d_cols.sf, s) != cudaSuccess)
+  if (launch_quant_cols_t(w_gu_s, 1, 2ll * fs, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s, nullptr,
+                          w.gu_rows.codes, w.gu_rows.sf) != cudaSuccess ||
+      launch_quant_cols_t(w_d_s, 1, d.d, fs, nullptr, w.d_cols.codes, w.d_cols.sf, s, nullptr, w.d_rows.codes,
+                          w.d_rows.sf) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
 moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s, int32_t* dev_status, void* stream) {
+                                 moe_bf16* gu_s, moe_bf16* y_s, int32_t* dev_status, void* stream) {
   moe_status st = mx_shared_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (d.T == 0) return MOE_OK;
-  if (!x || !wq_s || !mx_ws_s || !gu_s || !h_s || !y_s || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(h_s) || !al16(y_s))
-    return MOE_ERR_ALIGNMENT;
+  if (!x || !wq_s || !mx_ws_s || !gu_s || !y_s || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(y_s)) return MOE_ERR_ALIGNMENT;
   const int fs = d.f_shared, T = d.T;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
@@ -431,11 +453,11 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
     return MOE_ERR_CUDA;
   p = mx_params();
   p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1; p.f = fs;
-  p.row_limit = T; p.gu_out = gu_s; p.h_out = h_s; p.status = dev_status;
+  p.row_limit = T; p.gu_out = gu_s; p.status = dev_status;
   p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_quant_rows(h_s, T, fs, fs, nullptr, a.h_rows.codes, a.h_rows.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
+  p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   if (!make_tensor_map_u8(&ta, a.h_rows.codes, fs, T, 128, BM) ||
       !make_tensor_map_u8(&tb, w.d_rows.codes, fs, d.d, 128, bn))
@@ -448,9 +470,8 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
 }
 
 moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 const moe_bf16* gu_s, const moe_bf16* h_s, const moe_bf16* dy, moe_bf16* dgu_s,
-                                 moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
-                                 void* stream) {
+                                 const moe_bf16* gu_s, const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s,
+                                 moe_bf16* dw_d_s, int32_t* dev_status, void* stream) {
   moe_status st = mx_shared_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
@@ -463,16 +484,16 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (!x || !mx_ws_s || !gu_s || !h_s || !dy || !dgu_s || !dx_s) return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(h_s) || !al16(dy) || !al16(dgu_s) ||
-      !al16(dx_s) || !al16(dw_gu_s) || !al16(dw_d_s))
+  if (!x || !mx_ws_s || !gu_s || !dy || !dx_s) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(dy) || !al16(dx_s) || !al16(dw_gu_s) ||
+      !al16(dw_d_s))
     return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
   MxActs a = carve_shared_acts(d, mx_ws_s);
   CUtensorMap ta, tb;
   GemmParams p;
-  // dH = dy W_d_s with the SwiGLU' epilogue (weight 1, no dw)
+  // dH = dy W_d_s, SwiGLU' epilogue (weight 1, no dw) writing quantised dG|dU
   if (launch_quant_rows(dy, T, d.d, d.d, nullptr, a.dy_rows.codes, a.dy_rows.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   int bn = bn_mx(fs);
@@ -481,12 +502,13 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
     return MOE_ERR_CUDA;
   p = mx_params();
   p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = 1; p.f = fs;
-  p.row_limit = T; p.gu_in = gu_s; p.dgu_out = dgu_s; p.status = dev_status;
+  p.row_limit = T; p.gu_in = gu_s; p.status = dev_status;
   p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
-  // dW_d_s = dy^T h_s (K = T)
-  if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(h_s, 1, T, fs, nullptr, a.h_cols.codes, a.h_cols.sf, s) != cudaSuccess)
+  p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
+  p.q_cols_sf = a.dgu_cols.sf; p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // dW_d_s = dy^T h_s (K = T): dy column codes, h_s column codes from the forward
+  if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!make_tensor_map_u8(&ta, a.dy_cols.codes, T, d.d, 128, BM) ||
       !make_tensor_map_u8(&tb, a.h_cols.codes, T, fs, 128, bn))
@@ -497,8 +519,6 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   p.sfa = a.dy_cols.sf; p.sfb = a.h_cols.sf; p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
   if (launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dx_s = dgu_s W_gu_s (K = 2fs)
-  if (launch_quant_rows(dgu_s, T, 2 * fs, 2ll * fs, nullptr, a.dgu_rows.codes, a.dgu_rows.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   bn = bn_mx(d.d);
   if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * fs, T, 128, BM) ||
       !make_tensor_map_u8(&tb, w.gu_cols.codes, 2ll * fs, d.d, 128, bn))
@@ -509,8 +529,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
   if (launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dW_gu_s = dgu_s^T x (K = T)
-  if (launch_quant_cols_t(dgu_s, 1, T, 2 * fs, nullptr, a.dgu_cols.codes, a.dgu_cols.sf, s) != cudaSuccess ||
-      launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
+  if (launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!make_tensor_map_u8(&ta, a.dgu_cols.codes, T, 2ll * fs, 128, BM) ||
       !make_tensor_map_u8(&tb, a.xp_cols.codes, T, d.d, 128, bn))

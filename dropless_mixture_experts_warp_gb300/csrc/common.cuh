@@ -196,6 +196,62 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ MXFP8 quantisation
+// Scale rule: e = floor(log2(amax)) - 8 clamped to [-127, 127] (byte e + 127; 0 for an
+// all-zero block); codes = E4M3(x * 2^-e), round to nearest even, saturating (cvt).
+// Scale tiles: tile (r/128, k/128) of 512 bytes; word (r%32)*4 + (r%128)/32 holds the
+// four 32-element block scales of row r in that K range.
+
+__device__ __forceinline__ size_t sf_byte_offset(long long r, long long k, long long k_tiles) {
+  const long long tile = (r >> 7) * k_tiles + (k >> 7);
+  const int word = static_cast<int>((r & 31) * 4 + ((r & 127) >> 5));
+  return static_cast<size_t>(tile) * 512 + word * 4 + static_cast<int>((k & 127) >> 5);
+}
+
+// floor(log2(a)) - 8 clamped to [-127, 127] for a finite a >= 0 (-127 for a = 0).
+__device__ __forceinline__ int mx_scale_exp(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int ef = static_cast<int>((b >> 23) & 0xFF);
+  int fl;
+  if (ef > 0) {
+    fl = ef - 127;
+  } else {
+    const uint32_t m = b & 0x7FFFFF;
+    if (m == 0) return -127;
+    fl = (31 - __clz(m)) - 149;
+  }
+  return max(-127, min(127, fl - 8));
+}
+
+// 2^-e as an fp32 for e in [-127, 127] (2^-127 .. 2^127; 2^-127 is subnormal).
+__device__ __forceinline__ float exp2_neg(int e) {
+  const int f = 127 - e;  // biased exponent of 2^-e
+  return f > 0 ? __uint_as_float(static_cast<uint32_t>(f) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two fp32 -> two E4M3 bytes (lo from `lo`, hi from `hi`), RNE, saturating.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantise 32 fp32 values (one block) into 8 words of codes; returns the scale byte.
+__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&codes)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mx_scale_exp(amax);
+  const float s = exp2_neg(e);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t a = cvt_e4m3x2(v[4 * w + 0] * s, v[4 * w + 1] * s);
+    const uint32_t b = cvt_e4m3x2(v[4 * w + 2] * s, v[4 * w + 3] * s);
+    codes[w] = a | (b << 16);
+  }
+  return static_cast<uint32_t>(e + 127);
+}
+
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

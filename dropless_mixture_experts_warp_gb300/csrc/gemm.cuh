@@ -38,13 +38,21 @@ constexpr int TMEM_COLS = 512;
 constexpr int ACC_STRIDE = 256;
 // Epilogue warps: 8 for the SwiGLU' epilogue (two per TMEM lane quarter, splitting
 // the columns), 4 otherwise.  Block = producer warp + MMA warp + epilogue warps.
-__host__ __device__ constexpr int epi_warps(int epi) { return epi == 2 ? 8 : 4; }
+__host__ __device__ constexpr int epi_warps(int epi) { return (epi == 2 || epi == 4) ? 8 : 4; }
 __host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int MAX_EXPERTS = 1024;
 constexpr long long WAIT_LIMIT_CYCLES = 1ll << 31;  // about one second
 
-enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+enum Epi {
+  EPI_STORE = 0,
+  EPI_SWIGLU_FWD = 1,     // G|U (bf16, saved) and h (bf16)
+  EPI_SWIGLU_BWD = 2,     // dG|dU (bf16) and dw partials
+  EPI_SWIGLU_FWD_MX = 3,  // G|U (bf16, saved) and h quantised row- and column-wise (MXFP8)
+  EPI_SWIGLU_BWD_MX = 4   // dG|dU quantised row- and column-wise, and dw partials
+};
 enum Sched { SCHED_ROWS = 0, SCHED_KGROUP = 1 };
+// Epilogues whose accumulator holds gate columns then up columns (B = gate rows, up rows)
+__host__ __device__ constexpr bool gu_split(int epi) { return epi == EPI_SWIGLU_FWD || epi == EPI_SWIGLU_FWD_MX; }
 
 struct GemmParams {
   int BN;                       // accumulator width: 64, 128 or 256
@@ -73,6 +81,15 @@ struct GemmParams {
   const uint8_t* sfb;
   int a_sf_ktiles;
   int b_sf_ktiles;
+  // fused MXFP8 outputs of the *_MX epilogues: row-wise codes [rows][width] with SF
+  // tiles (K = width), and column-wise codes [width][q_cols_ld] with SF tiles
+  // (K = rows, q_cols_ktiles = q_cols_ld / 128); width = f (h) or 2f (dG|dU)
+  uint8_t* q_rows;
+  uint8_t* q_rows_sf;
+  uint8_t* q_cols;
+  uint8_t* q_cols_sf;
+  long long q_cols_ld;
+  int q_cols_ktiles;
 };
 
 struct TileCoord {
@@ -103,7 +120,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
     c.kblocks = p.K / KB;
     c.a_m = s_ro[e] + c.m * BM;
     c.a_k = 0;
-    c.out_col = (EPI == EPI_SWIGLU_FWD) ? c.n * (p.BN / 2) : c.n * p.BN;
+    c.out_col = gu_split(EPI) ? c.n * (p.BN / 2) : c.n * p.BN;
     c.b_n = B_MN ? c.out_col : e * p.b_rows_per_expert + c.out_col;
     c.b_k = B_MN ? e * p.b_k_per_expert : 0;
     c.out_row = c.a_m;
@@ -205,6 +222,153 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
           hdst[v] = make_uint4(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
                                pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
         }
+      }
+    }
+  } else if (EPI == EPI_SWIGLU_FWD_MX) {
+    // as EPI_SWIGLU_FWD, but h is not stored: it is quantised from fp32 along its row
+    // (one 32-column block per chunk) and down its column (the warp's 32 rows are one
+    // 32-row block: a warp-wide max per column gives the block scale)
+    const int hw = BN / 2;
+    const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+    const long long ld2 = 2ll * p.f;
+    const int lane = row_in_tile & 31;
+    const long long rblk = row - lane;
+    const int cb = half * (hw / NH);
+    for (int c0 = cb; c0 < cb + hw / NH; c0 += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(tbase + c0, g);
+      tmem_ld32(tbase + hw + c0, u);
+      tmem_wait_ld();
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+        hv[i] = w * (gv * sigmoidf_(gv)) * uv;
+      }
+      const int col = c.out_col + c0;
+      if (row_ok) {
+        uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + col);
+        uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + col);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          gdst[v] = make_uint4(pack_bf16(__uint_as_float(g[8 * v]), __uint_as_float(g[8 * v + 1])),
+                               pack_bf16(__uint_as_float(g[8 * v + 2]), __uint_as_float(g[8 * v + 3])),
+                               pack_bf16(__uint_as_float(g[8 * v + 4]), __uint_as_float(g[8 * v + 5])),
+                               pack_bf16(__uint_as_float(g[8 * v + 6]), __uint_as_float(g[8 * v + 7])));
+          udst[v] = make_uint4(pack_bf16(__uint_as_float(u[8 * v]), __uint_as_float(u[8 * v + 1])),
+                               pack_bf16(__uint_as_float(u[8 * v + 2]), __uint_as_float(u[8 * v + 3])),
+                               pack_bf16(__uint_as_float(u[8 * v + 4]), __uint_as_float(u[8 * v + 5])),
+                               pack_bf16(__uint_as_float(u[8 * v + 6]), __uint_as_float(u[8 * v + 7])));
+        }
+        uint32_t q[8];
+        const uint32_t sb = quant_block32(hv, q);
+        uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * p.f + col);
+        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float a = fabsf(hv[i]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        const int e = mx_scale_exp(a);
+        const uint32_t code = cvt_e4m3x2(hv[i] * exp2_neg(e), 0.0f) & 0xFFu;
+        if (row_ok) {
+          p.q_cols[static_cast<long long>(col + i) * p.q_cols_ld + row] = static_cast<uint8_t>(code);
+          if (lane == 0)
+            p.q_cols_sf[sf_byte_offset(col + i, rblk, p.q_cols_ktiles)] = static_cast<uint8_t>(e + 127);
+        }
+      }
+    }
+  } else if (EPI == EPI_SWIGLU_BWD_MX) {
+    // as EPI_SWIGLU_BWD, but dG|dU are quantised from fp32 along their row (blocks of
+    // 32 columns of 2f) and down their columns (the warp's 32 rows)
+    const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+    const long long ld2 = 2ll * p.f;
+    const int lane = row_in_tile & 31;
+    const long long rblk = row - lane;
+    float dwp = 0.0f;
+    const int cb = half * (BN / NH);
+    for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
+      uint4 g4[4], u4[4];
+      if (row_ok) {
+        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
+        const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) { g4[v] = gsrc[v]; u4[v] = usrc[v]; }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) { g4[v] = make_uint4(0u, 0u, 0u, 0u); u4[v] = g4[v]; }
+      }
+      uint32_t r[32];
+      tmem_ld32(tbase + c0, r);
+      tmem_wait_ld();
+      float dg[32], du[32];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t gw[4] = {g4[v].x, g4[v].y, g4[v].z, g4[v].w};
+        const uint32_t uw[4] = {u4[v].x, u4[v].y, u4[v].z, u4[v].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+          const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
+          const float dh = __uint_as_float(r[8 * v + i]);
+          const float sg = sigmoidf_(g);
+          const float silu = g * sg;
+          const float da = w * dh;
+          dwp += silu * u * dh;
+          dg[8 * v + i] = da * u * sg * (1.0f + g * (1.0f - sg));
+          du[8 * v + i] = da * silu;
+        }
+      }
+      const int col = c.out_col + c0;  // dG column; dU column = f + col
+      if (row_ok) {
+        uint32_t q[8];
+        uint32_t sb = quant_block32(dg, q);
+        uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + col);
+        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        p.q_rows_sf[sf_byte_offset(row, col, ld2 / 128)] = static_cast<uint8_t>(sb);
+        sb = quant_block32(du, q);
+        qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + p.f + col);
+        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        p.q_rows_sf[sf_byte_offset(row, p.f + col, ld2 / 128)] = static_cast<uint8_t>(sb);
+      }
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float v = i < 32 ? dg[i] : du[i - 32];
+        float a = fabsf(v);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        const int e = mx_scale_exp(a);
+        const uint32_t code = cvt_e4m3x2(v * exp2_neg(e), 0.0f) & 0xFFu;
+        const int qc = i < 32 ? col + i : p.f + col + (i - 32);
+        if (row_ok) {
+          p.q_cols[static_cast<long long>(qc) * p.q_cols_ld + row] = static_cast<uint8_t>(code);
+          if (lane == 0)
+            p.q_cols_sf[sf_byte_offset(qc, rblk, p.q_cols_ktiles)] = static_cast<uint8_t>(e + 127);
+        }
+      }
+    }
+    if (NH == 1) {
+      if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
+    } else if (p.dw_part) {
+      const uint32_t ph = *hand.phase;
+      *hand.phase ^= 1u;
+      if (half == 1) {
+        if (!mbar_wait_bounded(&hand.empty[quarter], ph ^ 1, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+          return false;
+        hand.s_dw[row_in_tile] = dwp;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hand.full[quarter]);
+      } else {
+        if (!mbar_wait_bounded(&hand.full[quarter], ph, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+          return false;
+        if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp + hand.s_dw[row_in_tile];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hand.empty[quarter]);
       }
     }
   } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN; this half: BN/2 of them
@@ -320,7 +484,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   const uint32_t tmem_base = s_tmem_base;
 
   const int BN = p.BN;
-  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
 
@@ -350,7 +514,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
             tma_load_2d(sa + 8192, &tmA, bar, c.a_m + 64, c.a_k + k0);
           }
           if (!B_MN) {
-            if (EPI == EPI_SWIGLU_FWD) {
+            if (gu_split(EPI)) {
               tma_load_2d(sb, &tmB, bar, k0, c.b_n);
               tma_load_2d(sb + (BN / 2) * 128, &tmB, bar, k0, c.b_n + p.f);
             } else {

@@ -53,8 +53,8 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
     c.kblocks = p.K / BK;
     c.a_m = s_ro[e] + c.m * 2 * BM + rank * BM;
     c.a_k = 0;
-    c.out_col = (EPI == EPI_SWIGLU_FWD) ? c.n * half_n : c.n * p.BN;
-    if (EPI == EPI_SWIGLU_FWD)  // leader: gate rows, peer: up rows
+    c.out_col = gu_split(EPI) ? c.n * half_n : c.n * p.BN;
+    if (gu_split(EPI))  // leader: gate rows, peer: up rows
       c.b_n = e * p.b_rows_per_expert + c.out_col + rank * p.f;
     else
       c.b_n = (B_MN ? 0 : e * p.b_rows_per_expert) + c.out_col + rank * half_n;
@@ -114,7 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   const int BN = p.BN;  // 128 or 256
-  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   __syncthreads();
   if (threadIdx.x == 0) {
     // pair tiles per expert, exclusive prefix (E <= 1024, once per launch)

@@ -22,6 +22,8 @@ cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMa
     case GEMM_ROWS_STORE: return launch_mx_t<SCHED_ROWS, EPI_STORE>(a, b, p, stream);
     case GEMM_ROWS_SWIGLU_BWD: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD>(a, b, p, stream);
     case GEMM_KGROUP_STORE: return launch_mx_t<SCHED_KGROUP, EPI_STORE>(a, b, p, stream);
+    case GEMM_ROWS_SWIGLU_FWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_FWD_MX>(a, b, p, stream);
+    case GEMM_ROWS_SWIGLU_BWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD_MX>(a, b, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 
   const int BN = p.BN;                       // 128 or 256
   const int num_acc = BN <= 128 ? 2 : 1;
-  const int n_tiles = (EPI == EPI_SWIGLU_FWD) ? p.N / (BN / 2) : p.N / BN;
+  const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
 
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                     p.sfa + (static_cast<size_t>(c.a_m / 128) * p.a_sf_ktiles + kbt) * 512, 512, bar);
           const int kbb = c.b_k + kb * MX_BK;
           const int kbtb = kbb / MX_BK;
-          if (EPI == EPI_SWIGLU_FWD) {           // gate rows then up rows, 128 each
+          if (gu_split(EPI)) {                    // gate rows then up rows, 128 each
             tma_load_2d(sb, &tmB, bar, kbb, c.b_n);
             tma_load_2d(sb + (BN / 2) * MX_BK, &tmB, bar, kbb, c.b_n + p.f);
             bulk_load(sa + MX_SFB_OFF,

@@ -54,7 +54,9 @@ enum GemmKind {
   GEMM_ROWS_SWIGLU_BWD = 3,  // ragged rows, K-major A, MN-major B, SwiGLU' epilogue
   GEMM_KGROUP_STORE = 4,     // ragged K (weight gradients), MN-major A and B
   GEMM_DENSE_AMN_BK = 5,     // dense, MN-major A, K-major B (test hook)
-  GEMM_DENSE_AMN_BMN = 6     // dense, MN-major A and B (test hook)
+  GEMM_DENSE_AMN_BMN = 6,    // dense, MN-major A and B (test hook)
+  GEMM_ROWS_SWIGLU_FWD_MXQ = 7,  // MXFP8 only: gate/up epilogue writing quantised h
+  GEMM_ROWS_SWIGLU_BWD_MXQ = 8   // MXFP8 only: SwiGLU' epilogue writing quantised dG|dU
 };
 
 cudaError_t launch_gemm_fwd(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
@@ -85,7 +87,14 @@ cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMa
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
-                                uint8_t* codes, uint8_t* sf, cudaStream_t stream);
+                                uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map = nullptr,
+                                uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr);
+cudaError_t launch_scatter_quant(bool from_route, const void* src, int T, int d, int E, int k,
+                                 const int32_t* topk_idx, const float* topk_w, const int32_t* split_sizes,
+                                 const int32_t* row_offsets, const RouteScratch* ws, uint8_t* codes, uint8_t* sf,
+                                 int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
+                                 int32_t* status, cudaStream_t stream);
+RouteScratch route_scratch(const moe_dims& d, void* ws);
 float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);

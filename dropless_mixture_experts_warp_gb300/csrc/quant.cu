@@ -15,56 +15,6 @@
 
 namespace moe {
 
-__device__ __forceinline__ size_t sf_byte_offset(long long r, long long k, long long k_tiles) {
-  const long long tile = (r >> 7) * k_tiles + (k >> 7);
-  const int word = static_cast<int>((r & 31) * 4 + ((r & 127) >> 5));
-  return static_cast<size_t>(tile) * 512 + word * 4 + static_cast<int>((k & 127) >> 5);
-}
-
-// floor(log2(a)) - 8 clamped to [-127, 127] for a finite a >= 0 (-127 for a = 0).
-__device__ __forceinline__ int mx_scale_exp(float a) {
-  const uint32_t b = __float_as_uint(a);
-  const int ef = static_cast<int>((b >> 23) & 0xFF);
-  int fl;
-  if (ef > 0) {
-    fl = ef - 127;
-  } else {
-    const uint32_t m = b & 0x7FFFFF;
-    if (m == 0) return -127;
-    fl = (31 - __clz(m)) - 149;
-  }
-  return max(-127, min(127, fl - 8));
-}
-
-// 2^-e as an fp32 for e in [-127, 127] (2^-127 .. 2^127; 2^-127 is subnormal).
-__device__ __forceinline__ float exp2_neg(int e) {
-  const int f = 127 - e;  // biased exponent of 2^-e
-  return f > 0 ? __uint_as_float(static_cast<uint32_t>(f) << 23) : __uint_as_float(0x00400000u);
-}
-
-// Two fp32 -> two E4M3 bytes (lo from `lo`, hi from `hi`), RNE, saturating.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Quantise 32 fp32 values (one block) into 8 words of codes; returns the scale byte.
-__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&codes)[8]) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int e = mx_scale_exp(amax);
-  const float s = exp2_neg(e);
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t a = cvt_e4m3x2(v[4 * w + 0] * s, v[4 * w + 1] * s);
-    const uint32_t b = cvt_e4m3x2(v[4 * w + 2] * s, v[4 * w + 3] * s);
-    codes[w] = a | (b << 16);
-  }
-  return static_cast<uint32_t>(e + 127);
-}
-
 // Row-wise: src bf16 [rows][C] (row stride ld elements) -> codes [rows][C], SF tiles
 // with C/128 K tiles.  One warp per row, a lane per 128-column block.  Rows at or
 // beyond *nrows_dev (if given) are skipped.
@@ -111,10 +61,16 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 // 128 x 128 tile; a thread one column and two 32-row blocks.  Rows at or beyond
 // *nrows_dev (if given) are skipped in whole 128-row tiles (the row space is padded
 // to 128 per group, so a tile is either fully inside or fully outside).
+// Optional: row_map (batch 1) reads row r from src row row_map[r] (a negative entry
+// reads zeros) -- the column-wise codes of a permuted matrix straight from its
+// source; codes_rows/sf_rows also write the row-wise codes of the same tile
+// ([batch*rows][C], K = C), so a weight is read once for both orientations.
 __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __restrict__ src, long long rows,
                                                            int C, const int32_t* __restrict__ nrows_dev,
-                                                           uint8_t* __restrict__ codes,
-                                                           uint8_t* __restrict__ sf) {
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                           const int32_t* __restrict__ row_map,
+                                                           uint8_t* __restrict__ codes_rows,
+                                                           uint8_t* __restrict__ sf_rows) {
   __shared__ uint16_t tile[128][128 + 8];
   const long long b = blockIdx.z;
   const long long r0 = static_cast<long long>(blockIdx.y) * 128;
@@ -122,12 +78,13 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   long long limit = rows;
   if (nrows_dev) limit = min(limit, static_cast<long long>(*nrows_dev));
   if (r0 >= limit) return;
-  const uint16_t* s = src + b * rows * C;
+  const uint16_t* s = src + (row_map ? 0 : b * rows * C);
   for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {  // 16 uint4 per 128-col row
     const int rr = i >> 4, q = i & 15;
-    const uint4 u = (r0 + rr < rows)
-                        ? *reinterpret_cast<const uint4*>(s + (r0 + rr) * C + c0 + q * 8)
-                        : make_uint4(0u, 0u, 0u, 0u);
+    long long sr = r0 + rr;
+    if (sr >= rows) sr = -1;
+    else if (row_map) sr = row_map[sr];
+    const uint4 u = sr >= 0 ? *reinterpret_cast<const uint4*>(s + sr * C + c0 + q * 8) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t* t = reinterpret_cast<uint32_t*>(&tile[rr][q * 8]);
     t[0] = u.x; t[1] = u.y; t[2] = u.z; t[3] = u.w;
   }
@@ -150,6 +107,117 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
     d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
     sfb[sf_byte_offset(c0 + c, r0 + g * 32, k_tiles)] = static_cast<uint8_t>(sb);
   }
+  if (codes_rows) {
+    // row-wise codes of the same tile: thread t takes row t/2, 64 columns
+    const int rr = threadIdx.x >> 1;
+    const int cc = (threadIdx.x & 1) * 64;
+    const long long grow = b * rows + r0 + rr;
+    uint4* d4 = reinterpret_cast<uint4*>(codes_rows + grow * C + c0 + cc);
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(static_cast<uint32_t>(tile[rr][cc + blk * 32 + i]) << 16);
+      uint32_t w[8];
+      const uint32_t sb = quant_block32(v, w);
+      d4[2 * blk] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[2 * blk + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      sf_rows[sf_byte_offset(grow, c0 + cc + blk * 32, C / 128)] = static_cast<uint8_t>(sb);
+    }
+  }
+}
+
+// Dispatch with quantisation: warp per token, the token's row is quantised along d
+// once (a lane per 128-column block) and its codes and scale words are copied to the
+// token's k rows; blocks past the token blocks zero the codes and scales of one
+// expert's padding rows.  FROM_ROUTE also computes the rows and writes the maps (as
+// moe_permute); otherwise rows come from token_to_row (as moe_combine_bwd).
+template <bool FROM_ROUTE>
+__global__ void __launch_bounds__(256) scatter_quant_kernel(
+    const uint16_t* __restrict__ src, int T, int d, int E, int k, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ split_sizes,
+    const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ block_base,
+    const int32_t* __restrict__ local_rank, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    int32_t* __restrict__ row_to_token, int32_t* __restrict__ token_to_row, float* __restrict__ w_rows,
+    int token_blocks, int rows_cap, int32_t* __restrict__ status) {
+  __shared__ int s_rows[8][32];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int kt = d / 128;
+  if (static_cast<int>(blockIdx.x) < token_blocks) {
+    const int t = blockIdx.x * 8 + wib;
+    if (t >= T) return;
+    if (lane < k) {
+      const long long gi = static_cast<long long>(t) * k + lane;
+      int r;
+      if (FROM_ROUTE) {
+        const int e = topk_idx[gi];
+        r = row_offsets[e] + block_base[static_cast<long long>(t / ROUTE_TOKENS) * E + e] + local_rank[gi];
+        if (r < 0 || r >= rows_cap) {
+          set_status(status, MOE_ERR_INVARIANT);
+          r = -1;
+        } else {
+          row_to_token[r] = t;
+          w_rows[r] = topk_w[gi];
+        }
+        token_to_row[gi] = r;
+      } else {
+        r = token_to_row[gi];
+        if (r < 0 || r >= rows_cap) r = -1;
+      }
+      s_rows[wib][lane] = r;
+    }
+    __syncwarp();
+    for (int cb = lane; cb < kt; cb += 32) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<long long>(t) * d + cb * 128);
+      uint32_t code[4][8];
+      uint32_t word = 0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = s4[g * 4 + q];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[q * 8 + 2 * i] = bf16_lo(w[i]);
+            v[q * 8 + 2 * i + 1] = bf16_hi(w[i]);
+          }
+        }
+        word |= quant_block32(v, code[g]) << (8 * g);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int r = s_rows[wib][j];
+        if (r < 0) continue;
+        uint4* d4 = reinterpret_cast<uint4*>(codes + static_cast<long long>(r) * d + cb * 128);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          d4[2 * g] = make_uint4(code[g][0], code[g][1], code[g][2], code[g][3]);
+          d4[2 * g + 1] = make_uint4(code[g][4], code[g][5], code[g][6], code[g][7]);
+        }
+        *reinterpret_cast<uint32_t*>(sf + sf_byte_offset(r, static_cast<long long>(cb) * 128, kt)) = word;
+      }
+    }
+  } else {
+    const int e = blockIdx.x - token_blocks;
+    const int r0 = max(0, row_offsets[e] + split_sizes[e]);
+    const int r1 = min(rows_cap, row_offsets[e + 1]);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const long long d16 = d / 16;
+    for (long long i = threadIdx.x; i < static_cast<long long>(r1 - r0) * d16; i += blockDim.x)
+      reinterpret_cast<uint4*>(codes + static_cast<long long>(r0) * d)[i] = z;
+    for (long long i = threadIdx.x; i < static_cast<long long>(r1 - r0) * kt; i += blockDim.x) {
+      const long long r = r0 + i / kt;
+      *reinterpret_cast<uint32_t*>(sf + sf_byte_offset(r, (i % kt) * 128, kt)) = 0u;
+    }
+    if (FROM_ROUTE) {
+      for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        row_to_token[r] = -1;
+        w_rows[r] = 0.0f;
+      }
+    }
+  }
 }
 
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
@@ -163,11 +231,32 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
 }
 
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
-                                uint8_t* codes, uint8_t* sf, cudaStream_t stream) {
+                                uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map,
+                                uint8_t* codes_rows, uint8_t* sf_rows) {
   if (rows == 0 || batch == 0) return cudaSuccess;
-  dim3 grid(C / 128, static_cast<unsigned>(rows / 128), batch);
-  quant_cols_t_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), rows, C, nrows_dev, codes,
-                                                sf);
+  dim3 grid(C / 128, static_cast<unsigned>(rows / 128), batch);  // callers pass rows % 128 == 0
+  quant_cols_t_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), rows, C, nrows_dev, codes, sf,
+                                                row_map, codes_rows, sf_rows);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_quant(bool from_route, const void* src, int T, int d, int E, int k,
+                                 const int32_t* topk_idx, const float* topk_w, const int32_t* split_sizes,
+                                 const int32_t* row_offsets, const RouteScratch* ws, uint8_t* codes, uint8_t* sf,
+                                 int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
+                                 int32_t* status, cudaStream_t stream) {
+  const int token_blocks = (T + 7) / 8;
+  const int grid = token_blocks + E;
+  if (from_route)
+    scatter_quant_kernel<true><<<grid, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(src), T, d, E, k, topk_idx, topk_w, split_sizes, row_offsets, ws->block_base,
+        ws->local_rank, codes, sf, row_to_token, token_to_row, w_rows, token_blocks, rows_cap, status);
+  else
+    scatter_quant_kernel<false><<<grid, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(src), T, d, E, k, nullptr, nullptr, split_sizes, row_offsets, nullptr,
+        nullptr, codes, sf, nullptr, const_cast<int32_t*>(token_to_row), nullptr, token_blocks, rows_cap,
+        nullptr);
   count_launch();
   return cudaGetLastError();
 }

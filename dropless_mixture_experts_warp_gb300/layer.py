@@ -96,24 +96,27 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
 
 def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None):
     dm = b.dims
+    mx8 = dm.prec == 1
     shared_out = None
-    if dm.f_shared and dm.prec == 1:
+    if dm.f_shared and mx8:
         B.moe_mx_quantize_shared_weights(dm, w_gu_s, w_d_s, b.wq_s, stream)
-        B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
+        B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.y_s, b.status, stream)
         shared_out = b.y_s
     elif dm.f_shared:
         B.moe_shared_mlp_fwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
         shared_out = b.y_s
     B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
                      b.workspace, b.status, stream)
-    B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
-                  b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
-    if dm.prec == 1:
-        # 16-bit master weights are quantised every step (they change every optimiser step)
+    if mx8:
+        # the 16-bit master weights are quantised every step (they change every optimiser step)
         B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
-        B.moe_gemm_gate_up_mx(dm, b.xp, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.h, b.status, stream)
-        B.moe_gemm_down_mx(dm, b.h, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
+        B.moe_permute_mx(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.mx_ws,
+                         b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
+        B.moe_gemm_gate_up_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.status, stream)
+        B.moe_gemm_down_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
     else:
+        B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
+                      b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
         B.moe_grouped_mlp_fwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.y_rows, b.status,
                               stream)
     B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, shared_out, b.y, stream)
@@ -121,24 +124,27 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
 
 
 def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None, w_d_s=None):
+    """x (the forward's input) is needed by the shared expert and by the MXFP8 path."""
     dm = b.dims
+    mx8 = dm.prec == 1
     shared_dx = None
-    if dm.f_shared and dm.prec == 1:
-        B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s,
-                                b.dw_d_s, b.status, stream)
+    if dm.f_shared and mx8:
+        B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
+                                stream)
         shared_dx = b.dx_s
     elif dm.f_shared:
         B.moe_shared_mlp_bwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s, b.dw_gu_s, b.dw_d_s,
                              b.status, stream)
         shared_dx = b.dx_s
-    B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
-    if dm.prec == 1:
-        B.moe_gemm_down_dgrad_mx(dm, b.dy_rows, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dgu, b.dw_rows,
-                                 b.workspace, b.status, stream)
-        B.moe_gemm_down_wgrad_mx(dm, b.dy_rows, b.h, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
-        B.moe_gemm_gate_up_dgrad_mx(dm, b.dgu, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
-        B.moe_gemm_gate_up_wgrad_mx(dm, b.dgu, b.xp, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+    if mx8:
+        B.moe_combine_bwd_mx(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.mx_ws, stream)
+        B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace,
+                                 b.status, stream)
+        B.moe_gemm_down_wgrad_mx(dm, dy, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+        B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
+        B.moe_gemm_gate_up_wgrad_mx(dm, x, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
     else:
+        B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu,
                               b.dxp, b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)
     B.moe_combine_fwd(dm, b.dxp, b.token_to_row, shared_dx, b.dx, stream)

@@ -353,61 +353,70 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
                           moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream);
 
 /*
- * The grouped GEMMs with MXFP8 operands (dims->prec may be either value; f % 128 == 0).
- * Each call first quantises its activation operands along the contraction axis of
- * its GEMM (row blocks along d, f or 2f; column blocks of 32 rows inside each
- * 128-aligned expert segment for the weight gradients) into `mx_ws`, then runs the
- * block-scaled tcgen05 GEMM with the same fused epilogues and the same bf16 outputs
- * as the bf16 calls.  The backward treats quantisation as the identity.
+ * The layer with MXFP8 GEMM operands (dims->prec may be either value; f % 128 == 0).
+ * Every GEMM operand is quantised along its own contraction axis, in the kernel that
+ * produces it: the routed token rows by moe_permute_mx and dY's rows by
+ * moe_combine_bwd_mx (one quantisation per token, copied to its k rows); h and dG|dU
+ * in the epilogues of the gate/up and SwiGLU' GEMMs, from fp32, both along their rows
+ * and down their columns in 32-row blocks of the 128-aligned expert segments; the
+ * column-wise codes of the routed x and dY rows by the weight-gradient calls, which
+ * gather them from x / dY through row_to_token.  bf16 copies of Xp, h, dY rows and
+ * dG|dU are never written.  The GEMMs are the block-scaled tcgen05 kernel with fp32
+ * accumulation and the same bf16 outputs (gu, y_rows, dxp, dW) as the bf16 calls.
+ * The backward treats quantisation as the identity.
  *   wq:    >= moe_mx_weights_size bytes, filled by moe_mx_quantize_weights from the
- *          bf16 master weights (W_gu along d and along 2f, W_d along f and along d);
- *          refill it whenever the weights change.
- *   mx_ws: >= moe_mx_workspace_size bytes of caller scratch for the quantised
- *          activations; the calls of one step must share it (the gate/up and down
- *          weight-gradient calls reuse nothing, each quantises what it reads).
- * Same arguments otherwise as moe_gemm_gate_up, moe_gemm_down, moe_gemm_down_dgrad,
- * moe_gemm_down_wgrad, moe_gemm_gate_up_dgrad, moe_gemm_gate_up_wgrad.
+ *          bf16 master weights (W_gu along d and along 2f, W_d along f and along d;
+ *          one read of each weight); refill it whenever the weights change.
+ *   mx_ws: >= moe_mx_workspace_size bytes of caller scratch holding the quantised
+ *          activations of one step; all the calls of the step share it, in this order:
+ *          moe_permute_mx, moe_gemm_gate_up_mx, moe_gemm_down_mx, (combine),
+ *          moe_combine_bwd_mx, moe_gemm_down_dgrad_mx, moe_gemm_down_wgrad_mx,
+ *          moe_gemm_gate_up_dgrad_mx, moe_gemm_gate_up_wgrad_mx.
+ * Other arguments as in the bf16 calls of the same names without "_mx".
  */
 size_t moe_mx_weights_size(const moe_dims* dims);
 size_t moe_mx_workspace_size(const moe_dims* dims);
 moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, const moe_bf16* w_d, void* wq,
                                    void* stream);
-moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const moe_bf16* xp, const int32_t* row_offsets,
-                               const float* w_rows, const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* h,
-                               int32_t* dev_status, void* stream);
-moe_status moe_gemm_down_mx(const moe_dims* dims, const moe_bf16* h, const int32_t* row_offsets, const void* wq,
-                            void* mx_ws, moe_bf16* y_rows, int32_t* dev_status, void* stream);
-moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const int32_t* row_offsets,
-                                  const float* w_rows, const void* wq, void* mx_ws, const moe_bf16* gu,
-                                  moe_bf16* dgu, float* dw_rows, void* workspace, int32_t* dev_status,
-                                  void* stream);
-moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy_rows, const moe_bf16* h,
+moe_status moe_permute_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, const float* topk_w,
+                          const int32_t* split_sizes, const int32_t* row_offsets, const void* workspace,
+                          void* mx_ws, int32_t* row_to_token, int32_t* token_to_row, float* w_rows,
+                          int32_t* dev_status, void* stream);
+moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                               const void* wq, void* mx_ws, moe_bf16* gu, int32_t* dev_status, void* stream);
+moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq, void* mx_ws,
+                            moe_bf16* y_rows, int32_t* dev_status, void* stream);
+moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* token_to_row,
+                              const int32_t* split_sizes, const int32_t* row_offsets, void* mx_ws, void* stream);
+moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, const moe_bf16* gu, float* dw_rows, void* workspace,
+                                  int32_t* dev_status, void* stream);
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
                                   const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
                                   void* stream);
-moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const int32_t* row_offsets,
-                                     const void* wq, void* mx_ws, moe_bf16* dxp, int32_t* dev_status,
+moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq,
+                                     void* mx_ws, moe_bf16* dxp, int32_t* dev_status, void* stream);
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* row_to_token,
+                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu, int32_t* dev_status,
                                      void* stream);
-moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* dgu, const moe_bf16* xp,
-                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu,
-                                     int32_t* dev_status, void* stream);
 
 /*
  * The shared expert with MXFP8 GEMM operands (DeepSeek-V3 shape in MXFP8; f_shared and
  * T multiples of 128).  wq_s (>= moe_mx_shared_weights_size bytes) holds W_gu_s and
  * W_d_s quantised along both of their axes, filled by moe_mx_quantize_shared_weights;
  * mx_ws_s (>= moe_mx_shared_workspace_size bytes) is scratch for the quantised
- * activations.  Otherwise as moe_shared_mlp_fwd / moe_shared_mlp_bwd.
+ * activations (h_s and dG|dU of the shared expert are kept only as codes there).
+ * Otherwise as moe_shared_mlp_fwd / moe_shared_mlp_bwd.
  */
 size_t moe_mx_shared_weights_size(const moe_dims* dims);
 size_t moe_mx_shared_workspace_size(const moe_dims* dims);
 moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* w_gu_s, const moe_bf16* w_d_s,
                                           void* wq_s, void* stream);
 moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 moe_bf16* gu_s, moe_bf16* h_s, moe_bf16* y_s, int32_t* dev_status, void* stream);
+                                 moe_bf16* gu_s, moe_bf16* y_s, int32_t* dev_status, void* stream);
 moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 const moe_bf16* gu_s, const moe_bf16* h_s, const moe_bf16* dy, moe_bf16* dgu_s,
-                                 moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s, int32_t* dev_status,
-                                 void* stream);
+                                 const moe_bf16* gu_s, const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s,
+                                 moe_bf16* dw_d_s, int32_t* dev_status, void* stream);
 
 /*
  * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the
