@@ -75,6 +75,20 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint
   return make_map(m, base, inner, outer, box_inner, box_outer);
 }
 
+// 2-D bf16 output [rows][ld] (cols <= ld used) for the tensor store of the GEMM
+// epilogue: box 32 x 32, 64-byte swizzle; rows beyond `rows` are not written.
+bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -147,15 +147,98 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
 
 __device__ __forceinline__ float sigmoidf_(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
-// Hand-off of the dw partials between the two epilogue warps of a TMEM lane
-// quarter (second half -> first half), through mbarriers so every wait is bounded.
+// Shared state of the epilogue warps: the hand-off of the dw partials between the
+// two epilogue warps of a TMEM lane quarter (second half -> first half, through
+// mbarriers so every wait is bounded) and, for the *_MX epilogues, this warp's
+// 32 x 17 fp32 transpose buffer.
 struct DwHandoff {
   float* s_dw;             // [BM] partials of the second half
   uint64_t* full;          // [4] second half has written s_dw
   uint64_t* empty;         // [4] first half has read it
   uint32_t* phase;         // this thread's phase bit
   volatile int* abort_flag;
+  float* xbuf = nullptr;   // [32][17] per warp (MX epilogues)
 };
+
+constexpr int XBUF_FLOATS = 32 * 17;
+
+// Column-wise MXFP8 codes of a 32-row x 32-column fp32 chunk held one row per lane
+// (v[i] = row `lane`, column col0 + i).  The warp's 32 rows are one 32-row block of
+// every column: the block scale comes from the column's maximum over them.  The
+// chunk goes through shared memory in two 16-column halves; then lane l holds rows
+// (l >> 4) * 16 .. +16 of column l & 15, so the maximum needs one shuffle and the
+// 16 codes leave as one 16-byte store.  codes: [cols][ld] (K = rows), scales: SF tiles.
+__device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* xb, int lane, uint8_t* codes,
+                                                   uint8_t* scales, long long ld, int ktiles, int col0,
+                                                   long long rblk, bool ok) {
+  const int cc = lane & 15, hh = lane >> 4;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xb[lane * 17 + j] = v[16 * s + j];
+    __syncwarp();
+    float cv[16];
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      cv[i] = xb[(hh * 16 + i) * 17 + cc];
+      a = fmaxf(a, fabsf(cv[i]));
+    }
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+    const int e = mx_scale_exp(a);
+    const float sc = exp2_neg(e);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = cvt_e4m3x2(cv[4 * q] * sc, cv[4 * q + 1] * sc) | (cvt_e4m3x2(cv[4 * q + 2] * sc, cv[4 * q + 3] * sc) << 16);
+    const int col = col0 + 16 * s + cc;
+    if (ok) {
+      *reinterpret_cast<uint4*>(codes + static_cast<long long>(col) * ld + rblk + hh * 16) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+      if (hh == 0) scales[sf_byte_offset(col, rblk, ktiles)] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+// STORE epilogue through shared memory and the tensor store: the warp owns 32 rows
+// of the tile (output rows y0 .. y0 + 31).  Each 32-column chunk is read from TMEM,
+// rounded to bf16 and written by row into one of the warp's two 2 KB buffers
+// (64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3), which
+// keeps the writes free of bank conflicts); one lane then stores the 32 x 32 box.
+// The accumulator columns are free once read: the stores drain while the next tile
+// accumulates.  `stg` is 1024-byte aligned; `nstore` counts the warp's stores.
+__device__ __forceinline__ void store_tile_tma(const CUtensorMap* tmC, const TileCoord& c, uint32_t tbase, int BN,
+                                               int lane, int y0, uint8_t* stg, uint32_t& nstore) {
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t r[32];
+    if (c.kblocks > 0) {
+      tmem_ld32(tbase + c0, r);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    uint8_t* buf = stg + (nstore & 1u) * 2048;
+    if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two chunks ago has read it
+    __syncwarp();
+    const uint32_t row_addr = smem_u32(buf) + lane * 64;
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(row_addr + ((j ^ sw) << 4), pack_bf16(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                   pack_bf16(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                   pack_bf16(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                   pack_bf16(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, buf, c.out_col + c0, y0);
+      bulk_commit();
+    }
+    ++nstore;
+  }
+}
 
 // Epilogue of one tile for one thread (one accumulator row, half of the columns):
 // reads fp32 accumulator columns from TMEM (32 at a time) and applies the fused EPI
@@ -267,19 +350,8 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
         p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float a = fabsf(hv[i]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        const int e = mx_scale_exp(a);
-        const uint32_t code = cvt_e4m3x2(hv[i] * exp2_neg(e), 0.0f) & 0xFFu;
-        if (row_ok) {
-          p.q_cols[static_cast<long long>(col + i) * p.q_cols_ld + row] = static_cast<uint8_t>(code);
-          if (lane == 0)
-            p.q_cols_sf[sf_byte_offset(col + i, rblk, p.q_cols_ktiles)] = static_cast<uint8_t>(e + 127);
-        }
-      }
+      quant_cols_chunk32(hv, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk,
+                         rblk + 32 <= p.row_limit);
     }
   } else if (EPI == EPI_SWIGLU_BWD_MX) {
     // as EPI_SWIGLU_BWD, but dG|dU are quantised from fp32 along their row (blocks of
@@ -336,21 +408,10 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
         p.q_rows_sf[sf_byte_offset(row, p.f + col, ld2 / 128)] = static_cast<uint8_t>(sb);
       }
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float v = i < 32 ? dg[i] : du[i - 32];
-        float a = fabsf(v);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        const int e = mx_scale_exp(a);
-        const uint32_t code = cvt_e4m3x2(v * exp2_neg(e), 0.0f) & 0xFFu;
-        const int qc = i < 32 ? col + i : p.f + col + (i - 32);
-        if (row_ok) {
-          p.q_cols[static_cast<long long>(qc) * p.q_cols_ld + row] = static_cast<uint8_t>(code);
-          if (lane == 0)
-            p.q_cols_sf[sf_byte_offset(qc, rblk, p.q_cols_ktiles)] = static_cast<uint8_t>(e + 127);
-        }
-      }
+      const bool blk_ok = rblk + 32 <= p.row_limit;
+      quant_cols_chunk32(dg, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
+      quant_cols_chunk32(du, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, p.f + col, rblk,
+                         blk_ok);
     }
     if (NH == 1) {
       if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;

@@ -3,8 +3,9 @@
 // Same roles and schedule as the bf16 kernel (gemm.cuh): warp 0 loads, warp 1 issues,
 // the warps after them run the shared epilogue.  Differences:
 //   * operands are E4M3 codes, both K-major, 128 codes (128 bytes) per stage row;
-//   * each stage also carries the E8M0 scale tiles of its A rows (512 B) and B rows
-//     (512 B per 128 rows), fetched with contiguous bulk copies; the MMA warp moves
+//   * each stage also has the E8M0 scale tiles of its A rows (512 B) and B rows
+//     (512 B per 128 rows), fetched with contiguous bulk copies into a region after
+//     the code stages; the MMA warp moves
 //     them into TMEM with tcgen05.cp (32x128b, replicated to the four lane quarters)
 //     and every MMA (K = 32) selects its byte of the scale words with the
 //     scale-factor id of the instruction descriptor;
@@ -19,18 +20,26 @@ namespace moe {
 constexpr int MX_BK = 128;                                  // K elements (= bytes) per stage
 constexpr int MX_A_BYTES = BM * MX_BK;                      // 16 KB
 constexpr int MX_B_BYTES_MAX = 256 * MX_BK;                 // 32 KB
-constexpr int MX_SFA_OFF = MX_A_BYTES + MX_B_BYTES_MAX;     // scale tiles after the codes
-constexpr int MX_SFB_OFF = MX_SFA_OFF + 512;
-constexpr int MX_STAGE_BYTES = 50 * 1024;                   // 48 KB codes + 1.5 KB scales, 1 KB aligned
+constexpr int MX_STAGE_BYTES = MX_A_BYTES + MX_B_BYTES_MAX;  // 48 KB of codes per stage
 constexpr int MX_STAGES = 4;
-constexpr int MX_SMEM_BYTES = MX_STAGES * MX_STAGE_BYTES + 1024;
+// scale tiles of stage s: SFA at MX_SF_OFF + s * MX_SF_STAGE, SFB (up to 2 tiles) 512 B after
+constexpr int MX_SF_OFF = MX_STAGES * MX_STAGE_BYTES;
+constexpr int MX_SF_STAGE = 1536;
+constexpr int MX_XBUF_OFF = MX_SF_OFF + MX_STAGES * MX_SF_STAGE;  // transpose buffers of the epilogue warps
+__host__ __device__ constexpr bool epi_quantises(int epi) { return epi == 3 || epi == 4; }
+// per epilogue warp: a transpose buffer (quantising epilogues) or two 2 KB staging
+// buffers of the tensor store (EPI_STORE)
+__host__ __device__ constexpr int mx_smem_bytes(int epi) {
+  return MX_XBUF_OFF + (epi_quantises(epi) ? epi_warps(epi) * XBUF_FLOATS * 4 : 0) +
+         (epi == 0 ? epi_warps(epi) * 4096 : 0) + 1024;
+}
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
 
 template <int SCHED, int EPI>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
-    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[MX_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[MX_STAGES];
@@ -62,7 +71,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (EPI == EPI_STORE) tma_prefetch_desc(&tmC);
+  }
   if (warp == 1) { tmem_alloc(&s_tmem_base, TMEM_COLS); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
@@ -89,6 +102,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                                  WAIT_LIMIT_CYCLES)) { ok = false; break; }
           uint8_t* sa = smem + stage * MX_STAGE_BYTES;
           uint8_t* sb = sa + MX_A_BYTES;
+          uint8_t* sf = smem + MX_SF_OFF + stage * MX_SF_STAGE;
           uint64_t* bar = &full_bar[stage];
           mbar_arrive_expect_tx(bar, stage_tx);
           armed |= 1u << stage;
@@ -96,22 +110,22 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           const int ka = c.a_k + kb * MX_BK;     // K index of A (and of B: b_k == a_k here)
           const int kbt = ka / MX_BK;
           tma_load_2d(sa, &tmA, bar, ka, c.a_m);
-          bulk_load(sa + MX_SFA_OFF,
+          bulk_load(sf,
                     p.sfa + (static_cast<size_t>(c.a_m / 128) * p.a_sf_ktiles + kbt) * 512, 512, bar);
           const int kbb = c.b_k + kb * MX_BK;
           const int kbtb = kbb / MX_BK;
           if (gu_split(EPI)) {                    // gate rows then up rows, 128 each
             tma_load_2d(sb, &tmB, bar, kbb, c.b_n);
             tma_load_2d(sb + (BN / 2) * MX_BK, &tmB, bar, kbb, c.b_n + p.f);
-            bulk_load(sa + MX_SFB_OFF,
+            bulk_load(sf + 512,
                       p.sfb + (static_cast<size_t>(c.b_n / 128) * p.b_sf_ktiles + kbtb) * 512, 512, bar);
-            bulk_load(sa + MX_SFB_OFF + 512,
+            bulk_load(sf + 1024,
                       p.sfb + (static_cast<size_t>((c.b_n + p.f) / 128) * p.b_sf_ktiles + kbtb) * 512, 512,
                       bar);
           } else {
             tma_load_2d(sb, &tmB, bar, kbb, c.b_n);
             for (int i = 0; i < BN / 128; ++i)
-              bulk_load(sa + MX_SFB_OFF + 512 * i,
+              bulk_load(sf + 512 + 512 * i,
                         p.sfb + (static_cast<size_t>(c.b_n / 128 + i) * p.b_sf_ktiles + kbtb) * 512, 512, bar);
           }
           if (++stage == MX_STAGES) { stage = 0; phase ^= 1; }
@@ -139,12 +153,13 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * MX_STAGE_BYTES);
           const uint32_t sb = sa + MX_A_BYTES;
+          const uint32_t sf = smem_u32(smem + MX_SF_OFF + stage * MX_SF_STAGE);
           const uint32_t sfa_t = tmem_base + MX_SF_TMEM_COL + stage * MX_SF_COLS_PER_STAGE;
           const uint32_t sfb_t = sfa_t + 4;
           // scale tiles: 32 rows x 16 B each, 8-row core matrices 128 B apart
-          tc_cp_32x128b_x4(sfa_t, smem_desc_plain(sa + MX_SFA_OFF, 0, 128));
+          tc_cp_32x128b_x4(sfa_t, smem_desc_plain(sf, 0, 128));
           for (int i = 0; i < BN / 128; ++i)
-            tc_cp_32x128b_x4(sfb_t + 4 * i, smem_desc_plain(sa + MX_SFB_OFF + 512 * i, 0, 128));
+            tc_cp_32x128b_x4(sfb_t + 4 * i, smem_desc_plain(sf + 512 + 512 * i, 0, 128));
 #pragma unroll
           for (int kk = 0; kk < MX_BK / 32; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
@@ -168,20 +183,30 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
-    const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
+    float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
+    uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 4096;
+    uint32_t nstore = 0;
+    const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const long long row = c.out_row + row_in_tile;
-      if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile, hand))
+      if (EPI == EPI_STORE) {
+        // output rows: the padded row space (SCHED_ROWS) or expert e's block of M rows
+        const long long y0 = (SCHED == SCHED_KGROUP ? static_cast<long long>(c.e) * p.M : 0ll) + c.out_row + q * 32;
+        store_tile_tma(&tmC, c, tbase, BN, lane, static_cast<int>(y0), stg, nstore);
+      } else if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile,
+                                     hand)) {
         break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
       if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
     }
+    if (EPI == EPI_STORE && lane == 0) bulk_wait_all();  // the tensor stores are complete
   }
 
   tc_fence_before();

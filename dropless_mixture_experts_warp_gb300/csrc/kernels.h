@@ -96,6 +96,7 @@ cudaError_t launch_scatter_quant(bool from_route, const void* src, int T, int d,
                                  int32_t* status, cudaStream_t stream);
 RouteScratch route_scratch(const moe_dims& d, void* ws);
 float* workspace_dw_part(const moe_dims& d, void* ws);
+bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,

@@ -75,6 +75,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     # with two experts, so an ncu capture stays near 2 GB of device memory
     "mixtral-e2": MoEConfig("mixtral-e2", T=4096, d=4096, f=14336, E=2, k=1, score=SOFTMAX,
                             bias="normal", bias_param=0.1, seed=1006),
+    # profiling case: the Qwen3-235B-A22B per-expert shapes (about 1024 rows per expert)
+    # with 16 experts, near 2 GB of device memory
+    "qwen235b-e16": MoEConfig("qwen235b-e16", T=2048, d=4096, f=1536, E=16, k=8, score=SOFTMAX,
+                              bias="zero", seed=1007),
     "dsv3": MoEConfig("dsv3", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
                       bias="zipf", bias_param=1.0, forced_empty=4, f_shared=2048, seed=1005),
 }
