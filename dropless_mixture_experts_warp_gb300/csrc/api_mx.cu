@@ -258,7 +258,7 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   float* dw_part = workspace_dw_part(d, workspace);
-  const int bn = bn_mx(d.f);
+  const int bn = 128;
   CUtensorMap ta, tb;
   if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, R_cap, 128, BM) ||
       !make_tensor_map_u8(&tb, w.d_cols.codes, d.d, static_cast<uint64_t>(d.f) * d.E, 128, bn))

@@ -36,9 +36,10 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES_MAX;
 constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_STRIDE = 256;
-// Epilogue warps: 8 for the SwiGLU' epilogue (two per TMEM lane quarter, splitting
-// the columns), 4 otherwise.  Block = producer warp + MMA warp + epilogue warps.
-__host__ __device__ constexpr int epi_warps(int epi) { return (epi == 2 || epi == 4) ? 8 : 4; }
+// Epilogue warps: 8 for the SwiGLU' epilogues and the quantising SwiGLU epilogue (two
+// per TMEM lane quarter, splitting the columns), 4 otherwise.  Block = producer warp +
+// MMA warp + epilogue warps.
+__host__ __device__ constexpr int epi_warps(int epi) { return (epi == 2 || epi == 3 || epi == 4) ? 8 : 4; }
 __host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int MAX_EXPERTS = 1024;
 constexpr long long WAIT_LIMIT_CYCLES = 1ll << 31;  // about one second

@@ -7,7 +7,7 @@
 
 namespace moe {
 
-constexpr int ROUTE_TOKENS = 256;  // tokens per routing block
+constexpr int ROUTE_TOKENS = 128;  // tokens per routing block (16 per warp)
 constexpr int ROW_ALIGN = MOE_ROW_ALIGN;
 
 inline int route_blocks(int T) { return T > 0 ? (T + ROUTE_TOKENS - 1) / ROUTE_TOKENS : 1; }

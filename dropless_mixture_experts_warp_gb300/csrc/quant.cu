@@ -65,13 +65,22 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 // reads zeros) -- the column-wise codes of a permuted matrix straight from its
 // source; codes_rows/sf_rows also write the row-wise codes of the same tile
 // ([batch*rows][C], K = C), so a weight is read once for both orientations.
+// The codes of a tile and its scales (exactly one 512-byte SF tile per orientation)
+// are assembled in shared memory and leave as whole 128-byte lines.
+constexpr int QC_LD = 128 + 16;  // padded code rows in shared memory (bytes)
+constexpr int QC_SMEM = 128 * (128 + 8) * 2 + 2 * 128 * QC_LD + 2 * 512;
+
 __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __restrict__ src, long long rows,
                                                            int C, const int32_t* __restrict__ nrows_dev,
                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                            const int32_t* __restrict__ row_map,
                                                            uint8_t* __restrict__ codes_rows,
                                                            uint8_t* __restrict__ sf_rows) {
-  __shared__ uint16_t tile[128][128 + 8];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  uint16_t(*tile)[128 + 8] = reinterpret_cast<uint16_t(*)[128 + 8]>(qsm);
+  uint8_t* ct = qsm + 128 * (128 + 8) * 2;  // column-wise codes [128 cols][QC_LD]
+  uint8_t* rt = ct + 128 * QC_LD;           // row-wise codes [128 rows][QC_LD]
+  uint8_t* sft = rt + 128 * QC_LD;          // the two SF tiles
   const long long b = blockIdx.z;
   const long long r0 = static_cast<long long>(blockIdx.y) * 128;
   const int c0 = blockIdx.x * 128;
@@ -79,21 +88,26 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   if (nrows_dev) limit = min(limit, static_cast<long long>(*nrows_dev));
   if (r0 >= limit) return;
   const uint16_t* s = src + (row_map ? 0 : b * rows * C);
-  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {  // 16 uint4 per 128-col row
-    const int rr = i >> 4, q = i & 15;
-    long long sr = r0 + rr;
-    if (sr >= rows) sr = -1;
-    else if (row_map) sr = row_map[sr];
-    const uint4 u = sr >= 0 ? *reinterpret_cast<const uint4*>(s + sr * C + c0 + q * 8) : make_uint4(0u, 0u, 0u, 0u);
-    uint32_t* t = reinterpret_cast<uint32_t*>(&tile[rr][q * 8]);
-    t[0] = u.x; t[1] = u.y; t[2] = u.z; t[3] = u.w;
+  {
+    uint4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // 16 uint4 per 128-column row, 8 per thread, all in flight
+      const int i = threadIdx.x + 256 * j;
+      const int rr = i >> 4, q = i & 15;
+      long long sr = r0 + rr;
+      if (sr >= rows) sr = -1;
+      else if (row_map) sr = row_map[sr];
+      u[j] = sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(s + sr * C + c0 + q * 8)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + 256 * j;
+      *reinterpret_cast<uint4*>(&tile[i >> 4][(i & 15) * 8]) = u[j];
+    }
   }
   __syncthreads();
   const int c = threadIdx.x & 127;
   const int gpair = threadIdx.x >> 7;  // 0: row blocks 0,1; 1: row blocks 2,3
-  const long long k_tiles = rows / 128;
-  uint8_t* cb = codes + b * static_cast<long long>(C) * rows + static_cast<long long>(c0 + c) * rows;
-  uint8_t* sfb = sf + b * (static_cast<long long>(C) * rows / 32);
 #pragma unroll
   for (int gg = 0; gg < 2; ++gg) {
     const int g = gpair * 2 + gg;
@@ -102,17 +116,15 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[g * 32 + i][c]) << 16);
     uint32_t w[8];
     const uint32_t sb = quant_block32(v, w);
-    uint4* d4 = reinterpret_cast<uint4*>(cb + r0 + g * 32);
+    uint4* d4 = reinterpret_cast<uint4*>(ct + c * QC_LD + g * 32);
     d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
     d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    sfb[sf_byte_offset(c0 + c, r0 + g * 32, k_tiles)] = static_cast<uint8_t>(sb);
+    sft[sf_byte_offset(c, g * 32, 1)] = static_cast<uint8_t>(sb);
   }
   if (codes_rows) {
     // row-wise codes of the same tile: thread t takes row t/2, 64 columns
     const int rr = threadIdx.x >> 1;
     const int cc = (threadIdx.x & 1) * 64;
-    const long long grow = b * rows + r0 + rr;
-    uint4* d4 = reinterpret_cast<uint4*>(codes_rows + grow * C + c0 + cc);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       float v[32];
@@ -121,9 +133,39 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
         v[i] = __uint_as_float(static_cast<uint32_t>(tile[rr][cc + blk * 32 + i]) << 16);
       uint32_t w[8];
       const uint32_t sb = quant_block32(v, w);
-      d4[2 * blk] = make_uint4(w[0], w[1], w[2], w[3]);
-      d4[2 * blk + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sf_rows[sf_byte_offset(grow, c0 + cc + blk * 32, C / 128)] = static_cast<uint8_t>(sb);
+      uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+    }
+  }
+  __syncthreads();
+  // column-wise codes: 128 lines of 128 bytes at codes + (c0 + line) * rows + r0
+  uint8_t* cb = codes + b * static_cast<long long>(C) * rows;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = threadIdx.x + 256 * j;
+    const int line = i >> 3, q = i & 7;
+    *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + line) * rows + r0 + q * 16) =
+        *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
+  }
+  const long long k_tiles = rows / 128;
+  if (threadIdx.x < 32) {
+    uint8_t* sfb = sf + b * (static_cast<long long>(C) * rows / 32) + ((c0 / 128) * k_tiles + r0 / 128) * 512;
+    reinterpret_cast<uint4*>(sfb)[threadIdx.x] = reinterpret_cast<const uint4*>(sft)[threadIdx.x];
+  }
+  if (codes_rows) {
+    const long long grow0 = b * rows + r0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = threadIdx.x + 256 * j;
+      const int line = i >> 3, q = i & 7;
+      *reinterpret_cast<uint4*>(codes_rows + (grow0 + line) * C + c0 + q * 16) =
+          *reinterpret_cast<const uint4*>(rt + line * QC_LD + q * 16);
+    }
+    if (threadIdx.x >= 32 && threadIdx.x < 64) {
+      uint8_t* sfr = sf_rows + ((grow0 / 128) * (C / 128) + c0 / 128) * 512;
+      reinterpret_cast<uint4*>(sfr)[threadIdx.x - 32] = reinterpret_cast<const uint4*>(sft + 512)[threadIdx.x - 32];
     }
   }
 }
@@ -235,7 +277,9 @@ cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int 
                                 uint8_t* codes_rows, uint8_t* sf_rows) {
   if (rows == 0 || batch == 0) return cudaSuccess;
   dim3 grid(C / 128, static_cast<unsigned>(rows / 128), batch);  // callers pass rows % 128 == 0
-  quant_cols_t_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), rows, C, nrows_dev, codes, sf,
+  const cudaError_t e = cudaFuncSetAttribute(quant_cols_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
+  if (e != cudaSuccess) return e;
+  quant_cols_t_kernel<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), rows, C, nrows_dev, codes, sf,
                                                 row_map, codes_rows, sf_rows);
   count_launch();
   return cudaGetLastError();

@@ -7,64 +7,69 @@ namespace moe {
 
 // ============================================================================ route
 
-// One block owns ROUTE_TOKENS consecutive tokens; each warp takes 32 of them, one at
-// a time, with the E logits spread over the lanes.  Selection is k rounds of a
-// warp-wide argmax on (logit, -index), so ties go to the lower expert index.
+// Order-preserving map of a finite fp32 (or -inf) to a nonzero uint32: a > b as
+// floats iff key(a) > key(b); -0 is taken as +0 so that the two tie.  0 = no candidate.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// One block owns ROUTE_TOKENS consecutive tokens; each warp takes ROUTE_TOKENS / 8
+// of them, one at a time, with the E logits spread over the lanes (PL per lane,
+// expert lane + 32 c in slot c).  Selection is k rounds of a warp argmax: the
+// largest order key over the warp (one redux), then the lowest expert index among
+// the lanes holding it (a second redux), so ties go to the lower expert index.
 // Per-block stable ranks come from a bitmask per expert over the block's tokens:
 // rank of token t for expert e = number of set bits below t.  The last block to
 // finish turns the per-block counts into split_sizes, offsets and row_offsets.
+template <int PL>
 __global__ void __launch_bounds__(256) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int score, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* __restrict__ block_hist, int32_t* __restrict__ block_base,
     int32_t* __restrict__ local_rank, int32_t* __restrict__ counter, int32_t* __restrict__ split_sizes,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets, int32_t* __restrict__ status) {
-  extern __shared__ uint32_t masks[];  // [E][ROUTE_TOKENS / 32]
+  extern __shared__ uint32_t masks[];  // [E][ROUTE_TOKENS / 32], then the E totals of the last block
   __shared__ int s_last;
   constexpr int WORDS = ROUTE_TOKENS / 32;
+  constexpr int TPW = ROUTE_TOKENS / 8;  // tokens per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * ROUTE_TOKENS;
 
   for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
 
-  const int per_lane = (E + 31) / 32;  // <= 32
-  for (int i = 0; i < 32; ++i) {
-    const int tl = warp * 32 + i;
+  for (int i = 0; i < TPW; ++i) {
+    const int tl = warp * TPW + i;
     const int t = tok0 + tl;
     if (t >= T) break;
     const float* row = logits + static_cast<long long>(t) * E;
-    float v[32];
+    uint32_t key[PL];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
+    for (int c = 0; c < PL; ++c) {
       const int e = lane + 32 * c;
-      v[c] = (c < per_lane && e < E) ? row[e] : -INFINITY;
+      key[c] = e < E ? order_key(row[e]) : 0u;
     }
-    uint32_t taken = 0u;  // bit c: local candidate c already selected
     int my_e = -1;
     float my_l = 0.0f;
     for (int j = 0; j < k; ++j) {
-      // best remaining candidate of this lane
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+      // this lane's best remaining slot: strict > keeps the lowest slot (lowest index) on ties
+      uint32_t bk = 0u;
+      int bc = 0;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int e = lane + 32 * c;
-        if (c < per_lane && e < E && !((taken >> c) & 1u)) {
-          if (v[c] > bv || (v[c] == bv && e < be) || be == 0x7fffffff) { bv = v[c]; be = e; }
-        }
-      }
-      // warp argmax: larger logit wins, equal logits -> lower index
+      for (int c = 0; c < PL; ++c)
+        if (key[c] > bk) { bk = key[c]; bc = c; }
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+      const int cand = (bk == wk && bk != 0u) ? lane + 32 * bc : 0x7fffffff;
+      const int we = __reduce_min_sync(0xffffffffu, cand);
+      if (we == cand && cand != 0x7fffffff) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
+        for (int c = 0; c < PL; ++c)
+          if (c == bc) key[c] = 0u;  // taken
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) { my_e = be; my_l = bv; }
+      if (lane == j) { my_e = we; my_l = key_value(wk); }
     }
     // weights of the selected experts, lanes 0..k-1
     const float top = __shfl_sync(0xffffffffu, my_l, 0);  // slot 0 holds the largest logit
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
     block_hist[static_cast<long long>(blockIdx.x) * E + e] = cnt;
   }
 
-  // last block: per-expert scan over blocks, then over experts
+  // last block: per-expert exclusive scan over blocks, then over experts
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1) == static_cast<int>(gridDim.x) - 1);
@@ -107,28 +112,57 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
   if (!s_last) return;
   __threadfence();
   const int nb = gridDim.x;
+  int* s_tot = reinterpret_cast<int*>(masks);  // the masks are no longer needed
+  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
+    int run = 0, b = 0;
+    for (; b + 16 <= nb; b += 16) {  // 16 loads in flight per thread
+      int h[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = __ldcg(&block_hist[static_cast<long long>(b + i) * E + e]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        block_base[static_cast<long long>(b + i) * E + e] = run;
+        run += h[i];
+      }
+    }
+    for (; b < nb; ++b) {
       block_base[static_cast<long long>(b) * E + e] = run;
       run += __ldcg(&block_hist[static_cast<long long>(b) * E + e]);
     }
     split_sizes[e] = run;
+    s_tot[e] = run;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long off = 0, roff = 0;
-    for (int e = 0; e < E; ++e) {
-      const int n = split_sizes[e];
+  if (warp == 0) {
+    // lane l owns experts [l * per, (l + 1) * per): local sums, warp exclusive scan, write
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    long long cnt = 0, pad = 0;
+    for (int e = e0; e < e1; ++e) {
+      cnt += s_tot[e];
+      pad += (s_tot[e] + ROW_ALIGN - 1) / ROW_ALIGN * ROW_ALIGN;
+    }
+    long long ic = cnt, ip = pad;  // inclusive scans
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long oc = __shfl_up_sync(0xffffffffu, ic, off);
+      const long long op = __shfl_up_sync(0xffffffffu, ip, off);
+      if (lane >= off) { ic += oc; ip += op; }
+    }
+    long long off = ic - cnt, roff = ip - pad;
+    for (int e = e0; e < e1; ++e) {
       offsets[e] = static_cast<int32_t>(off);
       row_offsets[e] = static_cast<int32_t>(roff);
-      off += n;
-      roff += (n + ROW_ALIGN - 1) / ROW_ALIGN * ROW_ALIGN;
+      off += s_tot[e];
+      roff += (s_tot[e] + ROW_ALIGN - 1) / ROW_ALIGN * ROW_ALIGN;
     }
-    offsets[E] = static_cast<int32_t>(off);
-    row_offsets[E] = static_cast<int32_t>(roff);
-    if (off != static_cast<long long>(T) * k) set_status(status, MOE_ERR_INVARIANT);
-    *counter = 0;
+    if (lane == 31) {
+      offsets[E] = static_cast<int32_t>(ic);
+      row_offsets[E] = static_cast<int32_t>(ip);
+      if (ic != static_cast<long long>(T) * k) set_status(status, MOE_ERR_INVARIANT);
+      *counter = 0;
+    }
   }
 }
 
@@ -296,10 +330,16 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int scor
   const int nb = route_blocks(T);
   cudaError_t err = cudaMemsetAsync(ws.counter, 0, sizeof(int32_t), stream);
   if (err != cudaSuccess) return err;
-  const size_t smem = static_cast<size_t>(E) * (ROUTE_TOKENS / 32) * sizeof(uint32_t);
-  route_topk_kernel<<<nb, 256, smem, stream>>>(logits, T, E, k, score, topk_idx, topk_w, ws.block_hist,
-                                               ws.block_base, ws.local_rank, ws.counter, split_sizes,
-                                               offsets, row_offsets, status);
+  // the masks [E][ROUTE_TOKENS / 32] and, in the last block, the E totals
+  const size_t smem = static_cast<size_t>(E) * (ROUTE_TOKENS / 32 > 1 ? ROUTE_TOKENS / 32 : 1) * sizeof(uint32_t);
+  auto kern = E <= 32 ? route_topk_kernel<1>
+              : E <= 64 ? route_topk_kernel<2>
+              : E <= 128 ? route_topk_kernel<4>
+              : E <= 256 ? route_topk_kernel<8>
+              : E <= 512 ? route_topk_kernel<16>
+                         : route_topk_kernel<32>;
+  kern<<<nb, 256, smem, stream>>>(logits, T, E, k, score, topk_idx, topk_w, ws.block_hist, ws.block_base,
+                                  ws.local_rank, ws.counter, split_sizes, offsets, row_offsets, status);
   count_launch();
   return cudaGetLastError();
 }
