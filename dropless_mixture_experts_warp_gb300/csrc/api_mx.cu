@@ -39,15 +39,14 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
   if (M < 128 || N < 128 || K < 128 || M % 128 || N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
   if (!al16(a) || !al16(b) || !al16(c) || !al16(a_sf) || !al16(b_sf)) return MOE_ERR_ALIGNMENT;
   const int bn = N % 256 == 0 ? 256 : 128;
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a, K, M, 128, BM) || !make_tensor_map_u8(&tb, b, K, N, 128, bn))
-    return MOE_ERR_CUDA;
+  const MxMat ma{a, a_sf, static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const MxMat mb{b, b_sf, static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.BN = bn; p.N = N; p.K = K; p.M = M; p.E = 1; p.row_offsets = nullptr; p.m_fastest = 1;
   p.out = c; p.ldo = N; p.row_limit = M; p.status = dev_status;
-  p.sfa = a_sf; p.sfb = b_sf; p.a_sf_ktiles = K / 128; p.b_sf_ktiles = K / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  p.a_sf_ktiles = K / 128; p.b_sf_ktiles = K / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -112,6 +111,10 @@ static MxActs carve_acts(const moe_dims& d, int64_t R_cap, void* base) {
   a.dgu_rows = carve_op(p, 2 * rf);
   a.dgu_cols = carve_op(p, 2 * rf);
   return a;
+}
+
+static MxMat mat(const MxOp& o, int64_t inner, int64_t outer) {
+  return MxMat{o.codes, o.sf, static_cast<uint64_t>(inner), static_cast<uint64_t>(outer)};
 }
 
 static moe_status mx_common(const moe_dims* dims) {
@@ -208,18 +211,16 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets,
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.xp_rows.codes, d.d, R_cap, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.gu_rows.codes, d.d, 2ll * d.f * d.E, 128, 128))
-    return MOE_ERR_CUDA;
+  MxMat ma = mat(a.xp_rows, d.d, R_cap);
+  MxMat mb = mat(w.gu_rows, d.d, 2ll * d.f * d.E);
   GemmParams p = mx_params();
   p.BN = 256; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = 2 * d.f;
   p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
   p.gu_out = gu; p.status = dev_status;
-  p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
   p.q_cols_ld = R_cap; p.q_cols_ktiles = static_cast<int>(R_cap / 128);
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq, void* mx_ws,
@@ -233,15 +234,13 @@ moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, co
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   const int bn = bn_mx(d.d);
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.h_rows.codes, d.f, R_cap, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.d_rows.codes, d.f, static_cast<uint64_t>(d.d) * d.E, 128, bn))
-    return MOE_ERR_CUDA;
+  MxMat ma = mat(a.h_rows, d.f, R_cap);
+  MxMat mb = mat(w.d_rows, d.f, static_cast<uint64_t>(d.d) * d.E);
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
-  p.sfa = a.h_rows.sf; p.sfb = w.d_rows.sf; p.a_sf_ktiles = d.f / 128; p.b_sf_ktiles = d.f / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  p.a_sf_ktiles = d.f / 128; p.b_sf_ktiles = d.f / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
@@ -258,19 +257,17 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   float* dw_part = workspace_dw_part(d, workspace);
-  const int bn = 128;
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, R_cap, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.d_cols.codes, d.d, static_cast<uint64_t>(d.f) * d.E, 128, bn))
-    return MOE_ERR_CUDA;
+  const int bn = 128;  // two accumulators: the SwiGLU' epilogue overlaps the next tile
+  MxMat ma = mat(a.dy_rows, d.d, R_cap);
+  MxMat mb = mat(w.d_cols, d.d, static_cast<uint64_t>(d.f) * d.E);
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.f;
   p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
   p.dw_part = dw_part; p.dw_stride = d.f / bn; p.status = dev_status;
-  p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
   p.q_cols_sf = a.dgu_cols.sf; p.q_cols_ld = R_cap; p.q_cols_ktiles = static_cast<int>(R_cap / 128);
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_st(launch_dw_reduce(dw_part, d.f / bn, row_offsets, d.E, dw_rows, static_cast<int>(R_cap), s));
 }
 
@@ -291,16 +288,14 @@ moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy, cons
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int bn = bn_mx(d.f);
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.dy_cols.codes, R_cap, d.d, 128, BM) ||
-      !make_tensor_map_u8(&tb, a.h_cols.codes, R_cap, d.f, 128, bn))
-    return MOE_ERR_CUDA;
+  MxMat ma = mat(a.dy_cols, R_cap, d.d);
+  MxMat mb = mat(a.h_cols, R_cap, d.f);
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.M = d.d; p.E = d.E; p.row_offsets = row_offsets; p.m_fastest = (d.d <= d.f) ? 1 : 0;
   p.out = dw_d; p.ldo = d.f; p.row_limit = d.d; p.status = dev_status;
-  p.sfa = a.dy_cols.sf; p.sfb = a.h_cols.sf; p.a_sf_ktiles = static_cast<int>(R_cap / 128);
+  p.a_sf_ktiles = static_cast<int>(R_cap / 128);
   p.b_sf_ktiles = static_cast<int>(R_cap / 128);
-  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ma, mb, p, s));
 }
 
 moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq,
@@ -314,15 +309,13 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_of
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   const int bn = bn_mx(d.d);
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * d.f, R_cap, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.gu_cols.codes, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E, 128, bn))
-    return MOE_ERR_CUDA;
+  MxMat ma = mat(a.dgu_rows, 2ll * d.f, R_cap);
+  MxMat mb = mat(w.gu_cols, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E);
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
-  p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * d.f / 128; p.b_sf_ktiles = 2 * d.f / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
+  p.a_sf_ktiles = 2 * d.f / 128; p.b_sf_ktiles = 2 * d.f / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* row_to_token,
@@ -342,17 +335,15 @@ moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, co
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_u8(&ta, a.dgu_cols.codes, R_cap, 2ll * d.f, 128, BM) ||
-      !make_tensor_map_u8(&tb, a.xp_cols.codes, R_cap, d.d, 128, bn))
-    return MOE_ERR_CUDA;
+  MxMat ma = mat(a.dgu_cols, R_cap, 2ll * d.f);
+  MxMat mb = mat(a.xp_cols, R_cap, d.d);
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.M = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets;
   p.m_fastest = (2 * d.f <= d.d) ? 1 : 0; p.out = dw_gu; p.ldo = d.d; p.row_limit = 2 * d.f;
   p.status = dev_status;
-  p.sfa = a.dgu_cols.sf; p.sfb = a.xp_cols.sf; p.a_sf_ktiles = static_cast<int>(R_cap / 128);
+  p.a_sf_ktiles = static_cast<int>(R_cap / 128);
   p.b_sf_ktiles = static_cast<int>(R_cap / 128);
-  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ma, mb, p, s));
 }
 
 }  // extern "C"
@@ -444,29 +435,27 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
   MxActs a = carve_shared_acts(d, mx_ws_s);
-  CUtensorMap ta, tb;
+  MxMat ma, mb;
   GemmParams p;
   if (launch_quant_rows(x, T, d.d, d.d, nullptr, a.xp_rows.codes, a.xp_rows.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (!make_tensor_map_u8(&ta, a.xp_rows.codes, d.d, T, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.gu_rows.codes, d.d, 2ll * fs, 128, 128))
-    return MOE_ERR_CUDA;
+  ma = mat(a.xp_rows, d.d, T);
+  mb = mat(w.gu_rows, d.d, 2ll * fs);
   p = mx_params();
   p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1; p.f = fs;
   p.row_limit = T; p.gu_out = gu_s; p.status = dev_status;
-  p.sfa = a.xp_rows.sf; p.sfb = w.gu_rows.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
   p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
-  if (!make_tensor_map_u8(&ta, a.h_rows.codes, fs, T, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.d_rows.codes, fs, d.d, 128, bn))
-    return MOE_ERR_CUDA;
+  ma = mat(a.h_rows, fs, T);
+  mb = mat(w.d_rows, fs, d.d);
   p = mx_params();
   p.BN = bn; p.N = d.d; p.K = fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
   p.out = y_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
-  p.sfa = a.h_rows.sf; p.sfb = w.d_rows.sf; p.a_sf_ktiles = fs / 128; p.b_sf_ktiles = fs / 128;
-  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s));
+  p.a_sf_ktiles = fs / 128; p.b_sf_ktiles = fs / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s));
 }
 
 moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
@@ -491,54 +480,50 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
   MxActs a = carve_shared_acts(d, mx_ws_s);
-  CUtensorMap ta, tb;
+  MxMat ma, mb;
   GemmParams p;
   // dH = dy W_d_s, SwiGLU' epilogue (weight 1, no dw) writing quantised dG|dU
   if (launch_quant_rows(dy, T, d.d, d.d, nullptr, a.dy_rows.codes, a.dy_rows.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   int bn = bn_mx(fs);
-  if (!make_tensor_map_u8(&ta, a.dy_rows.codes, d.d, T, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.d_cols.codes, d.d, fs, 128, bn))
-    return MOE_ERR_CUDA;
+  ma = mat(a.dy_rows, d.d, T);
+  mb = mat(w.d_cols, d.d, fs);
   p = mx_params();
   p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = 1; p.f = fs;
   p.row_limit = T; p.gu_in = gu_s; p.status = dev_status;
-  p.sfa = a.dy_rows.sf; p.sfb = w.d_cols.sf; p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
+  p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
   p.q_cols_sf = a.dgu_cols.sf; p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
-  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dW_d_s = dy^T h_s (K = T): dy column codes, h_s column codes from the forward
   if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (!make_tensor_map_u8(&ta, a.dy_cols.codes, T, d.d, 128, BM) ||
-      !make_tensor_map_u8(&tb, a.h_cols.codes, T, fs, 128, bn))
-    return MOE_ERR_CUDA;
+  ma = mat(a.dy_cols, T, d.d);
+  mb = mat(a.h_cols, T, fs);
   p = mx_params();
   p.BN = bn; p.N = fs; p.M = d.d; p.K = T; p.E = 1; p.m_fastest = (d.d <= fs) ? 1 : 0;
   p.out = dw_d_s; p.ldo = fs; p.row_limit = d.d; p.status = dev_status;
-  p.sfa = a.dy_cols.sf; p.sfb = a.h_cols.sf; p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
-  if (launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
+  if (launch_gemm_mx(GEMM_KGROUP_STORE, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dx_s = dgu_s W_gu_s (K = 2fs)
   bn = bn_mx(d.d);
-  if (!make_tensor_map_u8(&ta, a.dgu_rows.codes, 2ll * fs, T, 128, BM) ||
-      !make_tensor_map_u8(&tb, w.gu_cols.codes, 2ll * fs, d.d, 128, bn))
-    return MOE_ERR_CUDA;
+  ma = mat(a.dgu_rows, 2ll * fs, T);
+  mb = mat(w.gu_cols, 2ll * fs, d.d);
   p = mx_params();
   p.BN = bn; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
   p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
-  p.sfa = a.dgu_rows.sf; p.sfb = w.gu_cols.sf; p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
-  if (launch_gemm_mx(GEMM_ROWS_STORE, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
+  if (launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dW_gu_s = dgu_s^T x (K = T)
   if (launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (!make_tensor_map_u8(&ta, a.dgu_cols.codes, T, 2ll * fs, 128, BM) ||
-      !make_tensor_map_u8(&tb, a.xp_cols.codes, T, d.d, 128, bn))
-    return MOE_ERR_CUDA;
+  ma = mat(a.dgu_cols, T, 2ll * fs);
+  mb = mat(a.xp_cols, T, d.d);
   p = mx_params();
   p.BN = bn; p.N = d.d; p.M = 2 * fs; p.K = T; p.E = 1; p.m_fastest = (2 * fs <= d.d) ? 1 : 0;
   p.out = dw_gu_s; p.ldo = d.d; p.row_limit = 2 * fs; p.status = dev_status;
-  p.sfa = a.dgu_cols.sf; p.sfb = a.xp_cols.sf; p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
-  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ta, tb, p, s));
+  p.a_sf_ktiles = T / 128; p.b_sf_ktiles = T / 128;
+  return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ma, mb, p, s));
 }
 
 }  // extern "C"

@@ -352,7 +352,7 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
       }
       quant_cols_chunk32(hv, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk,
-                         rblk + 32 <= p.row_limit);
+                         __all_sync(0xffffffffu, row_ok));
     }
   } else if (EPI == EPI_SWIGLU_BWD_MX) {
     // as EPI_SWIGLU_BWD, but dG|dU are quantised from fp32 along their row (blocks of
@@ -409,7 +409,7 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
         p.q_rows_sf[sf_byte_offset(row, p.f + col, ld2 / 128)] = static_cast<uint8_t>(sb);
       }
-      const bool blk_ok = rblk + 32 <= p.row_limit;
+      const bool blk_ok = __all_sync(0xffffffffu, row_ok);  // the warp's 32 rows are one block
       quant_cols_chunk32(dg, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
       quant_cols_chunk32(du, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, p.f + col, rblk,
                          blk_ok);

@@ -31,8 +31,9 @@ struct PairTile {
   long long row_end;  // rows at or beyond this are not stored
 };
 
-// s_pt[e]: first pair tile of expert e (SCHED_ROWS); rank: 0 (leader) or 1.
-template <int SCHED, int EPI, bool B_MN>
+// s_pt[e]: first pair tile of expert e (SCHED_ROWS); rank: 0 (leader) or 1; KB: K
+// elements per stage.
+template <int SCHED, int EPI, bool B_MN, int KB = BK>
 __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_ro, const int* s_pt, int E,
                                               int n_tiles, int tile, int rank) {
   PairTile t;
@@ -50,7 +51,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
     if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
-    c.kblocks = p.K / BK;
+    c.kblocks = p.K / KB;
     c.a_m = s_ro[e] + c.m * 2 * BM + rank * BM;
     c.a_k = 0;
     c.out_col = gu_split(EPI) ? c.n * half_n : c.n * p.BN;
@@ -70,7 +71,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
     if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
-    c.kblocks = (s_ro[e + 1] - s_ro[e]) / BK;
+    c.kblocks = (s_ro[e + 1] - s_ro[e]) / KB;
     c.a_m = c.m * 2 * BM + rank * BM;
     c.a_k = s_ro[e];
     c.out_col = c.n * p.BN;

@@ -1,19 +1,12 @@
-// Instantiations of the MXFP8 grouped GEMM.
+// Launcher and single-CTA instantiations of the MXFP8 grouped GEMM.
 #include "gemm_mx.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 template <int SCHED, int EPI>
-static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmParams& p,
                                cudaStream_t stream) {
-  // the STORE epilogue writes through a tensor map of the output
-  CUtensorMap c = a;
-  if (EPI == EPI_STORE) {
-    if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
-    const uint64_t rows = SCHED == SCHED_KGROUP ? static_cast<uint64_t>(p.E) * p.M : static_cast<uint64_t>(p.row_limit);
-    if (!make_tensor_map_store(&c, p.out, p.N, p.ldo, rows)) return cudaErrorInvalidValue;
-  }
   auto kern = grouped_gemm_mx_kernel<SCHED, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mx_smem_bytes(EPI));
   if (err != cudaSuccess) return err;
@@ -22,15 +15,40 @@ static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                           cudaStream_t stream) {
+cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmParams p, cudaStream_t stream) {
+  const bool split = kind == GEMM_ROWS_SWIGLU_FWD_MXQ;
+  const bool kgroup = kind == GEMM_KGROUP_STORE;
+  const bool store = kind == GEMM_ROWS_STORE || kgroup;
+  if (!store && kind != GEMM_ROWS_SWIGLU_FWD_MXQ && kind != GEMM_ROWS_SWIGLU_BWD_MXQ) return cudaErrorInvalidValue;
+  if (p.BN != 128 && p.BN != 256) return cudaErrorInvalidValue;
+  if (split && p.BN != 256) return cudaErrorInvalidValue;  // gate and up halves are whole 128-row SF tiles
+  p.sfa = a.sf;
+  p.sfb = b.sf;
+  const bool pair = (!kgroup || p.M % 256 == 0) && num_sms() >= 2;
+  // B box: the CTA's half of the BN rows on pairs and for the split epilogue, else BN
+  const int b_box = (pair || split) ? p.BN / 2 : p.BN;
+  CUtensorMap ta, tb, tc;
+  if (!make_tensor_map_u8(&ta, a.codes, a.inner, a.outer, 128, BM) ||
+      !make_tensor_map_u8(&tb, b.codes, b.inner, b.outer, 128, b_box))
+    return cudaErrorInvalidValue;
+  tc = ta;
+  if (store) {  // the STORE epilogue writes through a tensor map of the output
+    if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
+    const uint64_t rows = kgroup ? static_cast<uint64_t>(p.E) * p.M : static_cast<uint64_t>(p.row_limit);
+    if (!make_tensor_map_store(&tc, p.out, p.N, p.ldo, rows)) return cudaErrorInvalidValue;
+  }
+  if (pair) {
+    CUtensorMap tsa, tsb;
+    if (!make_tensor_map_sf(&tsa, a.sf, a.inner * a.outer / 32) ||
+        !make_tensor_map_sf(&tsb, b.sf, b.inner * b.outer / 32))
+      return cudaErrorInvalidValue;
+    return launch_gemm_mx_pair(kind, ta, tb, tsa, tsb, tc, p, stream);
+  }
   switch (kind) {
-    case GEMM_ROWS_SWIGLU_FWD: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_FWD>(a, b, p, stream);
-    case GEMM_ROWS_STORE: return launch_mx_t<SCHED_ROWS, EPI_STORE>(a, b, p, stream);
-    case GEMM_ROWS_SWIGLU_BWD: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD>(a, b, p, stream);
-    case GEMM_KGROUP_STORE: return launch_mx_t<SCHED_KGROUP, EPI_STORE>(a, b, p, stream);
-    case GEMM_ROWS_SWIGLU_FWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_FWD_MX>(a, b, p, stream);
-    case GEMM_ROWS_SWIGLU_BWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD_MX>(a, b, p, stream);
+    case GEMM_ROWS_STORE: return launch_mx_t<SCHED_ROWS, EPI_STORE>(ta, tb, tc, p, stream);
+    case GEMM_KGROUP_STORE: return launch_mx_t<SCHED_KGROUP, EPI_STORE>(ta, tb, tc, p, stream);
+    case GEMM_ROWS_SWIGLU_FWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_FWD_MX>(ta, tb, tc, p, stream);
+    case GEMM_ROWS_SWIGLU_BWD_MXQ: return launch_mx_t<SCHED_ROWS, EPI_SWIGLU_BWD_MX>(ta, tb, tc, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

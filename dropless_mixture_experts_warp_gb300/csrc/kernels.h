@@ -68,22 +68,37 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
 cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmParams& p, cudaStream_t stream);
 
+// Grid of a persistent CTA-pair kernel: as many pairs as can be resident at once
+// (an SM whose TPC neighbour is unavailable cannot host half of a pair), at most
+// one per two SMs.
+int pair_grid(const void* kern, int threads, int smem_bytes);
+
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                                cudaStream_t stream) {
   auto kern = grouped_gemm_pair_kernel<SCHED, EPI, A_MN, B_MN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  const int grid = num_sms() & ~1;  // whole CTA pairs
+  static const int grid = pair_grid(reinterpret_cast<const void*>(kern), gemm_threads(EPI), P_SMEM_BYTES);
   kern<<<grid, gemm_threads(EPI), P_SMEM_BYTES, stream>>>(a, b, p);
   count_launch();
   return cudaGetLastError();
 }
 
-// MXFP8 variants (both operands K-major E4M3 codes + scale tiles); kind is one of
-// GEMM_ROWS_SWIGLU_FWD, GEMM_ROWS_STORE, GEMM_ROWS_SWIGLU_BWD, GEMM_KGROUP_STORE.
-cudaError_t launch_gemm_mx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                           cudaStream_t stream);
+// One MXFP8 operand, K-major: E4M3 codes [outer][inner] (inner = K) and their SF tiles.
+struct MxMat {
+  const uint8_t* codes;
+  const uint8_t* sf;
+  uint64_t inner, outer;
+};
+// MXFP8 grouped GEMM; kind is one of GEMM_ROWS_STORE, GEMM_KGROUP_STORE,
+// GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  Runs on CTA pairs where the
+// shape allows (BN >= 128; KGROUP: M % 256 == 0), else on single CTAs.  p.sfa/p.sfb
+// are taken from a and b.
+cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmParams p, cudaStream_t stream);
+cudaError_t launch_gemm_mx_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sfa,
+                                const CUtensorMap& sfb, const CUtensorMap& c, const GemmParams& p,
+                                cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
@@ -99,6 +114,7 @@ float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);
+bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
 
