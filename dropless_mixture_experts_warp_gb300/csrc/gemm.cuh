@@ -241,6 +241,53 @@ __device__ __forceinline__ void store_tile_tma(const CUtensorMap* tmC, const Til
   }
 }
 
+// STORE epilogue with early release.  Part 1: the warp's nc (<= 4) chunks of 32
+// accumulator columns from col0 into registers (zeros for a tile without K blocks);
+// the caller then hands the accumulator back to the MMA warp.
+__device__ __forceinline__ void acc_load_chunks(uint32_t tbase, int col0, int nc, bool have, uint32_t (&r)[4][32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < nc) {
+      if (have) {
+        tmem_ld32(tbase + col0 + 32 * i, r[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[i][j] = 0u;
+      }
+    }
+  }
+  tmem_wait_ld();
+}
+
+// Part 2: the chunks (columns x0 .. x0 + 32 nc of output rows y0 .. y0 + 31) leave as
+// bf16 through the warp's 2 KB staging buffer (64-byte swizzle, as store_tile_tma)
+// and one tensor store each, while the next tile accumulates.
+__device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const uint32_t (&r)[4][32], int nc, int x0,
+                                                 int y0, int lane, uint8_t* stg) {
+  const uint32_t row_addr = smem_u32(stg) + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < nc) {
+      if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_shared_v4(row_addr + ((j ^ sw) << 4),
+                     pack_bf16(__uint_as_float(r[i][8 * j + 0]), __uint_as_float(r[i][8 * j + 1])),
+                     pack_bf16(__uint_as_float(r[i][8 * j + 2]), __uint_as_float(r[i][8 * j + 3])),
+                     pack_bf16(__uint_as_float(r[i][8 * j + 4]), __uint_as_float(r[i][8 * j + 5])),
+                     pack_bf16(__uint_as_float(r[i][8 * j + 6]), __uint_as_float(r[i][8 * j + 7])));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmC, stg, x0 + 32 * i, y0);
+        bulk_commit();
+      }
+    }
+  }
+}
+
 // Epilogue of one tile for one thread (one accumulator row, half of the columns):
 // reads fp32 accumulator columns from TMEM (32 at a time) and applies the fused EPI
 // step.  The two epilogue warps of a TMEM lane quarter split the tile's columns

@@ -1,4 +1,4 @@
-// Launcher and single-CTA instantiations of the MXFP8 grouped GEMM.
+// Launcher and instantiations of the MXFP8 grouped GEMM.
 #include "gemm_mx.cuh"
 #include "kernels.h"
 
@@ -10,7 +10,7 @@ static cudaError_t launch_mx_t(const CUtensorMap& a, const CUtensorMap& b, const
   auto kern = grouped_gemm_mx_kernel<SCHED, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mx_smem_bytes(EPI));
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), gemm_threads(EPI), mx_smem_bytes(EPI), stream>>>(a, b, c, p);
+  kern<<<num_sms(), mx_threads(EPI), mx_smem_bytes(EPI), stream>>>(a, b, c, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -24,9 +24,8 @@ cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmPa
   if (split && p.BN != 256) return cudaErrorInvalidValue;  // gate and up halves are whole 128-row SF tiles
   p.sfa = a.sf;
   p.sfb = b.sf;
-  const bool pair = (!kgroup || p.M % 256 == 0) && num_sms() >= 2;
-  // B box: the CTA's half of the BN rows on pairs and for the split epilogue, else BN
-  const int b_box = (pair || split) ? p.BN / 2 : p.BN;
+  // B box: the gate (or up) half of the BN rows for the split epilogue, else BN
+  const int b_box = split ? p.BN / 2 : p.BN;
   CUtensorMap ta, tb, tc;
   if (!make_tensor_map_u8(&ta, a.codes, a.inner, a.outer, 128, BM) ||
       !make_tensor_map_u8(&tb, b.codes, b.inner, b.outer, 128, b_box))
@@ -36,13 +35,6 @@ cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmPa
     if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
     const uint64_t rows = kgroup ? static_cast<uint64_t>(p.E) * p.M : static_cast<uint64_t>(p.row_limit);
     if (!make_tensor_map_store(&tc, p.out, p.N, p.ldo, rows)) return cudaErrorInvalidValue;
-  }
-  if (pair) {
-    CUtensorMap tsa, tsb;
-    if (!make_tensor_map_sf(&tsa, a.sf, a.inner * a.outer / 32) ||
-        !make_tensor_map_sf(&tsb, b.sf, b.inner * b.outer / 32))
-      return cudaErrorInvalidValue;
-    return launch_gemm_mx_pair(kind, ta, tb, tsa, tsb, tc, p, stream);
   }
   switch (kind) {
     case GEMM_ROWS_STORE: return launch_mx_t<SCHED_ROWS, EPI_STORE>(ta, tb, tc, p, stream);

@@ -27,17 +27,21 @@ constexpr int MX_SF_OFF = MX_STAGES * MX_STAGE_BYTES;
 constexpr int MX_SF_STAGE = 1536;
 constexpr int MX_XBUF_OFF = MX_SF_OFF + MX_STAGES * MX_SF_STAGE;  // transpose buffers of the epilogue warps
 __host__ __device__ constexpr bool epi_quantises(int epi) { return epi == 3 || epi == 4; }
-// per epilogue warp: a transpose buffer (quantising epilogues) or two 2 KB staging
-// buffers of the tensor store (EPI_STORE)
+// Eight epilogue warps for every MX epilogue (two per TMEM lane quarter, splitting
+// the columns); STORE reads its accumulator columns at once and releases them early.
+__host__ __device__ constexpr int mx_epi_warps(int) { return 8; }
+__host__ __device__ constexpr int mx_threads(int epi) { return 64 + 32 * mx_epi_warps(epi); }
+// per epilogue warp: a transpose buffer (quantising epilogues) or a 2 KB staging
+// buffer of the tensor store (EPI_STORE)
 __host__ __device__ constexpr int mx_smem_bytes(int epi) {
-  return MX_XBUF_OFF + (epi_quantises(epi) ? epi_warps(epi) * XBUF_FLOATS * 4 : 0) +
-         (epi == 0 ? epi_warps(epi) * 4096 : 0) + 1024;
+  return MX_XBUF_OFF + (epi_quantises(epi) ? mx_epi_warps(epi) * XBUF_FLOATS * 4 : 0) +
+         (epi == 0 ? mx_epi_warps(epi) * 2048 : 0) + 1024;
 }
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
 
 template <int SCHED, int EPI>
-__global__ void __launch_bounds__(gemm_threads(EPI), 1)
+__global__ void __launch_bounds__(mx_threads(EPI), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
@@ -65,7 +69,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   if (threadIdx.x == 0) {
     for (int s = 0; s < MX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], epi_warps(EPI)); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], mx_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
     s_abort = 0;
@@ -184,8 +188,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
-    uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 4096;
-    uint32_t nstore = 0;
+    uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 2048;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
@@ -194,13 +197,21 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const long long row = c.out_row + row_in_tile;
       if (EPI == EPI_STORE) {
+        // this warp's half of the columns: read, release the accumulator, then store
+        const int col0 = ((warp - 2) >> 2) * (BN / 2);
+        uint32_t r[4][32];
+        acc_load_chunks(tbase, col0, BN / 64, c.kblocks > 0, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+        if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
         // output rows: the padded row space (SCHED_ROWS) or expert e's block of M rows
         const long long y0 = (SCHED == SCHED_KGROUP ? static_cast<long long>(c.e) * p.M : 0ll) + c.out_row + q * 32;
-        store_tile_tma(&tmC, c, tbase, BN, lane, static_cast<int>(y0), stg, nstore);
-      } else if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile,
-                                     hand)) {
-        break;
+        store_chunks_tma(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
+        continue;
       }
+      if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile, hand))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);

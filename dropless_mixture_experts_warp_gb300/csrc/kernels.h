@@ -92,13 +92,9 @@ struct MxMat {
   uint64_t inner, outer;
 };
 // MXFP8 grouped GEMM; kind is one of GEMM_ROWS_STORE, GEMM_KGROUP_STORE,
-// GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  Runs on CTA pairs where the
-// shape allows (BN >= 128; KGROUP: M % 256 == 0), else on single CTAs.  p.sfa/p.sfb
-// are taken from a and b.
+// GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  p.sfa/p.sfb are taken from a
+// and b.
 cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmParams p, cudaStream_t stream);
-cudaError_t launch_gemm_mx_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sfa,
-                                const CUtensorMap& sfb, const CUtensorMap& c, const GemmParams& p,
-                                cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
@@ -114,7 +110,6 @@ float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);
-bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
 
