@@ -288,6 +288,65 @@ __device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const u
   }
 }
 
+// Quantising SwiGLU epilogue (EPI_SWIGLU_FWD_MX) with early release.  The warp owns
+// 32 rows and two chunks of 32 h columns (h column cb + 32 i; G at accumulator
+// column cb + 32 i, U at hw + cb + 32 i).  Part 1 reads them, forms h = w silu(G) U
+// in fp32 and rounds G and U to bf16; the caller then releases the accumulator.
+struct FwdMxChunks {
+  float h[2][32];
+  uint32_t g[2][16], u[2][16];  // bf16 pairs
+};
+
+__device__ __forceinline__ void fwd_mx_load(uint32_t tbase, int hw, int cb, float w, FwdMxChunks& f) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t g[32], u[32];
+    tmem_ld32(tbase + cb + 32 * i, g);
+    tmem_ld32(tbase + hw + cb + 32 * i, u);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+      f.h[i][j] = w * (gv * sigmoidf_(gv)) * uv;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      f.g[i][j] = pack_bf16(__uint_as_float(g[2 * j]), __uint_as_float(g[2 * j + 1]));
+      f.u[i][j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
+    }
+  }
+}
+
+// Part 2: G|U (bf16, saved for the backward pass), the row-wise codes of h (one
+// 32-column block per chunk) and its column-wise codes (the warp's 32 rows are one
+// 32-row block of every column).
+__device__ __forceinline__ void fwd_mx_store(const GemmParams& p, const TileCoord& c, long long row, bool row_ok,
+                                             int cb, int lane, float* xbuf, const FwdMxChunks& f) {
+  const long long ld2 = 2ll * p.f;
+  const long long rblk = row - lane;
+  const bool blk_ok = __all_sync(0xffffffffu, row_ok);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int col = c.out_col + cb + 32 * i;
+    if (row_ok) {
+      uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + col);
+      uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + col);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        gdst[v] = make_uint4(f.g[i][4 * v], f.g[i][4 * v + 1], f.g[i][4 * v + 2], f.g[i][4 * v + 3]);
+        udst[v] = make_uint4(f.u[i][4 * v], f.u[i][4 * v + 1], f.u[i][4 * v + 2], f.u[i][4 * v + 3]);
+      }
+      uint32_t q[8];
+      const uint32_t sb = quant_block32(f.h[i], q);
+      uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * p.f + col);
+      qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
+    }
+    quant_cols_chunk32(f.h[i], xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
+  }
+}
+
 // Epilogue of one tile for one thread (one accumulator row, half of the columns):
 // reads fp32 accumulator columns from TMEM (32 at a time) and applies the fused EPI
 // step.  The two epilogue warps of a TMEM lane quarter split the tile's columns
@@ -355,52 +414,6 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         }
       }
     }
-  } else if (EPI == EPI_SWIGLU_FWD_MX) {
-    // as EPI_SWIGLU_FWD, but h is not stored: it is quantised from fp32 along its row
-    // (one 32-column block per chunk) and down its column (the warp's 32 rows are one
-    // 32-row block: a warp-wide max per column gives the block scale)
-    const int hw = BN / 2;
-    const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
-    const long long ld2 = 2ll * p.f;
-    const int lane = row_in_tile & 31;
-    const long long rblk = row - lane;
-    const int cb = half * (hw / NH);
-    for (int c0 = cb; c0 < cb + hw / NH; c0 += 32) {
-      uint32_t g[32], u[32];
-      tmem_ld32(tbase + c0, g);
-      tmem_ld32(tbase + hw + c0, u);
-      tmem_wait_ld();
-      float hv[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
-        hv[i] = w * (gv * sigmoidf_(gv)) * uv;
-      }
-      const int col = c.out_col + c0;
-      if (row_ok) {
-        uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + col);
-        uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + col);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          gdst[v] = make_uint4(pack_bf16(__uint_as_float(g[8 * v]), __uint_as_float(g[8 * v + 1])),
-                               pack_bf16(__uint_as_float(g[8 * v + 2]), __uint_as_float(g[8 * v + 3])),
-                               pack_bf16(__uint_as_float(g[8 * v + 4]), __uint_as_float(g[8 * v + 5])),
-                               pack_bf16(__uint_as_float(g[8 * v + 6]), __uint_as_float(g[8 * v + 7])));
-          udst[v] = make_uint4(pack_bf16(__uint_as_float(u[8 * v]), __uint_as_float(u[8 * v + 1])),
-                               pack_bf16(__uint_as_float(u[8 * v + 2]), __uint_as_float(u[8 * v + 3])),
-                               pack_bf16(__uint_as_float(u[8 * v + 4]), __uint_as_float(u[8 * v + 5])),
-                               pack_bf16(__uint_as_float(u[8 * v + 6]), __uint_as_float(u[8 * v + 7])));
-        }
-        uint32_t q[8];
-        const uint32_t sb = quant_block32(hv, q);
-        uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * p.f + col);
-        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
-      }
-      quant_cols_chunk32(hv, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk,
-                         __all_sync(0xffffffffu, row_ok));
-    }
   } else if (EPI == EPI_SWIGLU_BWD_MX) {
     // as EPI_SWIGLU_BWD, but dG|dU are quantised from fp32 along their row (blocks of
     // 32 columns of 2f) and down their columns (the warp's 32 rows)
@@ -410,17 +423,25 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
     const long long rblk = row - lane;
     float dwp = 0.0f;
     const int cb = half * (BN / NH);
-    for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
-      uint4 g4[4], u4[4];
+    // the saved G and U of the next chunk are fetched while this one is processed
+    uint4 ng4[4], nu4[4];
+    auto fetch = [&](int c0) {
       if (row_ok) {
         const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
         const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) { g4[v] = gsrc[v]; u4[v] = usrc[v]; }
+        for (int v = 0; v < 4; ++v) { ng4[v] = __ldg(gsrc + v); nu4[v] = __ldg(usrc + v); }
       } else {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) { g4[v] = make_uint4(0u, 0u, 0u, 0u); u4[v] = g4[v]; }
+        for (int v = 0; v < 4; ++v) { ng4[v] = make_uint4(0u, 0u, 0u, 0u); nu4[v] = ng4[v]; }
       }
+    };
+    fetch(cb);
+    for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
+      uint4 g4[4], u4[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) { g4[v] = ng4[v]; u4[v] = nu4[v]; }
+      if (c0 + 32 < cb + BN / NH) fetch(c0 + 32);
       uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_wait_ld();

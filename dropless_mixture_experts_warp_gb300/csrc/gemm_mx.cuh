@@ -210,6 +210,20 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         store_chunks_tma(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
         continue;
       }
+      if (EPI == EPI_SWIGLU_FWD_MX) {
+        // this warp's quarter of the h columns (BN / 4 = 64): read, release, then store
+        const bool row_ok = row < p.row_limit;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+        const int cb = ((warp - 2) >> 2) * (BN / 4);
+        FwdMxChunks f;
+        fwd_mx_load(tbase, BN / 2, cb, w, f);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+        if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
+        fwd_mx_store(p, c, row, row_ok, cb, lane, xbuf, f);
+        continue;
+      }
       if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile, hand))
         break;
       tc_fence_before();

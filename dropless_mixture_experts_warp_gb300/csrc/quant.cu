@@ -57,117 +57,148 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 }
 
 // Column-wise, transposed: src bf16 [batch][rows][C] -> codes [batch][C][rows] and SF
-// tiles (per batch) for an operand with C rows and a K of `rows`.  A block takes a
-// 128 x 128 tile; a thread one column and two 32-row blocks.  Rows at or beyond
-// *nrows_dev (if given) are skipped in whole 128-row tiles (the row space is padded
-// to 128 per group, so a tile is either fully inside or fully outside).
-// Optional: row_map (batch 1) reads row r from src row row_map[r] (a negative entry
-// reads zeros) -- the column-wise codes of a permuted matrix straight from its
-// source; codes_rows/sf_rows also write the row-wise codes of the same tile
-// ([batch*rows][C], K = C), so a weight is read once for both orientations.
-// The codes of a tile and its scales (exactly one 512-byte SF tile per orientation)
-// are assembled in shared memory and leave as whole 128-byte lines.
-constexpr int QC_LD = 128 + 16;  // padded code rows in shared memory (bytes)
-constexpr int QC_SMEM = 128 * (128 + 8) * 2 + 2 * 128 * QC_LD + 2 * 512;
+// tiles (per batch) for an operand with C rows and a K of `rows`.  The work is
+// 128 x 128 tiles; a thread takes one column and two 32-row blocks of a tile.  Rows
+// at or beyond *nrows_dev (if given) are skipped in whole 128-row tiles (the row
+// space is padded to 128 per group, so a tile is either fully inside or fully
+// outside).  Optional: row_map (batch 1) reads row r from src row row_map[r] (a
+// negative entry reads zeros) -- the column-wise codes of a permuted matrix straight
+// from its source; codes_rows/sf_rows also write the row-wise codes of the same tile
+// ([batch*rows][C], K = C), so a source is read once for both orientations.
+// Persistent blocks walk the tiles with the next tile's rows in flight (cp.async
+// into the second of two input buffers) while the current one is quantised; the
+// codes of a tile and its scales (exactly one 512-byte SF tile per orientation) are
+// assembled in shared memory and leave as whole 128-byte lines.
+constexpr int QC_IN_LD = 128 + 8;  // padded bf16 input rows
+constexpr int QC_LD = 128 + 16;    // padded code rows (bytes)
+constexpr int QC_IN_BYTES = 128 * QC_IN_LD * 2;
+constexpr int QC_SMEM = 2 * QC_IN_BYTES + 2 * 128 * QC_LD + 2 * 512;
 
-__global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __restrict__ src, long long rows,
-                                                           int C, const int32_t* __restrict__ nrows_dev,
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __restrict__ src, int batch,
+                                                           long long rows, int C,
+                                                           const int32_t* __restrict__ nrows_dev,
                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                            const int32_t* __restrict__ row_map,
                                                            uint8_t* __restrict__ codes_rows,
                                                            uint8_t* __restrict__ sf_rows) {
   extern __shared__ __align__(16) uint8_t qsm[];
-  uint16_t(*tile)[128 + 8] = reinterpret_cast<uint16_t(*)[128 + 8]>(qsm);
-  uint8_t* ct = qsm + 128 * (128 + 8) * 2;  // column-wise codes [128 cols][QC_LD]
-  uint8_t* rt = ct + 128 * QC_LD;           // row-wise codes [128 rows][QC_LD]
-  uint8_t* sft = rt + 128 * QC_LD;          // the two SF tiles
-  const long long b = blockIdx.z;
-  const long long r0 = static_cast<long long>(blockIdx.y) * 128;
-  const int c0 = blockIdx.x * 128;
+  uint8_t* ct = qsm + 2 * QC_IN_BYTES;  // column-wise codes [128 cols][QC_LD]
+  uint8_t* rt = ct + 128 * QC_LD;       // row-wise codes [128 rows][QC_LD]
+  uint8_t* sft = rt + 128 * QC_LD;      // the two SF tiles
   long long limit = rows;
   if (nrows_dev) limit = min(limit, static_cast<long long>(*nrows_dev));
-  if (r0 >= limit) return;
-  const uint16_t* s = src + (row_map ? 0 : b * rows * C);
-  {
-    uint4 u[8];
+  const int ctiles = C / 128;
+  const long long rtiles = (limit + 127) / 128;  // row tiles that hold rows
+  const long long total = static_cast<long long>(batch) * rtiles * ctiles;
+  const long long k_tiles = rows / 128;
+
+  // issue the loads of tile t into input buffer `buf`
+  auto fetch = [&](long long t, int buf) {
+    if (t < total) {
+      const int cti = static_cast<int>(t % ctiles);
+      const long long rti = (t / ctiles) % rtiles;
+      const long long b = t / (static_cast<long long>(ctiles) * rtiles);
+      const uint16_t* s = src + (row_map ? 0 : b * rows * C);
+      uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // 16 uint4 per 128-column row, 8 per thread, all in flight
-      const int i = threadIdx.x + 256 * j;
-      const int rr = i >> 4, q = i & 15;
-      long long sr = r0 + rr;
-      if (sr >= rows) sr = -1;
-      else if (row_map) sr = row_map[sr];
-      u[j] = sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(s + sr * C + c0 + q * 8)) : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < 8; ++j) {  // 16 x 16 bytes per 128-column row, 8 per thread
+        const int i = threadIdx.x + 256 * j;
+        const int rr = i >> 4, q = i & 15;
+        long long sr = rti * 128 + rr;
+        if (sr >= rows) sr = -1;
+        else if (row_map) sr = row_map[sr];
+        const bool ok = sr >= 0;
+        cp_async16(&tile[rr][q * 8], s + (ok ? sr * C + cti * 128 + q * 8 : 0), ok);
+      }
     }
+    cp_async_commit();  // possibly empty: keeps one group per tile
+  };
+
+  long long t = blockIdx.x;
+  fetch(t, 0);
+  for (int it = 0; t < total; ++it, t += gridDim.x) {
+    const int buf = it & 1;
+    fetch(t + gridDim.x, buf ^ 1);
+    cp_async_wait_prev();  // this tile's group has landed
+    __syncthreads();
+    const uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<const uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
+    const int cti = static_cast<int>(t % ctiles);
+    const long long rti = (t / ctiles) % rtiles;
+    const long long b = t / (static_cast<long long>(ctiles) * rtiles);
+    const long long r0 = rti * 128;
+    const int c0 = cti * 128;
+    const int c = threadIdx.x & 127;
+    const int gpair = threadIdx.x >> 7;  // 0: row blocks 0,1; 1: row blocks 2,3
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = threadIdx.x + 256 * j;
-      *reinterpret_cast<uint4*>(&tile[i >> 4][(i & 15) * 8]) = u[j];
-    }
-  }
-  __syncthreads();
-  const int c = threadIdx.x & 127;
-  const int gpair = threadIdx.x >> 7;  // 0: row blocks 0,1; 1: row blocks 2,3
-#pragma unroll
-  for (int gg = 0; gg < 2; ++gg) {
-    const int g = gpair * 2 + gg;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[g * 32 + i][c]) << 16);
-    uint32_t w[8];
-    const uint32_t sb = quant_block32(v, w);
-    uint4* d4 = reinterpret_cast<uint4*>(ct + c * QC_LD + g * 32);
-    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    sft[sf_byte_offset(c, g * 32, 1)] = static_cast<uint8_t>(sb);
-  }
-  if (codes_rows) {
-    // row-wise codes of the same tile: thread t takes row t/2, 64 columns
-    const int rr = threadIdx.x >> 1;
-    const int cc = (threadIdx.x & 1) * 64;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
+    for (int gg = 0; gg < 2; ++gg) {
+      const int g = gpair * 2 + gg;
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        v[i] = __uint_as_float(static_cast<uint32_t>(tile[rr][cc + blk * 32 + i]) << 16);
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[g * 32 + i][c]) << 16);
       uint32_t w[8];
       const uint32_t sb = quant_block32(v, w);
-      uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
+      uint4* d4 = reinterpret_cast<uint4*>(ct + c * QC_LD + g * 32);
       d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
       d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+      sft[sf_byte_offset(c, g * 32, 1)] = static_cast<uint8_t>(sb);
     }
-  }
-  __syncthreads();
-  // column-wise codes: 128 lines of 128 bytes at codes + (c0 + line) * rows + r0
-  uint8_t* cb = codes + b * static_cast<long long>(C) * rows;
+    if (codes_rows) {
+      // row-wise codes of the same tile: thread t takes row t/2, 64 columns
+      const int rr = threadIdx.x >> 1;
+      const int cc = (threadIdx.x & 1) * 64;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = threadIdx.x + 256 * j;
-    const int line = i >> 3, q = i & 7;
-    *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + line) * rows + r0 + q * 16) =
-        *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
-  }
-  const long long k_tiles = rows / 128;
-  if (threadIdx.x < 32) {
-    uint8_t* sfb = sf + b * (static_cast<long long>(C) * rows / 32) + ((c0 / 128) * k_tiles + r0 / 128) * 512;
-    reinterpret_cast<uint4*>(sfb)[threadIdx.x] = reinterpret_cast<const uint4*>(sft)[threadIdx.x];
-  }
-  if (codes_rows) {
-    const long long grow0 = b * rows + r0;
+      for (int blk = 0; blk < 2; ++blk) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          v[i] = __uint_as_float(static_cast<uint32_t>(tile[rr][cc + blk * 32 + i]) << 16);
+        uint32_t w[8];
+        const uint32_t sb = quant_block32(v, w);
+        uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+      }
+    }
+    __syncthreads();
+    // column-wise codes: 128 lines of 128 bytes at codes + (c0 + line) * rows + r0
+    uint8_t* cb = codes + b * static_cast<long long>(C) * rows;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = threadIdx.x + 256 * j;
       const int line = i >> 3, q = i & 7;
-      *reinterpret_cast<uint4*>(codes_rows + (grow0 + line) * C + c0 + q * 16) =
-          *reinterpret_cast<const uint4*>(rt + line * QC_LD + q * 16);
+      *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + line) * rows + r0 + q * 16) =
+          *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
     }
-    if (threadIdx.x >= 32 && threadIdx.x < 64) {
-      uint8_t* sfr = sf_rows + ((grow0 / 128) * (C / 128) + c0 / 128) * 512;
-      reinterpret_cast<uint4*>(sfr)[threadIdx.x - 32] = reinterpret_cast<const uint4*>(sft + 512)[threadIdx.x - 32];
+    if (threadIdx.x < 32) {
+      uint8_t* sfb = sf + b * (static_cast<long long>(C) * rows / 32) + ((c0 / 128) * k_tiles + r0 / 128) * 512;
+      reinterpret_cast<uint4*>(sfb)[threadIdx.x] = reinterpret_cast<const uint4*>(sft)[threadIdx.x];
     }
+    if (codes_rows) {
+      const long long grow0 = b * rows + r0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = threadIdx.x + 256 * j;
+        const int line = i >> 3, q = i & 7;
+        *reinterpret_cast<uint4*>(codes_rows + (grow0 + line) * C + c0 + q * 16) =
+            *reinterpret_cast<const uint4*>(rt + line * QC_LD + q * 16);
+      }
+      if (threadIdx.x >= 32 && threadIdx.x < 64) {
+        uint8_t* sfr = sf_rows + ((grow0 / 128) * (C / 128) + c0 / 128) * 512;
+        reinterpret_cast<uint4*>(sfr)[threadIdx.x - 32] = reinterpret_cast<const uint4*>(sft + 512)[threadIdx.x - 32];
+      }
+    }
+    __syncthreads();  // the input buffer, ct, rt and sft are reused
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Dispatch with quantisation: warp per token, the token's row is quantised along d
@@ -275,12 +306,13 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map,
                                 uint8_t* codes_rows, uint8_t* sf_rows) {
-  if (rows == 0 || batch == 0) return cudaSuccess;
-  dim3 grid(C / 128, static_cast<unsigned>(rows / 128), batch);  // callers pass rows % 128 == 0
+  if (rows == 0 || batch == 0) return cudaSuccess;  // callers pass rows % 128 == 0, C % 128 == 0
   const cudaError_t e = cudaFuncSetAttribute(quant_cols_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
   if (e != cudaSuccess) return e;
-  quant_cols_t_kernel<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), rows, C, nrows_dev, codes, sf,
-                                                row_map, codes_rows, sf_rows);
+  const long long tiles = static_cast<long long>(batch) * (rows / 128) * (C / 128);
+  const int grid = static_cast<int>(tiles < 2ll * num_sms() ? tiles : 2ll * num_sms());  // two blocks per SM
+  quant_cols_t_kernel<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), batch, rows, C, nrows_dev,
+                                                      codes, sf, row_map, codes_rows, sf_rows);
   count_launch();
   return cudaGetLastError();
 }
