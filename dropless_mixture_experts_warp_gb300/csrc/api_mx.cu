@@ -257,7 +257,7 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   float* dw_part = workspace_dw_part(d, workspace);
-  const int bn = 128;  // two accumulators: the SwiGLU' epilogue overlaps the next tile
+  const int bn = bn_mx(d.f);
   MxMat ma = mat(a.dy_rows, d.d, R_cap);
   MxMat mb = mat(w.d_cols, d.d, static_cast<uint64_t>(d.f) * d.E);
   GemmParams p = mx_params();

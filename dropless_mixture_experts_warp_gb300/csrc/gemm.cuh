@@ -347,6 +347,96 @@ __device__ __forceinline__ void fwd_mx_store(const GemmParams& p, const TileCoor
   }
 }
 
+// Quantising SwiGLU' epilogue (EPI_SWIGLU_BWD_MX) pieces.  The saved G and U of one
+// row's 32 h columns (bf16, 64 bytes each).
+struct GuChunk {
+  uint4 g[4], u[4];
+};
+
+__device__ __forceinline__ void load_gu_chunk(const GemmParams& p, long long row, bool row_ok, int col, GuChunk& x) {
+  if (row_ok) {
+    const long long ld2 = 2ll * p.f;
+    const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + col);
+    const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + col);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) { x.g[v] = __ldg(gsrc + v); x.u[v] = __ldg(usrc + v); }
+  } else {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) { x.g[v] = make_uint4(0u, 0u, 0u, 0u); x.u[v] = x.g[v]; }
+  }
+}
+
+// One 32-column chunk: dH (fp32, accumulator columns of h columns col .. col + 31)
+// and the saved G, U -> dG = w dH U silu'(G), dU = w dH silu(G), quantised along the
+// row (dG at column col, dU at f + col of dG|dU) and down the columns (the warp's 32
+// rows form one block); dwp gathers the row's sum of silu(G) U dH.
+__device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row, bool row_ok, bool blk_ok, float w,
+                                             int col, const uint32_t (&r)[32], const GuChunk& gu, float& dwp,
+                                             float* xbuf, int lane, long long rblk) {
+  const long long ld2 = 2ll * p.f;
+  float dg[32], du[32];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint32_t gw[4] = {gu.g[v].x, gu.g[v].y, gu.g[v].z, gu.g[v].w};
+    const uint32_t uw[4] = {gu.u[v].x, gu.u[v].y, gu.u[v].z, gu.u[v].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+      const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
+      const float dh = __uint_as_float(r[8 * v + i]);
+      const float sg = sigmoidf_(g);
+      const float silu = g * sg;
+      const float da = w * dh;
+      dwp += silu * u * dh;
+      dg[8 * v + i] = da * u * sg * (1.0f + g * (1.0f - sg));
+      du[8 * v + i] = da * silu;
+    }
+  }
+  if (row_ok) {
+    uint32_t q[8];
+    uint32_t sb = quant_block32(dg, q);
+    uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + col);
+    qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    p.q_rows_sf[sf_byte_offset(row, col, ld2 / 128)] = static_cast<uint8_t>(sb);
+    sb = quant_block32(du, q);
+    qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + p.f + col);
+    qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    p.q_rows_sf[sf_byte_offset(row, p.f + col, ld2 / 128)] = static_cast<uint8_t>(sb);
+  }
+  quant_cols_chunk32(dg, xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
+  quant_cols_chunk32(du, xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, p.f + col, rblk, blk_ok);
+}
+
+// The row's dw partial of this N tile: with two warps per lane quarter the second
+// half's sum goes through shared memory and the first half adds it (a fixed order).
+template <int NH>
+__device__ __forceinline__ bool dw_combine(const GemmParams& p, const TileCoord& c, long long row, bool row_ok,
+                                           int half, int quarter, int row_in_tile, const DwHandoff& hand, float dwp) {
+  const int lane = row_in_tile & 31;
+  if (NH == 1) {
+    if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
+  } else if (p.dw_part) {
+    const uint32_t ph = *hand.phase;
+    *hand.phase ^= 1u;
+    if (half == 1) {
+      if (!mbar_wait_bounded(&hand.empty[quarter], ph ^ 1, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+        return false;
+      hand.s_dw[row_in_tile] = dwp;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&hand.full[quarter]);
+    } else {
+      if (!mbar_wait_bounded(&hand.full[quarter], ph, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
+        return false;
+      if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp + hand.s_dw[row_in_tile];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&hand.empty[quarter]);
+    }
+  }
+  return true;
+}
+
 // Epilogue of one tile for one thread (one accumulator row, half of the columns):
 // reads fp32 accumulator columns from TMEM (32 at a time) and applies the fused EPI
 // step.  The two epilogue warps of a TMEM lane quarter split the tile's columns
@@ -418,89 +508,23 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
     // as EPI_SWIGLU_BWD, but dG|dU are quantised from fp32 along their row (blocks of
     // 32 columns of 2f) and down their columns (the warp's 32 rows)
     const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
-    const long long ld2 = 2ll * p.f;
     const int lane = row_in_tile & 31;
     const long long rblk = row - lane;
+    const bool blk_ok = __all_sync(0xffffffffu, row_ok);  // the warp's 32 rows are one block
     float dwp = 0.0f;
     const int cb = half * (BN / NH);
     // the saved G and U of the next chunk are fetched while this one is processed
-    uint4 ng4[4], nu4[4];
-    auto fetch = [&](int c0) {
-      if (row_ok) {
-        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
-        const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) { ng4[v] = __ldg(gsrc + v); nu4[v] = __ldg(usrc + v); }
-      } else {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) { ng4[v] = make_uint4(0u, 0u, 0u, 0u); nu4[v] = ng4[v]; }
-      }
-    };
-    fetch(cb);
+    GuChunk nx;
+    load_gu_chunk(p, row, row_ok, c.out_col + cb, nx);
     for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
-      uint4 g4[4], u4[4];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) { g4[v] = ng4[v]; u4[v] = nu4[v]; }
-      if (c0 + 32 < cb + BN / NH) fetch(c0 + 32);
+      const GuChunk cur = nx;
+      if (c0 + 32 < cb + BN / NH) load_gu_chunk(p, row, row_ok, c.out_col + c0 + 32, nx);
       uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_wait_ld();
-      float dg[32], du[32];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint32_t gw[4] = {g4[v].x, g4[v].y, g4[v].z, g4[v].w};
-        const uint32_t uw[4] = {u4[v].x, u4[v].y, u4[v].z, u4[v].w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-          const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
-          const float dh = __uint_as_float(r[8 * v + i]);
-          const float sg = sigmoidf_(g);
-          const float silu = g * sg;
-          const float da = w * dh;
-          dwp += silu * u * dh;
-          dg[8 * v + i] = da * u * sg * (1.0f + g * (1.0f - sg));
-          du[8 * v + i] = da * silu;
-        }
-      }
-      const int col = c.out_col + c0;  // dG column; dU column = f + col
-      if (row_ok) {
-        uint32_t q[8];
-        uint32_t sb = quant_block32(dg, q);
-        uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + col);
-        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        p.q_rows_sf[sf_byte_offset(row, col, ld2 / 128)] = static_cast<uint8_t>(sb);
-        sb = quant_block32(du, q);
-        qd = reinterpret_cast<uint4*>(p.q_rows + row * ld2 + p.f + col);
-        qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        p.q_rows_sf[sf_byte_offset(row, p.f + col, ld2 / 128)] = static_cast<uint8_t>(sb);
-      }
-      const bool blk_ok = __all_sync(0xffffffffu, row_ok);  // the warp's 32 rows are one block
-      quant_cols_chunk32(dg, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
-      quant_cols_chunk32(du, hand.xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, p.f + col, rblk,
-                         blk_ok);
+      bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + c0, r, cur, dwp, hand.xbuf, lane, rblk);
     }
-    if (NH == 1) {
-      if (row_ok && p.dw_part) p.dw_part[row * p.dw_stride + c.n] = dwp;
-    } else if (p.dw_part) {
-      const uint32_t ph = *hand.phase;
-      *hand.phase ^= 1u;
-      if (half == 1) {
-        if (!mbar_wait_bounded(&hand.empty[quarter], ph ^ 1, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
-          return false;
-        hand.s_dw[row_in_tile] = dwp;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&hand.full[quarter]);
-      } else {
-        if (!mbar_wait_bounded(&hand.full[quarter], ph, hand.abort_flag, p.status, WAIT_LIMIT_CYCLES))
-          return false;
-        if (row_ok) p.dw_part[row * p.dw_stride + c.n] = dwp + hand.s_dw[row_in_tile];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&hand.empty[quarter]);
-      }
-    }
+    if (!dw_combine<NH>(p, c, row, row_ok, half, quarter, row_in_tile, hand, dwp)) return false;
   } else {  // EPI_SWIGLU_BWD: accumulator = dH for h columns out_col .. +BN; this half: BN/2 of them
     const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
     const long long ld2 = 2ll * p.f;

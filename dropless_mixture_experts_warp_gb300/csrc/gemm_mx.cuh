@@ -20,12 +20,14 @@ namespace moe {
 constexpr int MX_BK = 128;                                  // K elements (= bytes) per stage
 constexpr int MX_A_BYTES = BM * MX_BK;                      // 16 KB
 constexpr int MX_B_BYTES_MAX = 256 * MX_BK;                 // 32 KB
-constexpr int MX_STAGE_BYTES = MX_A_BYTES + MX_B_BYTES_MAX;  // 48 KB of codes per stage
-constexpr int MX_STAGES = 4;
+// The code stages share 192 KB: four of 48 KB for BN = 256, six of 32 KB for BN =
+// 128 -- as many bytes in flight either way, which is what hides the load latency.
+constexpr int MX_CODE_BYTES = 4 * (MX_A_BYTES + MX_B_BYTES_MAX);
+constexpr int MX_MAX_STAGES = 6;
 // scale tiles of stage s: SFA at MX_SF_OFF + s * MX_SF_STAGE, SFB (up to 2 tiles) 512 B after
-constexpr int MX_SF_OFF = MX_STAGES * MX_STAGE_BYTES;
+constexpr int MX_SF_OFF = MX_CODE_BYTES;
 constexpr int MX_SF_STAGE = 1536;
-constexpr int MX_XBUF_OFF = MX_SF_OFF + MX_STAGES * MX_SF_STAGE;  // transpose buffers of the epilogue warps
+constexpr int MX_XBUF_OFF = MX_SF_OFF + MX_MAX_STAGES * MX_SF_STAGE;  // buffers of the epilogue warps
 __host__ __device__ constexpr bool epi_quantises(int epi) { return epi == 3 || epi == 4; }
 // Eight epilogue warps for every MX epilogue (two per TMEM lane quarter, splitting
 // the columns); STORE reads its accumulator columns at once and releases them early.
@@ -39,14 +41,18 @@ __host__ __device__ constexpr int mx_smem_bytes(int epi) {
 }
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
+// BN = 256 (four stages): the TMEM columns after the scale factors, 96 per epilogue
+// warp of a lane quarter, hold accumulator columns the SwiGLU' epilogue has yet to
+// process once it has released the accumulator
+constexpr int MX_SPARE_COL = MX_SF_TMEM_COL + 4 * MX_SF_COLS_PER_STAGE;
 
 template <int SCHED, int EPI>
 __global__ void __launch_bounds__(mx_threads(EPI), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t full_bar[MX_STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[MX_STAGES];
+  __shared__ __align__(8) uint64_t full_bar[MX_MAX_STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[MX_MAX_STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < MX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int s = 0; s < MX_MAX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], mx_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
@@ -88,6 +94,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
 
   const int BN = p.BN;                       // 128 or 256
   const int num_acc = BN <= 128 ? 2 : 1;
+  const int stage_bytes = MX_A_BYTES + BN * MX_BK;
+  const int stages = MX_CODE_BYTES / stage_bytes;  // 4 or 6
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
@@ -104,7 +112,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
                                  WAIT_LIMIT_CYCLES)) { ok = false; break; }
-          uint8_t* sa = smem + stage * MX_STAGE_BYTES;
+          uint8_t* sa = smem + stage * stage_bytes;
           uint8_t* sb = sa + MX_A_BYTES;
           uint8_t* sf = smem + MX_SF_OFF + stage * MX_SF_STAGE;
           uint64_t* bar = &full_bar[stage];
@@ -132,10 +140,10 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
               bulk_load(sf + 512 + 512 * i,
                         p.sfb + (static_cast<size_t>(c.b_n / 128 + i) * p.b_sf_ktiles + kbtb) * 512, 512, bar);
           }
-          if (++stage == MX_STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == stages) { stage = 0; phase ^= 1; }
         }
       }
-      for (int s = 0; s < MX_STAGES; ++s)
+      for (int s = 0; s < stages; ++s)
         if ((armed >> s) & 1u) mbar_drain(&full_bar[s], (armed_parity >> s) & 1u, WAIT_LIMIT_CYCLES);
     }
     __syncwarp();
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, p.status,
                                  WAIT_LIMIT_CYCLES)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * MX_STAGE_BYTES);
+          const uint32_t sa = smem_u32(smem + stage * stage_bytes);
           const uint32_t sb = sa + MX_A_BYTES;
           const uint32_t sf = smem_u32(smem + MX_SF_OFF + stage * MX_SF_STAGE);
           const uint32_t sfa_t = tmem_base + MX_SF_TMEM_COL + stage * MX_SF_COLS_PER_STAGE;
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
             tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
-          if (++stage == MX_STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == stages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         tc_commit(&tfull_bar[acc]);
@@ -222,6 +230,51 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         if (lane == 0) mbar_arrive(&tempty_bar[acc]);
         if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
         fwd_mx_store(p, c, row, row_ok, cb, lane, xbuf, f);
+        continue;
+      }
+      if (EPI == EPI_SWIGLU_BWD_MX && BN == 256) {
+        // this warp's 128 dH columns: three chunks go to spare TMEM columns, one stays in
+        // registers, the accumulator is released, then the chunks are processed
+        const int half = (warp - 2) >> 2;
+        const int cb = half * 128;
+        const bool row_ok = row < p.row_limit;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+        const long long rblk = row - lane;
+        const bool blk_ok = __all_sync(0xffffffffu, row_ok);
+        const uint32_t spare = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + MX_SPARE_COL + half * 96;
+        GuChunk nx;
+        load_gu_chunk(p, row, row_ok, c.out_col + cb + 96, nx);
+        uint32_t keep[32];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          uint32_t r[32];
+          tmem_ld32(tbase + cb + 32 * i, r);
+          tmem_wait_ld();
+          tmem_st32(spare + 32 * i, r);
+        }
+        tmem_ld32(tbase + cb + 96, keep);
+        tmem_wait_ld();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+        if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
+        float dwp = 0.0f;
+        {
+          const GuChunk cur = nx;
+          load_gu_chunk(p, row, row_ok, c.out_col + cb, nx);
+          bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + cb + 96, keep, cur, dwp, xbuf, lane, rblk);
+        }
+#pragma unroll 1
+        for (int i = 0; i < 3; ++i) {
+          const GuChunk cur = nx;
+          if (i < 2) load_gu_chunk(p, row, row_ok, c.out_col + cb + 32 * (i + 1), nx);
+          uint32_t r[32];
+          tmem_ld32(spare + 32 * i, r);
+          tmem_wait_ld();
+          bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + cb + 32 * i, r, cur, dwp, xbuf, lane, rblk);
+        }
+        if (!dw_combine<2>(p, c, row, row_ok, half, q, row_in_tile, hand, dwp)) break;
         continue;
       }
       if (!tile_epilogue<EPI>(p, c, tbase, row, row < p.row_limit, BN, (warp - 2) >> 2, q, row_in_tile, hand))
