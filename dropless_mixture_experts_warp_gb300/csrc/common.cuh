@@ -275,9 +275,11 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 
 // Quantise 32 fp32 values (one block) into 8 words of codes; returns the scale byte.
 __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&codes)[8]) {
-  float amax = 0.0f;
+  float m[8];  // a tree of maxima: short dependency chains
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  for (int j = 0; j < 8; ++j)
+    m[j] = fmaxf(fmaxf(fabsf(v[4 * j]), fabsf(v[4 * j + 1])), fmaxf(fabsf(v[4 * j + 2]), fabsf(v[4 * j + 3])));
+  const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
   const int e = mx_scale_exp(amax);
   const float s = exp2_neg(e);
 #pragma unroll

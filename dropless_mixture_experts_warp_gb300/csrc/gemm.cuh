@@ -179,13 +179,13 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
 #pragma unroll
     for (int j = 0; j < 16; ++j) xb[lane * 17 + j] = v[16 * s + j];
     __syncwarp();
-    float cv[16];
-    float a = 0.0f;
+    float cv[16], m[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      cv[i] = xb[(hh * 16 + i) * 17 + cc];
-      a = fmaxf(a, fabsf(cv[i]));
-    }
+    for (int i = 0; i < 16; ++i) cv[i] = xb[(hh * 16 + i) * 17 + cc];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m[j] = fmaxf(fmaxf(fabsf(cv[4 * j]), fabsf(cv[4 * j + 1])), fmaxf(fabsf(cv[4 * j + 2]), fabsf(cv[4 * j + 3])));
+    float a = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
     const int e = mx_scale_exp(a);
     const float sc = exp2_neg(e);
@@ -375,10 +375,12 @@ __device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row,
                                              float* xbuf, int lane, long long rblk) {
   const long long ld2 = 2ll * p.f;
   float dg[32], du[32];
+  float part[4];  // the chunk's dw terms in four fixed-order partial sums
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint32_t gw[4] = {gu.g[v].x, gu.g[v].y, gu.g[v].z, gu.g[v].w};
     const uint32_t uw[4] = {gu.u[v].x, gu.u[v].y, gu.u[v].z, gu.u[v].w};
+    part[v] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
@@ -387,11 +389,12 @@ __device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row,
       const float sg = sigmoidf_(g);
       const float silu = g * sg;
       const float da = w * dh;
-      dwp += silu * u * dh;
+      part[v] += silu * u * dh;
       dg[8 * v + i] = da * u * sg * (1.0f + g * (1.0f - sg));
       du[8 * v + i] = da * silu;
     }
   }
+  dwp += (part[0] + part[1]) + (part[2] + part[3]);
   if (row_ok) {
     uint32_t q[8];
     uint32_t sb = quant_block32(dg, q);
