@@ -35,14 +35,14 @@ UNIT = "TFLOP/s"
 GEMMS = ["gate_up", "down", "down_dgrad", "down_wgrad", "gate_up_dgrad", "gate_up_wgrad"]
 GEMM_FLOP_FACTOR = {"gate_up": 4, "down": 2, "down_dgrad": 2, "down_wgrad": 2, "gate_up_dgrad": 4,
                     "gate_up_wgrad": 4}   # x R*d*f
-GEMM_KERNEL_MX = {"gate_up": "grouped_gemm_mx_kernel<0,1>", "down": "grouped_gemm_mx_kernel<0,0>",
-                  "down_dgrad": "grouped_gemm_mx_kernel<0,2> + dw_reduce_kernel",
+GEMM_KERNEL_MX = {"gate_up": "grouped_gemm_mx_kernel<0,3>", "down": "grouped_gemm_mx_kernel<0,0>",
+                  "down_dgrad": "grouped_gemm_mx_kernel<0,4> + dw_reduce_kernel",
                   "down_wgrad": "grouped_gemm_mx_kernel<1,0>", "gate_up_dgrad": "grouped_gemm_mx_kernel<0,0>",
                   "gate_up_wgrad": "grouped_gemm_mx_kernel<1,0>"}
-GEMM_KERNEL = {"gate_up": "grouped_gemm_kernel<0,1,0,0>", "down": "grouped_gemm_kernel<0,0,0,0>",
-               "down_dgrad": "grouped_gemm_kernel<0,2,0,1> + dw_reduce_kernel",
-               "down_wgrad": "grouped_gemm_kernel<1,0,1,1>", "gate_up_dgrad": "grouped_gemm_kernel<0,0,0,1>",
-               "gate_up_wgrad": "grouped_gemm_kernel<1,0,1,1>"}
+GEMM_KERNEL = {"gate_up": "grouped_gemm_pair_kernel<0,1,0,0>", "down": "grouped_gemm_pair_kernel<0,0,0,0>",
+               "down_dgrad": "grouped_gemm_pair_kernel<0,2,0,1> + dw_reduce_kernel",
+               "down_wgrad": "grouped_gemm_pair_kernel<1,0,1,1>", "gate_up_dgrad": "grouped_gemm_pair_kernel<0,0,0,1>",
+               "gate_up_wgrad": "grouped_gemm_pair_kernel<1,0,1,1>"}
 
 
 def workload_name(cfg) -> str:
@@ -259,7 +259,7 @@ def run_native(args, cfg):
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
         B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
         if mx8:
-            B.moe_combine_bwd_mx(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.mx_ws, stream)
+            B.moe_combine_bwd_mx(dm, dy, b.row_to_token, b.split_sizes, b.row_offsets, b.mx_ws, stream)
         else:
             B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         mark(3)
@@ -267,11 +267,11 @@ def run_native(args, cfg):
             B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace,
                                      b.status, stream)
             mark(4)
-            B.moe_gemm_down_wgrad_mx(dm, dy, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+            B.moe_gemm_down_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
             mark(5)
             B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
             mark(6)
-            B.moe_gemm_gate_up_wgrad_mx(dm, x, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+            B.moe_gemm_gate_up_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
         else:
             B.moe_gemm_down_dgrad(dm, b.dy_rows, b.row_offsets, b.w_rows, w_d, b.gu, b.dgu, b.dw_rows,
                                   b.workspace, b.status, stream)
@@ -283,7 +283,7 @@ def run_native(args, cfg):
             B.moe_gemm_gate_up_wgrad(dm, b.dgu, b.xp, b.row_offsets, b.dw_gu, b.status, stream)
         mark(7)
         if cfg.f_shared and mx8:
-            B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
+            B.moe_shared_mlp_bwd_mx(dm, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
                                     stream)
         elif cfg.f_shared:
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,

@@ -77,7 +77,7 @@ SIGNATURES = {
     "moe_mx_shared_workspace_size": (ctypes.c_size_t, [_D]),
     "moe_mx_quantize_shared_weights": (ctypes.c_int32, [_D, _P, _P, _P, _P]),
     "moe_shared_mlp_fwd_mx": (ctypes.c_int32, [_D] + [_P] * 7),
-    "moe_shared_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 10),
+    "moe_shared_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 9),
     "moe_mx_quantize_rows": (ctypes.c_int32, [_P, ctypes.c_int64, _I, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_mx_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P]),
     "moe_gemm_mxfp8": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -89,9 +89,9 @@ SIGNATURES = {
     "moe_gemm_gate_up_mx": (ctypes.c_int32, [_D] + [_P] * 7),
     "moe_gemm_down_mx": (ctypes.c_int32, [_D] + [_P] * 6),
     "moe_gemm_down_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 9),
-    "moe_gemm_down_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_down_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 5),
     "moe_gemm_gate_up_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 6),
-    "moe_gemm_gate_up_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_gemm_gate_up_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 5),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -308,8 +308,8 @@ def moe_permute_mx(dims, x, topk_idx, topk_w, split_sizes, row_offsets, workspac
                  _ptr(w_rows), _ptr(dev_status), _stream(stream))
 
 
-def moe_combine_bwd_mx(dims, dy, token_to_row, split_sizes, row_offsets, mx_ws, stream=None):
-    return _call("moe_combine_bwd_mx", _d(dims), _ptr(dy), _ptr(token_to_row), _ptr(split_sizes),
+def moe_combine_bwd_mx(dims, dy, row_to_token, split_sizes, row_offsets, mx_ws, stream=None):
+    return _call("moe_combine_bwd_mx", _d(dims), _ptr(dy), _ptr(row_to_token), _ptr(split_sizes),
                  _ptr(row_offsets), _ptr(mx_ws), _stream(stream))
 
 
@@ -329,9 +329,9 @@ def moe_gemm_down_dgrad_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dw_rows, wo
                  _ptr(gu), _ptr(dw_rows), _ptr(workspace), _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_down_wgrad_mx(dims, dy, row_to_token, row_offsets, mx_ws, dw_d, dev_status, stream=None):
-    return _call("moe_gemm_down_wgrad_mx", _d(dims), _ptr(dy), _ptr(row_to_token), _ptr(row_offsets),
-                 _ptr(mx_ws), _ptr(dw_d), _ptr(dev_status), _stream(stream))
+def moe_gemm_down_wgrad_mx(dims, row_offsets, mx_ws, dw_d, dev_status, stream=None):
+    return _call("moe_gemm_down_wgrad_mx", _d(dims), _ptr(row_offsets), _ptr(mx_ws), _ptr(dw_d),
+                 _ptr(dev_status), _stream(stream))
 
 
 def moe_gemm_gate_up_dgrad_mx(dims, row_offsets, wq, mx_ws, dxp, dev_status, stream=None):
@@ -339,9 +339,9 @@ def moe_gemm_gate_up_dgrad_mx(dims, row_offsets, wq, mx_ws, dxp, dev_status, str
                  _ptr(dev_status), _stream(stream))
 
 
-def moe_gemm_gate_up_wgrad_mx(dims, x, row_to_token, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
-    return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(x), _ptr(row_to_token), _ptr(row_offsets),
-                 _ptr(mx_ws), _ptr(dw_gu), _ptr(dev_status), _stream(stream))
+def moe_gemm_gate_up_wgrad_mx(dims, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
+    return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(row_offsets), _ptr(mx_ws), _ptr(dw_gu),
+                 _ptr(dev_status), _stream(stream))
 
 def moe_mx_shared_weights_size(dims) -> int:
     return lib().moe_mx_shared_weights_size(_d(dims))
@@ -361,8 +361,8 @@ def moe_shared_mlp_fwd_mx(dims, x, wq_s, mx_ws_s, gu_s, y_s, dev_status, stream=
                  _ptr(dev_status), _stream(stream))
 
 
-def moe_shared_mlp_bwd_mx(dims, x, wq_s, mx_ws_s, gu_s, dy, dx_s, dw_gu_s, dw_d_s, dev_status, stream=None):
-    return _call("moe_shared_mlp_bwd_mx", _d(dims), _ptr(x), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(dy),
+def moe_shared_mlp_bwd_mx(dims, wq_s, mx_ws_s, gu_s, dy, dx_s, dw_gu_s, dw_d_s, dev_status, stream=None):
+    return _call("moe_shared_mlp_bwd_mx", _d(dims), _ptr(wq_s), _ptr(mx_ws_s), _ptr(gu_s), _ptr(dy),
                  _ptr(dx_s), _ptr(dw_gu_s), _ptr(dw_d_s), _ptr(dev_status), _stream(stream))
 
 

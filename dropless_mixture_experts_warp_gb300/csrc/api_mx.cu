@@ -178,27 +178,34 @@ moe_status moe_permute_mx(const moe_dims* dims, const moe_bf16* x, const int32_t
   if (!workspace) return MOE_ERR_WORKSPACE;
   if (!al16(x) || !al16(mx_ws)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxActs a = carve_acts(d, R_cap, mx_ws);
   RouteScratch rs = route_scratch(d, const_cast<void*>(workspace));
-  return cuda_st(launch_scatter_quant(true, x, d.T, d.d, d.E, d.k, topk_idx, topk_w, split_sizes, row_offsets, &rs,
-                                      a.xp_rows.codes, a.xp_rows.sf, row_to_token, token_to_row, w_rows,
-                                      static_cast<int>(R_cap), dev_status, static_cast<cudaStream_t>(stream)));
+  // the maps, then one gathered pass over x for the row-wise (gate/up GEMM) and the
+  // column-wise (gate/up weight gradient) codes of the permuted rows
+  if (launch_route_maps(d.T, d.E, d.k, topk_idx, topk_w, split_sizes, row_offsets, rs, row_to_token, token_to_row,
+                        w_rows, static_cast<int>(R_cap), dev_status, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (d.T == 0) return MOE_OK;
+  return cuda_st(launch_quant_cols_t(x, 1, R_cap, d.d, row_offsets + d.E, a.xp_cols.codes, a.xp_cols.sf, s,
+                                     row_to_token, a.xp_rows.codes, a.xp_rows.sf));
 }
 
-moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* token_to_row,
+moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
                               const int32_t* split_sizes, const int32_t* row_offsets, void* mx_ws, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!split_sizes || !row_offsets || !mx_ws) return MOE_ERR_INVALID_ARG;
-  if (d.T > 0 && (!dy || !token_to_row)) return MOE_ERR_INVALID_ARG;
+  if (!split_sizes || !row_offsets || !mx_ws || !row_to_token) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && !dy) return MOE_ERR_INVALID_ARG;
   if (!al16(dy) || !al16(mx_ws)) return MOE_ERR_ALIGNMENT;
+  if (d.T == 0) return MOE_OK;
   const int64_t R_cap = moe_row_capacity(dims);
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  return cuda_st(launch_scatter_quant(false, dy, d.T, d.d, d.E, d.k, nullptr, nullptr, split_sizes, row_offsets,
-                                      nullptr, a.dy_rows.codes, a.dy_rows.sf, nullptr,
-                                      const_cast<int32_t*>(token_to_row), nullptr, static_cast<int>(R_cap),
-                                      nullptr, static_cast<cudaStream_t>(stream)));
+  // one gathered pass over dY: row-wise codes (down dgrad) and column-wise codes (down wgrad)
+  return cuda_st(launch_quant_cols_t(dy, 1, R_cap, d.d, row_offsets + d.E, a.dy_cols.codes, a.dy_cols.sf,
+                                     static_cast<cudaStream_t>(stream), row_to_token, a.dy_rows.codes,
+                                     a.dy_rows.sf));
 }
 
 moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
@@ -271,22 +278,16 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   return cuda_st(launch_dw_reduce(dw_part, d.f / bn, row_offsets, d.E, dw_rows, static_cast<int>(R_cap), s));
 }
 
-moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
-                                  const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
-                                  void* stream) {
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d,
+                                  int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!row_to_token || !row_offsets || !mx_ws || !dw_d || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (d.T > 0 && !dy) return MOE_ERR_INVALID_ARG;
-  if (!al16(dy) || !al16(mx_ws) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
+  if (!row_offsets || !mx_ws || !dw_d || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(mx_ws) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  // column-wise codes of dY's routed rows, gathered from dY through row_to_token
-  if (launch_quant_cols_t(dy, 1, R_cap, d.d, row_offsets + d.E, a.dy_cols.codes, a.dy_cols.sf, s, row_to_token) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
   const int bn = bn_mx(d.f);
   MxMat ma = mat(a.dy_cols, R_cap, d.d);
   MxMat mb = mat(a.h_cols, R_cap, d.f);
@@ -318,22 +319,16 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_of
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* row_to_token,
-                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu, int32_t* dev_status,
-                                     void* stream) {
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const int32_t* row_offsets, void* mx_ws,
+                                     moe_bf16* dw_gu, int32_t* dev_status, void* stream) {
   moe_status st = mx_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (!row_to_token || !row_offsets || !mx_ws || !dw_gu || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (d.T > 0 && !x) return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(mx_ws) || !al16(dw_gu)) return MOE_ERR_ALIGNMENT;
+  if (!row_offsets || !mx_ws || !dw_gu || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!al16(mx_ws) || !al16(dw_gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxActs a = carve_acts(d, R_cap, mx_ws);
-  // column-wise codes of the permuted rows, gathered from x through row_to_token
-  if (launch_quant_cols_t(x, 1, R_cap, d.d, row_offsets + d.E, a.xp_cols.codes, a.xp_cols.sf, s, row_to_token) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   MxMat ma = mat(a.dgu_cols, R_cap, 2ll * d.f);
   MxMat mb = mat(a.xp_cols, R_cap, d.d);
@@ -437,7 +432,9 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   MxActs a = carve_shared_acts(d, mx_ws_s);
   MxMat ma, mb;
   GemmParams p;
-  if (launch_quant_rows(x, T, d.d, d.d, nullptr, a.xp_rows.codes, a.xp_rows.sf, s) != cudaSuccess)
+  // x along d (gate/up GEMM) and along T (its weight gradient, in the backward pass)
+  if (launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s, nullptr, a.xp_rows.codes,
+                          a.xp_rows.sf) != cudaSuccess)
     return MOE_ERR_CUDA;
   ma = mat(a.xp_rows, d.d, T);
   mb = mat(w.gu_rows, d.d, 2ll * fs);
@@ -458,9 +455,9 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s));
 }
 
-moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 const moe_bf16* gu_s, const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s,
-                                 moe_bf16* dw_d_s, int32_t* dev_status, void* stream) {
+moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* mx_ws_s, const moe_bf16* gu_s,
+                                 const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s,
+                                 int32_t* dev_status, void* stream) {
   moe_status st = mx_shared_common(dims);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
@@ -473,8 +470,8 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (!x || !mx_ws_s || !gu_s || !dy || !dx_s) return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(dy) || !al16(dx_s) || !al16(dw_gu_s) ||
+  if (!mx_ws_s || !gu_s || !dy || !dx_s) return MOE_ERR_INVALID_ARG;
+  if (!al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(dy) || !al16(dx_s) || !al16(dw_gu_s) ||
       !al16(dw_d_s))
     return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -483,7 +480,8 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   MxMat ma, mb;
   GemmParams p;
   // dH = dy W_d_s, SwiGLU' epilogue (weight 1, no dw) writing quantised dG|dU
-  if (launch_quant_rows(dy, T, d.d, d.d, nullptr, a.dy_rows.codes, a.dy_rows.sf, s) != cudaSuccess)
+  if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s, nullptr, a.dy_rows.codes,
+                          a.dy_rows.sf) != cudaSuccess)
     return MOE_ERR_CUDA;
   int bn = bn_mx(fs);
   ma = mat(a.dy_rows, d.d, T);
@@ -496,8 +494,6 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   p.q_cols_sf = a.dgu_cols.sf; p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
   if (launch_gemm_mx(GEMM_ROWS_SWIGLU_BWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dW_d_s = dy^T h_s (K = T): dy column codes, h_s column codes from the forward
-  if (launch_quant_cols_t(dy, 1, T, d.d, nullptr, a.dy_cols.codes, a.dy_cols.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   ma = mat(a.dy_cols, T, d.d);
   mb = mat(a.h_cols, T, fs);
   p = mx_params();
@@ -515,8 +511,6 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
   if (launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // dW_gu_s = dgu_s^T x (K = T)
-  if (launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   ma = mat(a.dgu_cols, T, 2ll * fs);
   mb = mat(a.xp_cols, T, d.d);
   p = mx_params();

@@ -95,16 +95,15 @@ struct MxMat {
 // GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  p.sfa/p.sfb are taken from a
 // and b.
 cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmParams p, cudaStream_t stream);
+cudaError_t launch_route_maps(int T, int E, int k, const int32_t* topk_idx, const float* topk_w,
+                              const int32_t* split_sizes, const int32_t* row_offsets, const RouteScratch& ws,
+                              int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
+                              int32_t* status, cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map = nullptr,
                                 uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr);
-cudaError_t launch_scatter_quant(bool from_route, const void* src, int T, int d, int E, int k,
-                                 const int32_t* topk_idx, const float* topk_w, const int32_t* split_sizes,
-                                 const int32_t* row_offsets, const RouteScratch* ws, uint8_t* codes, uint8_t* sf,
-                                 int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
-                                 int32_t* status, cudaStream_t stream);
 RouteScratch route_scratch(const moe_dims& d, void* ws);
 float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);

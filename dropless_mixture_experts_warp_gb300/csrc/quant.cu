@@ -201,96 +201,57 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Dispatch with quantisation: warp per token, the token's row is quantised along d
-// once (a lane per 128-column block) and its codes and scale words are copied to the
-// token's k rows; blocks past the token blocks zero the codes and scales of one
-// expert's padding rows.  FROM_ROUTE also computes the rows and writes the maps (as
-// moe_permute); otherwise rows come from token_to_row (as moe_combine_bwd).
-template <bool FROM_ROUTE>
-__global__ void __launch_bounds__(256) scatter_quant_kernel(
-    const uint16_t* __restrict__ src, int T, int d, int E, int k, const int32_t* __restrict__ topk_idx,
-    const float* __restrict__ topk_w, const int32_t* __restrict__ split_sizes,
-    const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ block_base,
-    const int32_t* __restrict__ local_rank, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-    int32_t* __restrict__ row_to_token, int32_t* __restrict__ token_to_row, float* __restrict__ w_rows,
-    int token_blocks, int rows_cap, int32_t* __restrict__ status) {
-  __shared__ int s_rows[8][32];
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int kt = d / 128;
-  if (static_cast<int>(blockIdx.x) < token_blocks) {
-    const int t = blockIdx.x * 8 + wib;
-    if (t >= T) return;
-    if (lane < k) {
-      const long long gi = static_cast<long long>(t) * k + lane;
-      int r;
-      if (FROM_ROUTE) {
-        const int e = topk_idx[gi];
-        r = row_offsets[e] + block_base[static_cast<long long>(t / ROUTE_TOKENS) * E + e] + local_rank[gi];
-        if (r < 0 || r >= rows_cap) {
-          set_status(status, MOE_ERR_INVARIANT);
-          r = -1;
-        } else {
-          row_to_token[r] = t;
-          w_rows[r] = topk_w[gi];
-        }
-        token_to_row[gi] = r;
-      } else {
-        r = token_to_row[gi];
-        if (r < 0 || r >= rows_cap) r = -1;
-      }
-      s_rows[wib][lane] = r;
+// Routing maps of the dispatch, without moving data: for every selection (t, j) its
+// row in the padded row space (expert segment start + block base + stable rank
+// within the block), both directions, and the routing weight of each row; blocks
+// past the selection blocks mark one expert's padding rows (token -1, weight 0).
+__global__ void __launch_bounds__(256) route_maps_kernel(int T, int E, int k, const int32_t* __restrict__ topk_idx,
+                                                         const float* __restrict__ topk_w,
+                                                         const int32_t* __restrict__ split_sizes,
+                                                         const int32_t* __restrict__ row_offsets,
+                                                         const int32_t* __restrict__ block_base,
+                                                         const int32_t* __restrict__ local_rank,
+                                                         int32_t* __restrict__ row_to_token,
+                                                         int32_t* __restrict__ token_to_row, float* __restrict__ w_rows,
+                                                         int sel_blocks, int rows_cap, int32_t* __restrict__ status) {
+  if (static_cast<int>(blockIdx.x) < sel_blocks) {
+    const long long gi = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+    if (gi >= static_cast<long long>(T) * k) return;
+    const int t = static_cast<int>(gi / k);
+    const int e = topk_idx[gi];
+    int r = -1;
+    if (e >= 0 && e < E)
+      r = row_offsets[e] + block_base[static_cast<long long>(t / ROUTE_TOKENS) * E + e] + local_rank[gi];
+    if (r < 0 || r >= rows_cap) {  // an out-of-range expert index or stale routing scratch
+      set_status(status, MOE_ERR_INVARIANT);
+      r = -1;
+    } else {
+      row_to_token[r] = t;
+      w_rows[r] = topk_w[gi];
     }
-    __syncwarp();
-    for (int cb = lane; cb < kt; cb += 32) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src + static_cast<long long>(t) * d + cb * 128);
-      uint32_t code[4][8];
-      uint32_t word = 0;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = s4[g * 4 + q];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v[q * 8 + 2 * i] = bf16_lo(w[i]);
-            v[q * 8 + 2 * i + 1] = bf16_hi(w[i]);
-          }
-        }
-        word |= quant_block32(v, code[g]) << (8 * g);
-      }
-      for (int j = 0; j < k; ++j) {
-        const int r = s_rows[wib][j];
-        if (r < 0) continue;
-        uint4* d4 = reinterpret_cast<uint4*>(codes + static_cast<long long>(r) * d + cb * 128);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          d4[2 * g] = make_uint4(code[g][0], code[g][1], code[g][2], code[g][3]);
-          d4[2 * g + 1] = make_uint4(code[g][4], code[g][5], code[g][6], code[g][7]);
-        }
-        *reinterpret_cast<uint32_t*>(sf + sf_byte_offset(r, static_cast<long long>(cb) * 128, kt)) = word;
-      }
-    }
+    token_to_row[gi] = r;
   } else {
-    const int e = blockIdx.x - token_blocks;
+    const int e = blockIdx.x - sel_blocks;
     const int r0 = max(0, row_offsets[e] + split_sizes[e]);
     const int r1 = min(rows_cap, row_offsets[e + 1]);
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    const long long d16 = d / 16;
-    for (long long i = threadIdx.x; i < static_cast<long long>(r1 - r0) * d16; i += blockDim.x)
-      reinterpret_cast<uint4*>(codes + static_cast<long long>(r0) * d)[i] = z;
-    for (long long i = threadIdx.x; i < static_cast<long long>(r1 - r0) * kt; i += blockDim.x) {
-      const long long r = r0 + i / kt;
-      *reinterpret_cast<uint32_t*>(sf + sf_byte_offset(r, (i % kt) * 128, kt)) = 0u;
-    }
-    if (FROM_ROUTE) {
-      for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-        row_to_token[r] = -1;
-        w_rows[r] = 0.0f;
-      }
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+      row_to_token[r] = -1;
+      w_rows[r] = 0.0f;
     }
   }
+}
+
+cudaError_t launch_route_maps(int T, int E, int k, const int32_t* topk_idx, const float* topk_w,
+                              const int32_t* split_sizes, const int32_t* row_offsets, const RouteScratch& ws,
+                              int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
+                              int32_t* status, cudaStream_t stream) {
+  const long long sel = static_cast<long long>(T) * k;
+  const int sel_blocks = static_cast<int>((sel + 255) / 256);
+  route_maps_kernel<<<sel_blocks + E, 256, 0, stream>>>(T, E, k, topk_idx, topk_w, split_sizes, row_offsets,
+                                                        ws.block_base, ws.local_rank, row_to_token, token_to_row,
+                                                        w_rows, sel_blocks, rows_cap, status);
+  count_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long ld, const int32_t* nrows_dev,
@@ -317,24 +278,5 @@ cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_scatter_quant(bool from_route, const void* src, int T, int d, int E, int k,
-                                 const int32_t* topk_idx, const float* topk_w, const int32_t* split_sizes,
-                                 const int32_t* row_offsets, const RouteScratch* ws, uint8_t* codes, uint8_t* sf,
-                                 int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
-                                 int32_t* status, cudaStream_t stream) {
-  const int token_blocks = (T + 7) / 8;
-  const int grid = token_blocks + E;
-  if (from_route)
-    scatter_quant_kernel<true><<<grid, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(src), T, d, E, k, topk_idx, topk_w, split_sizes, row_offsets, ws->block_base,
-        ws->local_rank, codes, sf, row_to_token, token_to_row, w_rows, token_blocks, rows_cap, status);
-  else
-    scatter_quant_kernel<false><<<grid, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(src), T, d, E, k, nullptr, nullptr, split_sizes, row_offsets, nullptr,
-        nullptr, codes, sf, nullptr, const_cast<int32_t*>(token_to_row), nullptr, token_blocks, rows_cap,
-        nullptr);
-  count_launch();
-  return cudaGetLastError();
-}
 
 }  // namespace moe

@@ -129,7 +129,7 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
     mx8 = dm.prec == 1
     shared_dx = None
     if dm.f_shared and mx8:
-        B.moe_shared_mlp_bwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
+        B.moe_shared_mlp_bwd_mx(dm, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
                                 stream)
         shared_dx = b.dx_s
     elif dm.f_shared:
@@ -137,12 +137,12 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
                              b.status, stream)
         shared_dx = b.dx_s
     if mx8:
-        B.moe_combine_bwd_mx(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.mx_ws, stream)
+        B.moe_combine_bwd_mx(dm, dy, b.row_to_token, b.split_sizes, b.row_offsets, b.mx_ws, stream)
         B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace,
                                  b.status, stream)
-        B.moe_gemm_down_wgrad_mx(dm, dy, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
+        B.moe_gemm_down_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
         B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
-        B.moe_gemm_gate_up_wgrad_mx(dm, x, b.row_to_token, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+        B.moe_gemm_gate_up_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
     else:
         B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu,

@@ -355,15 +355,15 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
 /*
  * The layer with MXFP8 GEMM operands (dims->prec may be either value; f % 128 == 0).
  * Every GEMM operand is quantised along its own contraction axis, in the kernel that
- * produces it: the routed token rows by moe_permute_mx and dY's rows by
- * moe_combine_bwd_mx (one quantisation per token, copied to its k rows); h and dG|dU
- * in the epilogues of the gate/up and SwiGLU' GEMMs, from fp32, both along their rows
- * and down their columns in 32-row blocks of the 128-aligned expert segments; the
- * column-wise codes of the routed x and dY rows by the weight-gradient calls, which
- * gather them from x / dY through row_to_token.  bf16 copies of Xp, h, dY rows and
- * dG|dU are never written.  The GEMMs are the block-scaled tcgen05 kernel with fp32
- * accumulation and the same bf16 outputs (gu, y_rows, dxp, dW) as the bf16 calls.
- * The backward treats quantisation as the identity.
+ * produces it: the routed token rows by moe_permute_mx and dY's routed rows by
+ * moe_combine_bwd_mx, each in one gathered pass that writes both the row-wise codes
+ * (blocks along d, for the row GEMMs) and the column-wise codes (blocks of 32 rows
+ * down each column of the 128-aligned expert segments, for the weight gradients);
+ * h and dG|dU in the epilogues of the gate/up and SwiGLU' GEMMs, from fp32, in both
+ * orientations.  bf16 copies of Xp, h, dY rows and dG|dU are never written.  The
+ * GEMMs are the block-scaled tcgen05 kernel with fp32 accumulation and the same bf16
+ * outputs (gu, y_rows, dxp, dW) as the bf16 calls.  The backward treats
+ * quantisation as the identity.
  *   wq:    >= moe_mx_weights_size bytes, filled by moe_mx_quantize_weights from the
  *          bf16 master weights (W_gu along d and along 2f, W_d along f and along d;
  *          one read of each weight); refill it whenever the weights change.
@@ -372,6 +372,9 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
  *          moe_permute_mx, moe_gemm_gate_up_mx, moe_gemm_down_mx, (combine),
  *          moe_combine_bwd_mx, moe_gemm_down_dgrad_mx, moe_gemm_down_wgrad_mx,
  *          moe_gemm_gate_up_dgrad_mx, moe_gemm_gate_up_wgrad_mx.
+ *   moe_permute_mx writes the routing maps (row_to_token, token_to_row, w_rows) as
+ *          moe_permute does; moe_combine_bwd_mx gathers dY through its row_to_token.
+ *   The weight-gradient calls take their operands from mx_ws only.
  * Other arguments as in the bf16 calls of the same names without "_mx".
  */
 size_t moe_mx_weights_size(const moe_dims* dims);
@@ -386,26 +389,25 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets,
                                const void* wq, void* mx_ws, moe_bf16* gu, int32_t* dev_status, void* stream);
 moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq, void* mx_ws,
                             moe_bf16* y_rows, int32_t* dev_status, void* stream);
-moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* token_to_row,
+moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
                               const int32_t* split_sizes, const int32_t* row_offsets, void* mx_ws, void* stream);
 moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
                                   const void* wq, void* mx_ws, const moe_bf16* gu, float* dw_rows, void* workspace,
                                   int32_t* dev_status, void* stream);
-moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
-                                  const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d, int32_t* dev_status,
-                                  void* stream);
+moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_d,
+                                  int32_t* dev_status, void* stream);
 moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_offsets, const void* wq,
                                      void* mx_ws, moe_bf16* dxp, int32_t* dev_status, void* stream);
-moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const moe_bf16* x, const int32_t* row_to_token,
-                                     const int32_t* row_offsets, void* mx_ws, moe_bf16* dw_gu, int32_t* dev_status,
-                                     void* stream);
+moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const int32_t* row_offsets, void* mx_ws,
+                                     moe_bf16* dw_gu, int32_t* dev_status, void* stream);
 
 /*
  * The shared expert with MXFP8 GEMM operands (DeepSeek-V3 shape in MXFP8; f_shared and
  * T multiples of 128).  wq_s (>= moe_mx_shared_weights_size bytes) holds W_gu_s and
  * W_d_s quantised along both of their axes, filled by moe_mx_quantize_shared_weights;
  * mx_ws_s (>= moe_mx_shared_workspace_size bytes) is scratch for the quantised
- * activations (h_s and dG|dU of the shared expert are kept only as codes there).
+ * activations (h_s and dG|dU of the shared expert are kept only as codes there); the
+ * forward quantises x in both orientations there, so the backward takes no x.
  * Otherwise as moe_shared_mlp_fwd / moe_shared_mlp_bwd.
  */
 size_t moe_mx_shared_weights_size(const moe_dims* dims);
@@ -414,9 +416,9 @@ moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* 
                                           void* wq_s, void* stream);
 moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
                                  moe_bf16* gu_s, moe_bf16* y_s, int32_t* dev_status, void* stream);
-moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const moe_bf16* x, const void* wq_s, void* mx_ws_s,
-                                 const moe_bf16* gu_s, const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s,
-                                 moe_bf16* dw_d_s, int32_t* dev_status, void* stream);
+moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* mx_ws_s, const moe_bf16* gu_s,
+                                 const moe_bf16* dy, moe_bf16* dx_s, moe_bf16* dw_gu_s, moe_bf16* dw_d_s,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * Dense GEMM through the same tcgen05 kernel (one group), for unit tests of the
