@@ -72,7 +72,8 @@ def source_hash() -> str:
 
 
 def read_traffic(kernel_key: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernels have not changed since."""
+    """DRAM bytes per launch recorded from an ncu capture, if the kernels have not changed since.
+    kernel_key is "<precision>:<config>:<gemm>"."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -373,7 +374,7 @@ def run_native(args, cfg):
     achieved = dom_flops / (gemm_ms[dom] * 1e-3) / 1e12
     # MXFP8 has no measured peak: bf16's measured figure times the nominal 2x ratio
     peak = peaks["bf16_tflops_sustained"] * (2.0 if mx8 else 1.0)
-    traffic = read_traffic(dom)
+    traffic = read_traffic(f"{args.prec}:{cfg.name}:{dom}")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -79,6 +79,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     # with 16 experts, near 2 GB of device memory
     "qwen235b-e16": MoEConfig("qwen235b-e16", T=2048, d=4096, f=1536, E=16, k=8, score=SOFTMAX,
                               bias="zero", seed=1007),
+    # profiling case for the memory-bound kernels: token rows far larger than L2
+    # (x 256 MB, routed rows 512 MB) with small experts
+    "hbm-probe": MoEConfig("hbm-probe", T=32768, d=4096, f=128, E=8, k=2, score=SOFTMAX,
+                           bias="normal", bias_param=0.5, seed=1008),
     "dsv3": MoEConfig("dsv3", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
                       bias="zipf", bias_param=1.0, forced_empty=4, f_shared=2048, seed=1005),
 }
