@@ -1,9 +1,10 @@
 """The MXFP8 layer path through the C ABI against the MXFP8 oracle.
 
-Weight codes and scales are compared bit for bit; layer outputs and gradients by
-max|gpu - oracle| / max|oracle| <= 6e-2.  The GPU quantises the bf16-stored h and
-dG|dU while the oracle quantises its fp32/fp64 values, and accumulation orders
-differ, so intermediate codes may differ by one step; the tolerance covers that.
+Codes and scales of what both sides quantise from the same bits (the weights, the
+routed x rows, dY's routed rows, in both orientations) are compared bit for bit;
+layer outputs and gradients by max|gpu - oracle| / max|oracle| <= 6e-2.  h and dG|dU
+are quantised from fp32 on the GPU and from fp64 in the oracle after different
+accumulation orders, so their codes may differ by one step; the tolerance covers that.
 """
 import numpy as np
 import pytest
@@ -106,3 +107,44 @@ def test_mx_weight_codes_and_scales_bit_exact():
     c, s = mx.mx_quantize(np.swapaxes(w_d, 1, 2).reshape(E * f, d))
     assert np.array_equal(regions[3][0].reshape(E * f, d), c)
     assert np.array_equal(scales_from_tiles(regions[3][1], E * f, d), s)
+
+
+def _mx_ws_regions(b, R_cap, d, f):
+    """(codes, scales) of the step's quantised activations, in the library's order."""
+    ws = host(b.mx_ws)
+    rd, rf = R_cap * d, R_cap * f
+    out, off = {}, 0
+    for name, elems in (("xp_rows", rd), ("xp_cols", rd), ("h_rows", rf), ("h_cols", rf), ("dy_rows", rd),
+                        ("dy_cols", rd), ("dgu_rows", 2 * rf), ("dgu_cols", 2 * rf)):
+        out[name] = (ws[off:off + elems], ws[off + _a256(elems):off + _a256(elems) + elems // 32])
+        off += _a256(elems) + _a256(elems // 32)
+    return out
+
+
+@pytest.mark.parametrize("name", ["mx-ragged", "mx-zipf"])
+def test_mx_activation_codes_bit_exact(name):
+    """Routed x rows and dY rows: row-wise codes (blocks along d) and column-wise codes
+    (blocks of 32 rows of the 128-aligned expert segments), padding rows all zero."""
+    need_gpu()
+    from test_gpu_mx import scales_from_tiles
+    cfg = CASES[name]
+    b, inp, _, _ = _run(cfg)
+    d, f = cfg.d, cfg.f
+    r2t = host(b.row_to_token)
+    R_cap = r2t.size
+    ro = host(b.row_offsets)
+    used = int(ro[-1])
+    reg = _mx_ws_regions(b, R_cap, d, f)
+    for src, rows_key, cols_key in ((inp["x"], "xp_rows", "xp_cols"), (inp["dy"], "dy_rows", "dy_cols")):
+        vals = synth.bf16_to_f32(src).astype(np.float64)
+        p = np.zeros((used, d))
+        live = r2t[:used] >= 0
+        p[live] = vals[r2t[:used][live]]
+        c, sc = mx.mx_quantize(p)
+        codes, sf = reg[rows_key]
+        assert np.array_equal(codes.reshape(R_cap, d)[:used], c), rows_key
+        assert np.array_equal(scales_from_tiles(sf, R_cap, d)[:used], sc), rows_key
+        c, sc = mx.mx_quantize(p.T)
+        codes, sf = reg[cols_key]
+        assert np.array_equal(codes.reshape(d, R_cap)[:, :used], c), cols_key
+        assert np.array_equal(scales_from_tiles(sf, d, R_cap)[:, :used // 32], sc), cols_key
