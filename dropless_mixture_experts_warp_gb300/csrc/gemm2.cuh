@@ -24,7 +24,14 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = BM * BK * 2;                // 16 KB
 constexpr int P_B_BYTES_MAX = 128 * BK * 2;           // half of a 256-row B tile
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024;
+// STORE runs eight epilogue warps that read their accumulator columns at once and
+// write them through 2 KB staging buffers and tensor stores; the other epilogues keep
+// the shared epilogue's warp count.
+__host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
+__host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
+__host__ __device__ constexpr int p_smem_bytes(int epi) {
+  return P_STAGES * P_STAGE_BYTES + (epi == 0 ? pair_epi_warps(epi) * 2048 : 0) + 1024;
+}
 
 struct PairTile {
   TileCoord c;
@@ -85,9 +92,9 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
 }
 
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[P_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[P_STAGES];
@@ -126,13 +133,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1
     }
     s_pt[E] = run;
     for (int s = 0; s < P_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 2 * epi_warps(EPI)); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 2 * pair_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (EPI == EPI_STORE) tma_prefetch_desc(&tmC);
+  }
   if (warp == 1) { tmem_alloc_pair(&s_tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
   tc_fence_before();
   cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
@@ -227,12 +238,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
+    uint8_t* stg = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * 2048;
     for (int tile = pair; tile < total; tile += npairs) {
       const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * ACC_STRIDE;
       const long long row = t.c.out_row + row_in_tile;
+      if (EPI == EPI_STORE) {
+        // this warp's half of the columns: read, release the accumulator, then store
+        const int col0 = ((warp - 2) >> 2) * (BN / 2);
+        uint32_t r[4][32];
+        acc_load_chunks(tbase, col0, BN / 64, t.c.kblocks > 0, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        if (t.c.out_row + q * 32 < t.row_end) {  // 32-row blocks never straddle an expert's end
+          const long long y0 =
+              (SCHED == SCHED_KGROUP ? static_cast<long long>(t.c.e) * p.M : 0ll) + t.c.out_row + q * 32;
+          store_chunks_tma(&tmC, r, BN / 64, t.c.out_col + col0, static_cast<int>(y0), lane, stg);
+        }
+        continue;
+      }
       if (!tile_epilogue<EPI>(p, t.c, tbase, row, row < t.row_end, BN, (warp - 2) >> 2, q, row_in_tile, hand))
         break;
       tc_fence_before();
@@ -240,6 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EPI), 1
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    if (EPI == EPI_STORE && lane == 0) bulk_wait_all();  // the tensor stores are complete
   }
 
   tc_fence_before();

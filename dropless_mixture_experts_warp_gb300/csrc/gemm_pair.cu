@@ -5,21 +5,28 @@ namespace moe {
 
 cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                              cudaStream_t stream) {
+  CUtensorMap c = a;
+  if (kind != GEMM_ROWS_SWIGLU_FWD && kind != GEMM_ROWS_SWIGLU_BWD) {  // STORE: a map of the output
+    if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
+    const uint64_t rows = kind == GEMM_KGROUP_STORE ? static_cast<uint64_t>(p.E) * p.M
+                                                    : static_cast<uint64_t>(p.row_limit);
+    if (!make_tensor_map_store(&c, p.out, p.N, p.ldo, rows)) return cudaErrorInvalidValue;
+  }
   switch (kind) {
     case GEMM_ROWS_SWIGLU_FWD:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_FWD, false, false>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_FWD, false, false>(a, b, c, p, stream);
     case GEMM_ROWS_STORE:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, false>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, false>(a, b, c, p, stream);
     case GEMM_ROWS_STORE_BMN:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, true>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, true>(a, b, c, p, stream);
     case GEMM_ROWS_SWIGLU_BWD:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_BWD, false, true>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_BWD, false, true>(a, b, c, p, stream);
     case GEMM_KGROUP_STORE:
-      return launch_gemm_pair_t<SCHED_KGROUP, EPI_STORE, true, true>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_KGROUP, EPI_STORE, true, true>(a, b, c, p, stream);
     case GEMM_DENSE_AMN_BK:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, false>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, false>(a, b, c, p, stream);
     case GEMM_DENSE_AMN_BMN:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, true>(a, b, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, true>(a, b, c, p, stream);
     default:
       return cudaErrorInvalidValue;
   }

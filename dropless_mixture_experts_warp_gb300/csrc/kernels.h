@@ -73,14 +73,15 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
 // one per two SMs.
 int pair_grid(const void* kern, int threads, int smem_bytes);
 
+// c: tensor map of the bf16 output for the STORE epilogue (ignored otherwise)
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                               cudaStream_t stream) {
+cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                               const GemmParams& p, cudaStream_t stream) {
   auto kern = grouped_gemm_pair_kernel<SCHED, EPI, A_MN, B_MN>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(EPI));
   if (err != cudaSuccess) return err;
-  static const int grid = pair_grid(reinterpret_cast<const void*>(kern), gemm_threads(EPI), P_SMEM_BYTES);
-  kern<<<grid, gemm_threads(EPI), P_SMEM_BYTES, stream>>>(a, b, p);
+  static const int grid = pair_grid(reinterpret_cast<const void*>(kern), pair_threads(EPI), p_smem_bytes(EPI));
+  kern<<<grid, pair_threads(EPI), p_smem_bytes(EPI), stream>>>(a, b, c, p);
   count_launch();
   return cudaGetLastError();
 }
