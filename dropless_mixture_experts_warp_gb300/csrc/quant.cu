@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 
 // Column-wise, transposed: src bf16 [batch][rows][C] -> codes [batch][C][rows] and SF
 // tiles (per batch) for an operand with C rows and a K of `rows`.  The work is
-// 128 x 128 tiles; a thread takes one column and two 32-row blocks of a tile.  Rows
+// 128 x 128 tiles; a thread takes two columns of one 32-row block of a tile.  Rows
 // at or beyond *nrows_dev (if given) are skipped in whole 128-row tiles (the row
 // space is padded to 128 per group, so a tile is either fully inside or fully
 // outside).  Optional: row_map (batch 1) reads row r from src row row_map[r] (a
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 // Persistent blocks walk the tiles with the next tile's rows in flight (cp.async
 // into the second of two input buffers) while the current one is quantised; the
 // codes of a tile and its scales (exactly one 512-byte SF tile per orientation) are
-// assembled in shared memory and leave as whole 128-byte lines.
+// assembled in shared memory and leave as whole 128-byte lines.  Column blocks are
+// read two columns at a time (32-bit shared loads), row blocks 16 bytes at a time.
 constexpr int QC_IN_LD = 128 + 8;  // padded bf16 input rows
 constexpr int QC_LD = 128 + 16;    // padded code rows (bytes)
 constexpr int QC_IN_BYTES = 128 * QC_IN_LD * 2;
@@ -135,31 +136,47 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
     const long long b = t / (static_cast<long long>(ctiles) * rtiles);
     const long long r0 = rti * 128;
     const int c0 = cti * 128;
-    const int c = threadIdx.x & 127;
-    const int gpair = threadIdx.x >> 7;  // 0: row blocks 0,1; 1: row blocks 2,3
+    {
+      // column-wise: thread t takes columns 2 (t & 63), +1 and the 32-row block t >> 6;
+      // one 32-bit shared load brings both columns of a row
+      const int cp = threadIdx.x & 63, g = threadIdx.x >> 6;
+      float v0[32], v1[32];
 #pragma unroll
-    for (int gg = 0; gg < 2; ++gg) {
-      const int g = gpair * 2 + gg;
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(static_cast<uint32_t>(tile[g * 32 + i][c]) << 16);
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[g * 32 + i][2 * cp]);
+        v0[i] = bf16_lo(w);
+        v1[i] = bf16_hi(w);
+      }
       uint32_t w[8];
-      const uint32_t sb = quant_block32(v, w);
-      uint4* d4 = reinterpret_cast<uint4*>(ct + c * QC_LD + g * 32);
+      uint32_t sb = quant_block32(v0, w);
+      // ct line cp holds column 2 cp, line 64 + cp column 2 cp + 1 (no bank conflicts)
+      uint4* d4 = reinterpret_cast<uint4*>(ct + cp * QC_LD + g * 32);
       d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
       d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sft[sf_byte_offset(c, g * 32, 1)] = static_cast<uint8_t>(sb);
+      sft[sf_byte_offset(2 * cp, g * 32, 1)] = static_cast<uint8_t>(sb);
+      sb = quant_block32(v1, w);
+      d4 = reinterpret_cast<uint4*>(ct + (64 + cp) * QC_LD + g * 32);
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      sft[sf_byte_offset(2 * cp + 1, g * 32, 1)] = static_cast<uint8_t>(sb);
     }
     if (codes_rows) {
-      // row-wise codes of the same tile: thread t takes row t/2, 64 columns
+      // row-wise codes of the same tile: thread t takes row t/2, 64 columns (16-byte loads)
       const int rr = threadIdx.x >> 1;
       const int cc = (threadIdx.x & 1) * 64;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = __uint_as_float(static_cast<uint32_t>(tile[rr][cc + blk * 32 + i]) << 16);
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(&tile[rr][cc + blk * 32 + q * 8]);
+          const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[q * 8 + 2 * i] = bf16_lo(ww[i]);
+            v[q * 8 + 2 * i + 1] = bf16_hi(ww[i]);
+          }
+        }
         uint32_t w[8];
         const uint32_t sb = quant_block32(v, w);
         uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
@@ -169,13 +186,14 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
       }
     }
     __syncthreads();
-    // column-wise codes: 128 lines of 128 bytes at codes + (c0 + line) * rows + r0
+    // column-wise codes: 128 lines of 128 bytes at codes + (c0 + column) * rows + r0
     uint8_t* cb = codes + b * static_cast<long long>(C) * rows;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = threadIdx.x + 256 * j;
       const int line = i >> 3, q = i & 7;
-      *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + line) * rows + r0 + q * 16) =
+      const int col = line < 64 ? 2 * line : 2 * (line - 64) + 1;
+      *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + col) * rows + r0 + q * 16) =
           *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
     }
     if (threadIdx.x < 32) {
