@@ -146,7 +146,14 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
   return c;
 }
 
-__device__ __forceinline__ float sigmoidf_(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+// Logistic sigmoid through the identity sigmoid(g) = (1 + tanh(g / 2)) / 2 on the
+// hardware tanh approximation: one special-function operation instead of an
+// exponential and a reciprocal (absolute error about 2^-12, below bf16 resolution).
+__device__ __forceinline__ float sigmoidf_(float g) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
+  return fmaf(0.5f, t, 0.5f);
+}
 
 // Shared state of the epilogue warps: the hand-off of the dw partials between the
 // two epilogue warps of a TMEM lane quarter (second half -> first half, through
