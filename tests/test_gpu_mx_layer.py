@@ -28,9 +28,9 @@ CASES = {
 }
 
 
-def _run(cfg):
+def _run(cfg, inp=None):
     from dropless_mixture_experts_warp_gb300 import layer
-    inp = synth.token_inputs(cfg)
+    inp = inp or synth.token_inputs(cfg)
     w_gu_b, w_d_b = synth.all_expert_weights(cfg)
     dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, "mxfp8")
     b = layer.allocate(dims)
@@ -148,3 +148,55 @@ def test_mx_activation_codes_bit_exact(name):
         codes, sf = reg[cols_key]
         assert np.array_equal(codes.reshape(d, R_cap)[:, :used], c), cols_key
         assert np.array_equal(scales_from_tiles(sf, d, R_cap)[:, :used // 32], sc), cols_key
+
+
+def _mx_oracle(cfg, inp, w_gu_b, w_d_b):
+    f64 = lambda a: synth.bf16_to_f32(a).astype(np.float64)  # noqa: E731
+    fwd = mx.moe_forward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), cfg.k, cfg.score)
+    bwd = mx.moe_backward_mx(f64(inp["x"]), inp["logits"], f64(w_gu_b), f64(w_d_b), f64(inp["dy"]), fwd,
+                             cfg.k, cfg.score)
+    return fwd, bwd
+
+
+def test_mx_all_tokens_on_one_expert():
+    """One expert takes every row (many 128-row tiles), the others are empty."""
+    need_gpu()
+    cfg = synth.small_config("mx-one", T=300, d=128, f=128, E=4, k=1, seed=44)
+    inp = synth.token_inputs(cfg)
+    inp["logits"] = inp["logits"].copy()
+    inp["logits"][:, 2] += 1e4
+    b, inp, w_gu_b, w_d_b = _run(cfg, inp)
+    assert list(host(b.split_sizes)) == [0, 0, 300, 0]
+    fwd, bwd = _mx_oracle(cfg, inp, w_gu_b, w_d_b)
+    for key, got in (("Y", b.y), ("dX", b.dx), ("dW_gu", b.dw_gu), ("dW_d", b.dw_d)):
+        assert rel_err(host(got), fwd[key] if key == "Y" else bwd[key]) <= TOL_MXFP8, key
+    for e in (0, 1, 3):
+        assert torch.count_nonzero(b.dw_gu[e]) == 0 and torch.count_nonzero(b.dw_d[e]) == 0
+
+
+def test_mx_single_token():
+    need_gpu()
+    cfg = synth.small_config("mx-single", T=1, d=128, f=128, E=1, k=1, seed=45)
+    b, inp, w_gu_b, w_d_b = _run(cfg)
+    fwd, bwd = _mx_oracle(cfg, inp, w_gu_b, w_d_b)
+    for key, got in (("Y", b.y), ("dX", b.dx), ("dW_gu", b.dw_gu), ("dW_d", b.dw_d)):
+        assert rel_err(host(got), fwd[key] if key == "Y" else bwd[key]) <= TOL_MXFP8, key
+
+
+def test_mx_zero_tokens():
+    need_gpu()
+    from dropless_mixture_experts_warp_gb300 import layer
+    d, f, E, k = 128, 128, 4, 2
+    dims = layer.dims_of(0, d, f, E, k, 0, synth.SOFTMAX, "mxfp8")
+    b = layer.allocate(dims)
+    b.dw_gu.fill_(1.0)
+    b.dw_d.fill_(1.0)
+    z = torch.empty(0, d, dtype=torch.bfloat16, device="cuda")
+    lz = torch.empty(0, E, dtype=torch.float32, device="cuda")
+    w_gu = torch.randn(E, 2 * f, d, device="cuda").to(torch.bfloat16)
+    w_d = torch.randn(E, d, f, device="cuda").to(torch.bfloat16)
+    layer.forward(b, z, lz, w_gu, w_d)
+    layer.backward(b, z, lz, w_gu, w_d, x=z)
+    layer.check(b)
+    assert host(b.split_sizes).sum() == 0 and host(b.row_offsets)[-1] == 0
+    assert torch.count_nonzero(b.dw_gu) == 0 and torch.count_nonzero(b.dw_d) == 0
