@@ -54,11 +54,18 @@ def workload_name(cfg) -> str:
     return names.get(cfg.name, cfg.name) + " fwd+bwd"
 
 
+def l2_note(cfg) -> str:
+    weights = 3 * cfg.E * cfg.d * cfg.f * 2
+    if weights > 129e6:
+        return f"inputs larger than L2 (expert weights alone {weights / 1e9:.2f} GB > 129 MB)"
+    return "inputs smaller than L2 (a small case: not a bandwidth measurement)"
+
+
 def config_json(cfg, prec="bf16"):
     bias = {"normal": f"N(0,{cfg.bias_param})", "zipf": f"Zipf(s={cfg.bias_param})", "zero": "0"}[cfg.bias]
     return {"workload": workload_name(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
             "f_shared": cfg.f_shared, "routing": f"{cfg.score} top-{cfg.k}, router bias {bias}",
-            "precision": prec, "l2": "inputs larger than L2 (weights alone exceed 129 MB)",
+            "precision": prec, "l2": l2_note(cfg),
             "parallelism": "replicas"}
 
 
@@ -193,6 +200,24 @@ def run_reference(args, cfg):
     return 0
 
 
+# ---------------------------------------------------------------------------- replicas
+
+def reduce_max(values, dist, device):
+    """Elementwise maximum of per-rank values over all ranks: with N replicas the
+    slowest one sets the job's time.  Identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rate(world, flops_per_replica, ms):
+    """Whole-job throughput in TFLOP/s: every replica's FLOPs over the slowest step time."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------- native
 
 def run_native(args, cfg):
@@ -320,11 +345,7 @@ def run_native(args, cfg):
     if dist:
         dist.barrier()
     layer.check(bufs, stream)
-    ms = start.elapsed_time(end) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max([start.elapsed_time(end) / args.steps], dist, dev)[0]
 
     # event windows: mark 0 after permute, 1 after gate_up, 2 after down, 3 after combine_bwd,
     # 4..7 after each backward GEMM call
@@ -359,16 +380,12 @@ def run_native(args, cfg):
             dl_h.copy_(bufs.d_logits, non_blocking=True)
     end.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = start.elapsed_time(end) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max([start.elapsed_time(end) / e2e_steps], dist, dev)[0]
     layer.check(bufs, stream)
 
     peaks, peak_src = measured_peaks()
     flops = cfg.flops_fwd_bwd()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_rate(world, flops, ms)
     dom = max(GEMMS, key=lambda g: gemm_ms[g])
     dom_flops = GEMM_FLOP_FACTOR[dom] * unit
     achieved = dom_flops / (gemm_ms[dom] * 1e-3) / 1e12
@@ -390,7 +407,7 @@ def run_native(args, cfg):
                      "flops_per_launch": dom_flops, "ms_per_launch": gemm_ms[dom]},
         "gemm_ms": {g: round(v, 4) for g, v in gemm_ms.items()},
         "gemm_tflops": {g: GEMM_FLOP_FACTOR[g] * unit / (gemm_ms[g] * 1e-3) / 1e12 for g in GEMMS},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_rate(world, flops, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clocks,
