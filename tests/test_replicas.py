@@ -32,7 +32,7 @@ def _rank(rank, world, port, out):
 
 def test_slowest_replica_sets_the_time_and_all_work_counts():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == [15.0, 3.0]
     import bench
