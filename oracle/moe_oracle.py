@@ -41,6 +41,13 @@ Readings where the pages are silent (each restated in the design doc):
   R5  the shared expert (DeepSeek-V3 shape only) is a dense SwiGLU MLP on every
       token with weight 1, added after the k routed terms; it does not touch the
       router gradient.
+  R6  group-limited routing (a DeepSeek-V3 router variant, from neither page): the
+      E experts form n_group equal groups; a group's score is the sum of its two
+      largest selection scores c = sigmoid(l) + b (b a per-expert bias that steers
+      selection only); the topk_group best groups (ties to the lower group) are
+      eligible and the top-k of c among their experts are chosen (ties to the lower
+      index); weights are routed_scale * s_j / sum_S s.  Selection is decided in
+      fp32, the precision the kernel decides in.
 """
 from __future__ import annotations
 
@@ -88,6 +95,39 @@ def route(logits: np.ndarray, k: int, score: str = SOFTMAX, dtype=np.float64):
         raise ValueError(score)
     ps = np.take_along_axis(p, idx, axis=1)
     w = ps / ps.sum(axis=1, keepdims=True)
+    return idx, w
+
+
+def route_grouped(logits: np.ndarray, k: int, n_group: int, topk_group: int, bias=None,
+                  routed_scale: float = 1.0, dtype=np.float64):
+    """Group-limited top-k with sigmoid scores (R6).  Returns (idx [T,k], w [T,k]).
+
+    The selection scores c = fp32(sigmoid(l)) + fp32(b) and the group scores (sum of a
+    group's two largest c) are fp32, as in the kernel; the weights use dtype.
+    """
+    T, E = logits.shape
+    if E % n_group or E // n_group < 2 or not (1 <= topk_group <= n_group):
+        raise ValueError("need E % n_group == 0, at least 2 experts per group, 1 <= topk_group <= n_group")
+    gs = E // n_group
+    if not (1 <= k <= topk_group * gs):
+        raise ValueError("need 1 <= k <= topk_group * E / n_group")
+    l32 = np.asarray(logits, np.float32)
+    one = np.float32(1.0)
+    with np.errstate(over="ignore"):
+        s32 = one / (one + np.exp(-l32))
+    b32 = np.zeros(E, np.float32) if bias is None else np.asarray(bias, np.float32)
+    c = s32 + b32[None, :]
+    top2 = -np.sort(-c.reshape(T, n_group, gs), axis=2)[:, :, :2]
+    gscore = top2[:, :, 0] + top2[:, :, 1]                       # fp32 sum
+    gorder = np.lexsort((np.broadcast_to(np.arange(n_group), (T, n_group)), -gscore.astype(np.float64)), axis=-1)
+    eligible = np.zeros((T, n_group), bool)
+    np.put_along_axis(eligible, gorder[:, :topk_group], True, axis=1)
+    masked = np.where(np.repeat(eligible, gs, axis=1), c.astype(np.float64), -np.inf)
+    idx = select_topk(masked, k)
+    l = np.asarray(logits, dtype)
+    with np.errstate(over="ignore"):
+        sp = 1.0 / (1.0 + np.exp(-np.take_along_axis(l, idx, axis=1)))
+    w = routed_scale * sp / sp.sum(axis=1, keepdims=True)
     return idx, w
 
 
@@ -157,18 +197,23 @@ def swiglu_expert_forward(x_rows: np.ndarray, w_gu: np.ndarray, w_d: np.ndarray,
 
 
 def moe_forward(x, logits, w_gu, w_d, k: int, score: str = SOFTMAX,
-                w_gu_s=None, w_d_s=None, dtype=np.float64) -> Dict[str, np.ndarray]:
+                w_gu_s=None, w_d_s=None, dtype=np.float64, grouped: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """Forward of the layer on token-major inputs.
 
     x [T,d], logits [T,E], w_gu [E,2f,d], w_d [E,d,f] (any float type; widened to
     ``dtype``).  Returns Y [T,d] plus the routing and per-(token, slot) values the
-    backward needs.
+    backward needs.  grouped: {"n_group", "topk_group", "bias", "routed_scale"} selects
+    the group-limited sigmoid router (R6) instead of route().
     """
     x = np.asarray(x, dtype)
     T, d = x.shape
     E = w_gu.shape[0]
     f = w_d.shape[2]
-    idx, w = route(logits, k, score, dtype)
+    if grouped is not None:
+        idx, w = route_grouped(logits, k, grouped["n_group"], grouped["topk_group"], grouped.get("bias"),
+                               grouped.get("routed_scale", 1.0), dtype)
+    else:
+        idx, w = route(logits, k, score, dtype)
     y_slot = np.zeros((T, k, d), dtype)
     g_slot = np.zeros((T, k, f), dtype)
     u_slot = np.zeros((T, k, f), dtype)
@@ -192,14 +237,17 @@ def moe_forward(x, logits, w_gu, w_d, k: int, score: str = SOFTMAX,
     return out
 
 
-def route_backward(logits, idx, w, dw, score: str = SOFTMAX, dtype=np.float64) -> np.ndarray:
-    """Gradient of the router logits from dL/dw [T,k], by the chain rule through route().
+def route_backward(logits, idx, w, dw, score: str = SOFTMAX, dtype=np.float64,
+                   routed_scale: float = 1.0) -> np.ndarray:
+    """Gradient of the router logits from dL/dw [T,k], by the chain rule through route()
+    (and through route_grouped(): w = routed_scale * s_j / Z_S, the bias steering the
+    selection only).
 
     softmax: w_j = p_j / Z_S with Z_S = sum_S p and p = softmax(l):
         dL/dp_i = (dw_i - sum_S w dw) / Z_S for i in S, 0 otherwise;
         dL/dl_m = p_m (dL/dp_m - sum_i p_i dL/dp_i).
-    sigmoid: w_j = s_j / Z_S with s = sigmoid(l):
-        dL/ds_i = (dw_i - sum_S w dw) / Z_S for i in S; dL/dl = dL/ds * s (1 - s).
+    sigmoid: w_j = a s_j / Z_S with s = sigmoid(l) (a = routed_scale, 1 for route()):
+        dL/ds_i = (a dw_i - sum_S w dw) / Z_S for i in S; dL/dl = dL/ds * s (1 - s).
     """
     l = np.asarray(logits, dtype)
     T, E = l.shape
@@ -212,7 +260,7 @@ def route_backward(logits, idx, w, dw, score: str = SOFTMAX, dtype=np.float64) -
     zs = ps.sum(axis=1, keepdims=True)
     c = (w * dw).sum(axis=1, keepdims=True)
     dp = np.zeros((T, E), dtype)
-    np.put_along_axis(dp, idx, (dw - c) / zs, axis=1)
+    np.put_along_axis(dp, idx, (routed_scale * dw - c) / zs, axis=1)
     if score == SOFTMAX:
         return p * (dp - (p * dp).sum(axis=1, keepdims=True))
     return dp * p * (1.0 - p)
@@ -220,7 +268,7 @@ def route_backward(logits, idx, w, dw, score: str = SOFTMAX, dtype=np.float64) -
 
 def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
                  score: str = SOFTMAX, w_gu_s=None, w_d_s=None,
-                 dtype=np.float64) -> Dict[str, np.ndarray]:
+                 dtype=np.float64, grouped: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """Backward of moe_forward for the loss L = sum(Y * dY).
 
     Per expert e and each of its rows (token t, slot j):
@@ -264,7 +312,8 @@ def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
     for j in range(k):
         dx += dx_slot[:, j]
     out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw,
-           "d_logits": route_backward(logits, idx, w, dw, score, dtype)}
+           "d_logits": route_backward(logits, idx, w, dw, SIGMOID if grouped is not None else score, dtype,
+                                      1.0 if grouped is None else grouped.get("routed_scale", 1.0))}
     if w_gu_s is not None:
         fs = w_d_s.shape[1]
         wg = np.asarray(w_gu_s, dtype)

@@ -325,3 +325,84 @@ def test_planted_mistakes_are_caught(monkeypatch):
     x, logits, w_gu, w_d, dy, _ = _small_problem(63)
     with pytest.raises(ValueError):
         om.moe_forward(x, logits, w_gu, np.swapaxes(w_d, 1, 2), 2, om.SOFTMAX)
+
+
+# ---------------------------------------------------------------- group-limited routing
+
+def _sig32(l):
+    one = np.float32(1.0)
+    return one / (one + np.exp(-np.asarray(l, np.float32)))
+
+
+def _grouped_by_loops(logits, k, n_group, topk_group, bias):
+    """The group-limited selection written as per-token loops with explicit sort keys."""
+    T, E = logits.shape
+    gs = E // n_group
+    out = np.zeros((T, k), np.int64)
+    for t in range(T):
+        c = [np.float32(_sig32(logits[t, e]) + np.float32(bias[e])) for e in range(E)]
+        gsc = []
+        for g in range(n_group):
+            vals = sorted((c[e] for e in range(g * gs, (g + 1) * gs)), reverse=True)
+            gsc.append(np.float32(vals[0] + vals[1]))
+        groups = sorted(range(n_group), key=lambda g: (-float(gsc[g]), g))[:topk_group]
+        cand = [e for e in range(E) if e // gs in groups]
+        out[t] = sorted(cand, key=lambda e: (-float(c[e]), e))[:k]
+    return out
+
+
+@pytest.mark.parametrize("E,n_group,topk_group,k", [(16, 4, 2, 4), (24, 3, 1, 2), (32, 8, 4, 8), (12, 6, 6, 3)])
+def test_grouped_routing_matches_loop_definition(E, n_group, topk_group, k):
+    rng = np.random.default_rng(E + n_group)
+    logits = rng.standard_normal((40, E)).astype(np.float32)
+    bias = rng.standard_normal(E).astype(np.float32) * 0.3
+    idx, w = om.route_grouped(logits, k, n_group, topk_group, bias, 2.5)
+    assert np.array_equal(idx, _grouped_by_loops(logits, k, n_group, topk_group, bias))
+    s = scipy.special.expit(np.take_along_axis(logits.astype(np.float64), idx, axis=1))
+    np.testing.assert_allclose(w, 2.5 * s / s.sum(axis=1, keepdims=True), rtol=1e-12)
+
+
+def test_grouped_routing_with_one_group_is_plain_sigmoid_topk():
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((64, 16)).astype(np.float32)
+    idx, w = om.route_grouped(logits, 4, 1, 1)
+    idx0, w0 = om.route(logits, 4, om.SIGMOID)
+    assert np.array_equal(idx, idx0)
+    np.testing.assert_allclose(w, w0, rtol=1e-12)
+
+
+def test_grouped_routing_bias_steers_selection_only():
+    rng = np.random.default_rng(6)
+    logits = rng.standard_normal((32, 16)).astype(np.float32)
+    bias = np.zeros(16, np.float32)
+    bias[11] = 10.0                      # expert 11 (group 2 of 4) is always chosen
+    idx, w = om.route_grouped(logits, 3, 4, 2, bias)
+    assert np.all((idx == 11).any(axis=1))
+    s = scipy.special.expit(np.take_along_axis(logits.astype(np.float64), idx, axis=1))
+    np.testing.assert_allclose(w, s / s.sum(axis=1, keepdims=True), rtol=1e-12)   # no bias in w
+
+
+def test_grouped_routing_only_picks_from_the_best_groups():
+    rng = np.random.default_rng(7)
+    E, n_group, topk_group, k = 32, 8, 2, 4
+    logits = rng.standard_normal((50, E)).astype(np.float32)
+    idx, _ = om.route_grouped(logits, k, n_group, topk_group)
+    c = _sig32(logits).reshape(50, n_group, E // n_group)
+    gsc = np.sort(c, axis=2)[:, :, -2:].sum(axis=2)
+    for t in range(50):
+        best = set(np.argsort(-gsc[t], kind="stable")[:topk_group])
+        assert set(idx[t] // (E // n_group)) <= best
+
+
+def test_grouped_router_backward_matches_finite_differences():
+    x, logits, w_gu, w_d, dy, _ = _small_problem(51, T=8, d=16, f=8, E=8, k=2)
+    bias = np.linspace(-0.2, 0.2, 8)
+    grouped = {"n_group": 4, "topk_group": 2, "bias": bias, "routed_scale": 2.5}
+    fwd = om.moe_forward(x, logits, w_gu, w_d, 2, om.SIGMOID, grouped=grouped)
+    bwd = om.moe_backward(x, logits, w_gu, w_d, dy, fwd, 2, om.SIGMOID, grouped=grouped)
+
+    def fun():
+        return float((om.moe_forward(x, logits, w_gu, w_d, 2, om.SIGMOID, grouped=grouped)["Y"] * dy).sum())
+    fd = _fd(fun, logits)
+    assert np.abs(bwd["d_logits"] - fd).max() / np.abs(fd).max() < 1e-6
+    assert np.abs(bwd["dX"] - _fd(fun, x)).max() / np.abs(bwd["dX"]).max() < 1e-6
