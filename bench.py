@@ -50,6 +50,7 @@ def workload_name(cfg) -> str:
              "qwen30b": "Qwen3-30B-A3B-shaped MoE layer", "qwen235b": "Qwen3-235B-A22B-shaped MoE layer",
              "qwen235b-zipf": "Qwen3-235B-A22B-shaped MoE layer (Zipf routing)",
              "dsv3": "DeepSeek-V3-shaped routed-expert layer",
+             "dsv3-grouped": "DeepSeek-V3-shaped routed-expert layer with group-limited routing",
              "mixtral-e2": "Mixtral-8x7B-shaped experts (2 of them) MoE layer"}
     return names.get(cfg.name, cfg.name) + " fwd+bwd"
 
@@ -64,7 +65,9 @@ def l2_note(cfg) -> str:
 def config_json(cfg, prec="bf16"):
     bias = {"normal": f"N(0,{cfg.bias_param})", "zipf": f"Zipf(s={cfg.bias_param})", "zero": "0"}[cfg.bias]
     return {"workload": workload_name(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
-            "f_shared": cfg.f_shared, "routing": f"{cfg.score} top-{cfg.k}, router bias {bias}",
+            "f_shared": cfg.f_shared, "routing": f"{cfg.score} top-{cfg.k}, router bias {bias}" +
+            (f", group-limited ({cfg.topk_group} of {cfg.n_group} groups), routed scale {cfg.routed_scale}, "
+             f"selection bias N(0,{cfg.sel_bias_std})" if cfg.n_group else ""),
             "precision": prec, "l2": l2_note(cfg),
             "parallelism": "replicas"}
 
@@ -156,8 +159,9 @@ def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: flo
         dy = synth.bf16_to_f32(dy_bits[sub])
         lg = logits[sub]
         t0 = time.perf_counter()
-        fwd = fwd_fn(x, lg, w_gu32, w_d32, cfg.k, cfg.score, dtype=np.float32)
-        bwd_fn(x, lg, w_gu32, w_d32, dy, fwd, cfg.k, cfg.score, dtype=np.float32)
+        gr = synth.grouped_options(cfg)
+        fwd = fwd_fn(x, lg, w_gu32, w_d32, cfg.k, cfg.score, dtype=np.float32, grouped=gr)
+        bwd_fn(x, lg, w_gu32, w_d32, dy, fwd, cfg.k, cfg.score, dtype=np.float32, grouped=gr)
         t_total += time.perf_counter() - t0
         done_tok += chunk
     flops = 18.0 * done_tok * cfg.k * cfg.d * cfg.f
@@ -250,6 +254,8 @@ def run_native(args, cfg):
     x, logits, dy, w_gu, w_d = inp["x"], inp["logits"], inp["dy"], inp["w_gu"], inp["w_d"]
     R = cfg.T * cfg.k
     unit = R * cfg.d * cfg.f
+    grouped = synth.grouped_options(cfg)
+    sel_bias = torch.from_numpy(grouped["bias"]).to(dev) if grouped is not None else None
 
     def step(ev=None):
         b, dm = bufs, dims
@@ -257,8 +263,13 @@ def run_native(args, cfg):
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
-        B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
-                         b.workspace, b.status, stream)
+        if grouped is not None:
+            B.moe_route_topk_grouped(dm, logits, sel_bias, grouped["n_group"], grouped["topk_group"],
+                                     grouped["routed_scale"], b.topk_idx, b.topk_w, b.split_sizes, b.offsets,
+                                     b.row_offsets, b.workspace, b.status, stream)
+        else:
+            B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
+                             b.workspace, b.status, stream)
         if mx8:
             # the 16-bit master weights are quantised every step; x is quantised in the dispatch
             B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
@@ -315,7 +326,12 @@ def run_native(args, cfg):
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
                                  b.dw_gu_s, b.dw_d_s, b.status, stream)
         B.moe_combine_fwd(dm, b.dxp, b.token_to_row, b.dx_s, b.dx, stream)
-        B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
+        if grouped is not None:
+            B.moe_route_topk_bwd_scaled(dm, logits, b.topk_idx, b.topk_w, grouped["routed_scale"], b.dw_rows,
+                                        b.token_to_row, b.d_logits, stream)
+        else:
+            B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits,
+                                 stream)
 
     for _ in range(args.warmup):
         step()

@@ -59,6 +59,8 @@ SIGNATURES = {
     "moe_combine_bwd": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_mlp_bwd": (ctypes.c_int32, [_D] + [_P] * 16),
     "moe_route_topk_bwd": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_topk_grouped": (ctypes.c_int32, [_D, _P, _P, _I, _I, ctypes.c_float] + [_P] * 8),
+    "moe_route_topk_bwd_scaled": (ctypes.c_int32, [_D, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P]),
     "moe_check_status": (ctypes.c_int32, [_P, _P]),
     "moe_gemm_bf16": (ctypes.c_int32, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_gemm_gate_up": (ctypes.c_int32, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -199,6 +201,19 @@ def moe_grouped_mlp_bwd(dims, xp, row_offsets, w_rows, w_gu, w_d, gu, h, dy_rows
     return _call("moe_grouped_mlp_bwd", _d(dims), _ptr(xp), _ptr(row_offsets), _ptr(w_rows), _ptr(w_gu),
                  _ptr(w_d), _ptr(gu), _ptr(h), _ptr(dy_rows), _ptr(dgu), _ptr(dxp), _ptr(dw_gu), _ptr(dw_d),
                  _ptr(dw_rows), _ptr(workspace), _ptr(dev_status), _stream(stream))
+
+
+def moe_route_topk_grouped(dims, logits, bias, n_group, topk_group, routed_scale, topk_idx, topk_w, split_sizes,
+                           offsets, row_offsets, workspace, dev_status, stream=None):
+    return _call("moe_route_topk_grouped", _d(dims), _ptr(logits), _ptr(bias), int(n_group), int(topk_group),
+                 float(routed_scale), _ptr(topk_idx), _ptr(topk_w), _ptr(split_sizes), _ptr(offsets),
+                 _ptr(row_offsets), _ptr(workspace), _ptr(dev_status), _stream(stream))
+
+
+def moe_route_topk_bwd_scaled(dims, logits, topk_idx, topk_w, routed_scale, dw_rows, token_to_row, d_logits,
+                              stream=None):
+    return _call("moe_route_topk_bwd_scaled", _d(dims), _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+                 float(routed_scale), _ptr(dw_rows), _ptr(token_to_row), _ptr(d_logits), _stream(stream))
 
 
 def moe_route_topk_bwd(dims, logits, topk_idx, topk_w, dw_rows, token_to_row, d_logits, stream=None):

@@ -239,6 +239,26 @@ moe_status moe_route_topk(const moe_dims* dims, const float* logits, int32_t* to
                                        static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_route_topk_grouped(const moe_dims* dims, const float* logits, const float* bias, int32_t n_group,
+                                  int32_t topk_group, float routed_scale, int32_t* topk_idx, float* topk_w,
+                                  int32_t* split_sizes, int32_t* offsets, int32_t* row_offsets, void* workspace,
+                                  int32_t* dev_status, void* stream) {
+  moe_status st = moe_check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (d.score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (n_group < 1 || n_group > 32 || d.E % n_group != 0 || d.E / n_group < 2) return MOE_ERR_INVALID_ARG;
+  if (topk_group < 1 || topk_group > n_group || d.k > topk_group * (d.E / n_group)) return MOE_ERR_INVALID_ARG;
+  if (!(routed_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (!split_sizes || !offsets || !row_offsets || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (!logits || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (!workspace) return MOE_ERR_WORKSPACE;
+  Carve c = carve(d, workspace);
+  const GroupedRoute gr{bias, n_group, topk_group, routed_scale};
+  return cuda_status(launch_route_topk(logits, d.T, d.E, d.k, d.score, topk_idx, topk_w, split_sizes, offsets,
+                                       row_offsets, c.route, dev_status, static_cast<cudaStream_t>(stream), &gr));
+}
+
 moe_status moe_permute(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx,
                        const float* topk_w, const int32_t* split_sizes,
                        const int32_t* row_offsets, const void* workspace, moe_bf16* xp,
@@ -557,6 +577,20 @@ moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
   return cuda_status(launch_route_bwd(logits, d.T, d.E, d.k, d.score, topk_idx, topk_w, dw_rows,
                                       token_to_row, d_logits, static_cast<int>(row_capacity(d)),
                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route_topk_bwd_scaled(const moe_dims* dims, const float* logits, const int32_t* topk_idx,
+                                     const float* topk_w, float routed_scale, const float* dw_rows,
+                                     const int32_t* token_to_row, float* d_logits, void* stream) {
+  moe_status st = moe_check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (d.score != MOE_SCORE_SIGMOID || !(routed_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (!logits || !topk_idx || !topk_w || !dw_rows || !token_to_row || !d_logits))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route_bwd(logits, d.T, d.E, d.k, d.score, topk_idx, topk_w, dw_rows, token_to_row,
+                                      d_logits, static_cast<int>(row_capacity(d)),
+                                      static_cast<cudaStream_t>(stream), routed_scale));
 }
 
 moe_status moe_check_status(const int32_t* dev_status, void* stream) {

@@ -23,10 +23,16 @@ struct RouteScratch {
 void count_launch();
 int num_sms();
 
+// Options of the group-limited sigmoid router (see route_topk_kernel).
+struct GroupedRoute {
+  const float* bias;  // [E] selection bias or NULL
+  int n_group, topk_group;
+  float scale;        // routed scaling factor of the weights
+};
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int score, int32_t* topk_idx,
                               float* topk_w, int32_t* split_sizes, int32_t* offsets,
                               int32_t* row_offsets, const RouteScratch& ws, int32_t* status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const GroupedRoute* grouped = nullptr);
 cudaError_t launch_permute(const void* x, int T, int d, int E, int k, const int32_t* topk_idx,
                            const float* topk_w, const int32_t* split_sizes, const int32_t* row_offsets,
                            const RouteScratch& ws, void* xp, int32_t* row_to_token,
@@ -42,7 +48,7 @@ cudaError_t launch_dw_reduce(const float* part, int stride, const int32_t* row_o
 cudaError_t launch_route_bwd(const float* logits, int T, int E, int k, int score,
                              const int32_t* topk_idx, const float* topk_w, const float* dw_rows,
                              const int32_t* token_to_row, float* d_logits, int rows_cap,
-                             cudaStream_t stream);
+                             cudaStream_t stream, float scale = 1.0f);
 
 cudaError_t launch_wait_timeout(int32_t* status, long long limit, cudaStream_t stream);
 

@@ -25,12 +25,16 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // Per-block stable ranks come from a bitmask per expert over the block's tokens:
 // rank of token t for expert e = number of set bits below t.  The last block to
 // finish turns the per-block counts into split_sizes, offsets and row_offsets.
-template <int PL>
+// GROUPED: the group-limited sigmoid router -- selection on c = sigmoid(l) + bias
+// (fp32); a group's score is the sum of its two largest c; the topk_group best groups
+// (ties to the lower group) are eligible; weights routed_scale * s / sum of the k s.
+template <int PL, bool GROUPED>
 __global__ void __launch_bounds__(256) route_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int score, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, int32_t* __restrict__ block_hist, int32_t* __restrict__ block_base,
-    int32_t* __restrict__ local_rank, int32_t* __restrict__ counter, int32_t* __restrict__ split_sizes,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets, int32_t* __restrict__ status) {
+    const float* __restrict__ logits, int T, int E, int k, int score, GroupedRoute gr,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ block_hist,
+    int32_t* __restrict__ block_base, int32_t* __restrict__ local_rank, int32_t* __restrict__ counter,
+    int32_t* __restrict__ split_sizes, int32_t* __restrict__ offsets, int32_t* __restrict__ row_offsets,
+    int32_t* __restrict__ status) {
   extern __shared__ uint32_t masks[];  // [E][ROUTE_TOKENS / 32], then the E totals of the last block
   __shared__ int s_last;
   constexpr int WORDS = ROUTE_TOKENS / 32;
@@ -41,16 +45,56 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
   for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
 
+  // GROUPED: the group of each of this lane's expert slots (fixed for the launch)
+  int grp[PL];
+#pragma unroll
+  for (int c = 0; c < PL; ++c) grp[c] = GROUPED ? (lane + 32 * c) / (E / gr.n_group) : 0;
+
   for (int i = 0; i < TPW; ++i) {
     const int tl = warp * TPW + i;
     const int t = tok0 + tl;
     if (t >= T) break;
     const float* row = logits + static_cast<long long>(t) * E;
     uint32_t key[PL];
+    float sv[PL];  // GROUPED: the sigmoid scores
 #pragma unroll
     for (int c = 0; c < PL; ++c) {
       const int e = lane + 32 * c;
-      key[c] = e < E ? order_key(row[e]) : 0u;
+      if (GROUPED) {
+        sv[c] = e < E ? 1.0f / (1.0f + expf(-row[e])) : 0.0f;
+        key[c] = e < E ? order_key(sv[c] + (gr.bias ? gr.bias[e] : 0.0f)) : 0u;
+      } else {
+        key[c] = e < E ? order_key(row[e]) : 0u;
+      }
+    }
+    if (GROUPED) {
+      // group scores (lane g keeps group g's), then the topk_group best groups
+      float my_gscore = 0.0f;
+      for (int g = 0; g < gr.n_group; ++g) {
+        uint32_t b1 = 0u, b2 = 0u;  // this lane's two best keys in group g
+#pragma unroll
+        for (int c = 0; c < PL; ++c) {
+          if (lane + 32 * c < E && grp[c] == g) {
+            if (key[c] > b1) { b2 = b1; b1 = key[c]; } else if (key[c] > b2) { b2 = key[c]; }
+          }
+        }
+        const uint32_t m1 = __reduce_max_sync(0xffffffffu, b1);
+        const int own = __reduce_min_sync(0xffffffffu, (b1 == m1 && b1 != 0u) ? lane : 32);
+        const uint32_t m2 = __reduce_max_sync(0xffffffffu, lane == own ? b2 : b1);
+        if (lane == g) my_gscore = key_value(m1) + key_value(m2);
+      }
+      uint32_t gkey = lane < gr.n_group ? order_key(my_gscore) : 0u;
+      uint32_t chosen = 0u;
+      for (int r = 0; r < gr.topk_group; ++r) {
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, gkey);
+        const int wg = __reduce_min_sync(0xffffffffu, (gkey == wk && gkey != 0u) ? lane : 32);
+        chosen |= 1u << (wg & 31);
+        if (lane == wg) gkey = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < PL; ++c) {
+        if (lane + 32 * c < E && !((chosen >> grp[c]) & 1u)) key[c] = 0u;
+      }
     }
     int my_e = -1;
     float my_l = 0.0f;
@@ -69,18 +113,31 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
         for (int c = 0; c < PL; ++c)
           if (c == bc) key[c] = 0u;  // taken
       }
-      if (lane == j) { my_e = we; my_l = key_value(wk); }
+      if (GROUPED) {
+        float bs = 0.0f;  // the owner lane's sigmoid score of the chosen expert
+#pragma unroll
+        for (int c = 0; c < PL; ++c)
+          if (c == bc) bs = sv[c];
+        const float ws = __shfl_sync(0xffffffffu, bs, we & 31);
+        if (lane == j) { my_e = we; my_l = ws; }
+      } else if (lane == j) {
+        my_e = we;
+        my_l = key_value(wk);
+      }
     }
     // weights of the selected experts, lanes 0..k-1
     const float top = __shfl_sync(0xffffffffu, my_l, 0);  // slot 0 holds the largest logit
     float s = 0.0f;
-    if (lane < k) s = (score == MOE_SCORE_SOFTMAX) ? expf(my_l - top) : 1.0f / (1.0f + expf(-my_l));
+    if (lane < k) {
+      if (GROUPED) s = my_l;  // already the sigmoid score
+      else s = (score == MOE_SCORE_SOFTMAX) ? expf(my_l - top) : 1.0f / (1.0f + expf(-my_l));
+    }
     float tot = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
     if (lane < k) {
       topk_idx[static_cast<long long>(t) * k + lane] = my_e;
-      topk_w[static_cast<long long>(t) * k + lane] = s / tot;
+      topk_w[static_cast<long long>(t) * k + lane] = GROUPED ? gr.scale * s / tot : s / tot;
       atomicOr(&masks[my_e * WORDS + (tl >> 5)], 1u << (tl & 31));
     }
   }
@@ -292,7 +349,7 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
     const float* __restrict__ logits, int T, int E, int k, int score,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
     const float* __restrict__ dw_rows, const int32_t* __restrict__ token_to_row,
-    float* __restrict__ d_logits, int rows_cap) {
+    float* __restrict__ d_logits, int rows_cap, float scale) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -316,7 +373,8 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
   for (int i = lane; i < E; i += 32) out[i] = 0.0f;
   __syncwarp();
   if (lane < k) {
-    const float g = (score == MOE_SCORE_SOFTMAX) ? w * (dw - c) : (dw - c) / z * s * (1.0f - s);
+    // sigmoid weights w = scale * s_j / z: dL/ds_i = (scale dw_i - sum w dw) / z
+    const float g = (score == MOE_SCORE_SOFTMAX) ? w * (dw - c) : (scale * dw - c) / z * s * (1.0f - s);
     out[e] = g;
   }
 }
@@ -326,19 +384,20 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int score, int32_t* topk_idx,
                               float* topk_w, int32_t* split_sizes, int32_t* offsets,
                               int32_t* row_offsets, const RouteScratch& ws, int32_t* status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const GroupedRoute* grouped) {
   const int nb = route_blocks(T);
   cudaError_t err = cudaMemsetAsync(ws.counter, 0, sizeof(int32_t), stream);
   if (err != cudaSuccess) return err;
   // the masks [E][ROUTE_TOKENS / 32] and, in the last block, the E totals
   const size_t smem = static_cast<size_t>(E) * (ROUTE_TOKENS / 32 > 1 ? ROUTE_TOKENS / 32 : 1) * sizeof(uint32_t);
-  auto kern = E <= 32 ? route_topk_kernel<1>
-              : E <= 64 ? route_topk_kernel<2>
-              : E <= 128 ? route_topk_kernel<4>
-              : E <= 256 ? route_topk_kernel<8>
-              : E <= 512 ? route_topk_kernel<16>
-                         : route_topk_kernel<32>;
-  kern<<<nb, 256, smem, stream>>>(logits, T, E, k, score, topk_idx, topk_w, ws.block_hist, ws.block_base,
+  GroupedRoute gr{};
+  if (grouped) gr = *grouped;
+#define MOE_ROUTE_PICK(G)                                                                                   \
+  (E <= 32 ? route_topk_kernel<1, G> : E <= 64 ? route_topk_kernel<2, G> : E <= 128 ? route_topk_kernel<4, G> \
+   : E <= 256 ? route_topk_kernel<8, G> : E <= 512 ? route_topk_kernel<16, G> : route_topk_kernel<32, G>)
+  auto kern = grouped ? MOE_ROUTE_PICK(true) : MOE_ROUTE_PICK(false);
+#undef MOE_ROUTE_PICK
+  kern<<<nb, 256, smem, stream>>>(logits, T, E, k, score, gr, topk_idx, topk_w, ws.block_hist, ws.block_base,
                                   ws.local_rank, ws.counter, split_sizes, offsets, row_offsets, status);
   count_launch();
   return cudaGetLastError();
@@ -393,10 +452,10 @@ cudaError_t launch_dw_reduce(const float* part, int stride, const int32_t* row_o
 cudaError_t launch_route_bwd(const float* logits, int T, int E, int k, int score,
                              const int32_t* topk_idx, const float* topk_w, const float* dw_rows,
                              const int32_t* token_to_row, float* d_logits, int rows_cap,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float scale) {
   if (T == 0) return cudaSuccess;
   route_bwd_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, T, E, k, score, topk_idx, topk_w, dw_rows,
-                                                    token_to_row, d_logits, rows_cap);
+                                                    token_to_row, d_logits, rows_cap, scale);
   count_launch();
   return cudaGetLastError();
 }

@@ -94,7 +94,9 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
     )
 
 
-def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None):
+def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None, grouped=None):
+    """grouped: {"n_group", "topk_group", "bias" (device [E] fp32 or None), "routed_scale"} selects the
+    group-limited sigmoid router instead of the plain top-k."""
     dm = b.dims
     mx8 = dm.prec == 1
     shared_out = None
@@ -105,8 +107,13 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
     elif dm.f_shared:
         B.moe_shared_mlp_fwd(dm, x, w_gu_s, w_d_s, b.gu_s, b.h_s, b.y_s, b.status, stream)
         shared_out = b.y_s
-    B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
-                     b.workspace, b.status, stream)
+    if grouped is not None:
+        B.moe_route_topk_grouped(dm, logits, grouped.get("bias"), grouped["n_group"], grouped["topk_group"],
+                                 grouped.get("routed_scale", 1.0), b.topk_idx, b.topk_w, b.split_sizes,
+                                 b.offsets, b.row_offsets, b.workspace, b.status, stream)
+    else:
+        B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
+                         b.workspace, b.status, stream)
     if mx8:
         # the 16-bit master weights are quantised every step (they change every optimiser step)
         B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
@@ -123,8 +130,9 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
     return b.y
 
 
-def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None, w_d_s=None):
-    """x (the forward's input) is needed by the shared expert and by the MXFP8 path."""
+def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None, w_d_s=None, grouped=None):
+    """x (the forward's input) is needed by the shared expert and by the MXFP8 path; grouped as in
+    forward()."""
     dm = b.dims
     mx8 = dm.prec == 1
     shared_dx = None
@@ -148,7 +156,11 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
         B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu,
                               b.dxp, b.dw_gu, b.dw_d, b.dw_rows, b.workspace, b.status, stream)
     B.moe_combine_fwd(dm, b.dxp, b.token_to_row, shared_dx, b.dx, stream)
-    B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
+    if grouped is not None:
+        B.moe_route_topk_bwd_scaled(dm, logits, b.topk_idx, b.topk_w, grouped.get("routed_scale", 1.0), b.dw_rows,
+                                    b.token_to_row, b.d_logits, stream)
+    else:
+        B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits, stream)
     return b.dx
 
 

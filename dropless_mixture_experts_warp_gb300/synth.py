@@ -50,6 +50,12 @@ class MoEConfig:
     f_shared: int = 0            # always-on shared expert width (0 = none)
     router_std: float = 0.02
     seed: int = 1000
+    # group-limited sigmoid routing (0 = plain top-k): groups, eligible groups, the
+    # routed scaling factor and the std of a per-expert selection bias
+    n_group: int = 0
+    topk_group: int = 0
+    routed_scale: float = 1.0
+    sel_bias_std: float = 0.0
 
     @property
     def R(self) -> int:
@@ -83,6 +89,11 @@ CONFIGS: Dict[str, MoEConfig] = {
     # (x 256 MB, routed rows 512 MB) with small experts
     "hbm-probe": MoEConfig("hbm-probe", T=32768, d=4096, f=128, E=8, k=2, score=SOFTMAX,
                            bias="normal", bias_param=0.5, seed=1008),
+    # DeepSeek-V3 shape with its group-limited router: 8 groups of 32, 4 eligible,
+    # routed scale 2.5, a small per-expert selection bias
+    "dsv3-grouped": MoEConfig("dsv3-grouped", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
+                              bias="zipf", bias_param=1.0, forced_empty=4, f_shared=2048, seed=1009,
+                              n_group=8, topk_group=4, routed_scale=2.5, sel_bias_std=0.05),
     "dsv3": MoEConfig("dsv3", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
                       bias="zipf", bias_param=1.0, forced_empty=4, f_shared=2048, seed=1005),
 }
@@ -149,6 +160,21 @@ def router_bias(cfg: MoEConfig) -> np.ndarray:
     for e in cfg.forced_empty_ids:
         b[e] = np.float32(-1e4)
     return b
+
+
+def selection_bias(cfg: MoEConfig) -> np.ndarray:
+    """Per-expert selection bias [E] fp32 of the group-limited router (zeros if unused)."""
+    if not cfg.n_group or cfg.sel_bias_std == 0.0:
+        return np.zeros(cfg.E, np.float32)
+    return (np.random.default_rng(cfg.seed + 31).standard_normal(cfg.E) * cfg.sel_bias_std).astype(np.float32)
+
+
+def grouped_options(cfg: MoEConfig):
+    """The group-limited routing options of a config as plain values (None if plain top-k)."""
+    if not cfg.n_group:
+        return None
+    return {"n_group": cfg.n_group, "topk_group": cfg.topk_group, "routed_scale": cfg.routed_scale,
+            "bias": selection_bias(cfg)}
 
 
 def token_inputs(cfg: MoEConfig, T: Optional[int] = None) -> Dict[str, np.ndarray]:

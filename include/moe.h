@@ -117,6 +117,24 @@ moe_status moe_route_topk(const moe_dims* dims, const float* logits, int32_t* to
                           void* stream);
 
 /*
+ * Group-limited routing (the DeepSeek-V3 router variant; neither page states it -- a
+ * NEXT step of the route of step 1): dims->score must be MOE_SCORE_SIGMOID.
+ *   s = sigmoid(logit); selection score c = s + bias[e] (fp32; bias may be NULL = 0 and
+ *   steers selection only); the E experts form n_group groups of E / n_group
+ *   consecutive experts; a group's score is the sum of its two largest c; the
+ *   topk_group best groups are eligible (ties to the lower group); the top-k of c over
+ *   their experts are chosen (ties to the lower expert, slot j the j-th best);
+ *   topk_w = routed_scale * s_j / sum_j s_j.
+ * Requirements: 1 <= n_group <= 32, E % n_group == 0, E / n_group >= 2,
+ *   1 <= topk_group <= n_group, k <= topk_group * E / n_group, routed_scale > 0;
+ *   otherwise MOE_ERR_INVALID_ARG.  Outputs, workspace and errors as moe_route_topk.
+ */
+moe_status moe_route_topk_grouped(const moe_dims* dims, const float* logits, const float* bias, int32_t n_group,
+                                  int32_t topk_group, float routed_scale, int32_t* topk_idx, float* topk_w,
+                                  int32_t* split_sizes, int32_t* offsets, int32_t* row_offsets, void* workspace,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * Step 2 -- dispatch: copy every token to one row per selected expert, experts
  * contiguous, tokens of one expert in token order [DROPLESS "Az egyenetlen terhelés
  * lassítja a tanítást": ragged per-expert tensors; MEGA "Mega MoE คืออะไร?":
@@ -272,6 +290,15 @@ moe_status moe_route_topk_bwd(const moe_dims* dims, const float* logits,
                               const int32_t* topk_idx, const float* topk_w,
                               const float* dw_rows, const int32_t* token_to_row,
                               float* d_logits, void* stream);
+
+/*
+ * Router backward of moe_route_topk_grouped (sigmoid scores, weights scaled by
+ * routed_scale; the bias has no gradient): as moe_route_topk_bwd with
+ *   dL/ds_i = (routed_scale * dw_i - sum_j w_j dw_j) / sum_j s_j for the chosen i.
+ */
+moe_status moe_route_topk_bwd_scaled(const moe_dims* dims, const float* logits, const int32_t* topk_idx,
+                                     const float* topk_w, float routed_scale, const float* dw_rows,
+                                     const int32_t* token_to_row, float* d_logits, void* stream);
 
 /*
  * moe_gemm_down_dgrad without a workspace, for callers that cannot allocate device

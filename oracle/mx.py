@@ -141,19 +141,24 @@ def mx_matmul(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:
 # ----------------------------------------------------------------------------------
 
 def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=None,
-                   dtype=np.float64, matmul=mx_matmul):
+                   dtype=np.float64, matmul=mx_matmul, grouped=None):
     """Forward of the layer with every GEMM operand quantised along its contraction axis.
 
     Same steps as moe_oracle.moe_forward; the two GEMMs of each expert become
     G|U = mx(X_e, W_gu[e]) (both along d) and Y = mx(H_e, W_d[e]) (both along f).
-    ``matmul`` is the GEMM used (identity quantisation gives back the plain forward).
+    ``matmul`` is the GEMM used (identity quantisation gives back the plain forward);
+    ``grouped`` selects the group-limited router as in moe_oracle.moe_forward.
     """
     from . import moe_oracle as om
     x = np.asarray(x, dtype)
     T, d = x.shape
     E = w_gu.shape[0]
     f = w_d.shape[2]
-    idx, w = om.route(logits, k, score, dtype)
+    if grouped is not None:
+        idx, w = om.route_grouped(logits, k, grouped["n_group"], grouped["topk_group"], grouped.get("bias"),
+                                  grouped.get("routed_scale", 1.0), dtype)
+    else:
+        idx, w = om.route(logits, k, score, dtype)
     y_slot = np.zeros((T, k, d), dtype)
     g_slot = np.zeros((T, k, f), dtype)
     u_slot = np.zeros((T, k, f), dtype)
@@ -183,7 +188,7 @@ def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=
 
 
 def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=None, w_d_s=None,
-                    dtype=np.float64, matmul=mx_matmul):
+                    dtype=np.float64, matmul=mx_matmul, grouped=None):
     """Backward with MXFP8 GEMM operands (quantisation treated as identity in the chain rule).
 
     Per expert e, rows in token order (its segment):
@@ -227,7 +232,8 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
     for j in range(k):
         dx += dx_slot[:, j]
     out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw,
-           "d_logits": om.route_backward(logits, idx, w, dw, score, dtype)}
+           "d_logits": om.route_backward(logits, idx, w, dw, om.SIGMOID if grouped is not None else score, dtype,
+                                         1.0 if grouped is None else grouped.get("routed_scale", 1.0))}
     if w_gu_s is not None:
         fs = w_d_s.shape[1]
         wg = np.asarray(w_gu_s, dtype)
