@@ -540,15 +540,14 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
     const long long ld2 = 2ll * p.f;
     float dwp = 0.0f;
     const int cb = half * (BN / NH);
+    // the saved G and U of the next chunk are fetched while this one is processed
+    GuChunk nx;
+    load_gu_chunk(p, row, row_ok, c.out_col + cb, nx);
     for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
-      // the saved G and U are fetched before the accumulator so both latencies overlap
       uint4 g4[4], u4[4];
-      if (row_ok) {
-        const uint4* gsrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + c.out_col + c0);
-        const uint4* usrc = reinterpret_cast<const uint4*>(p.gu_in + row * ld2 + p.f + c.out_col + c0);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) { g4[v] = gsrc[v]; u4[v] = usrc[v]; }
-      }
+      for (int v = 0; v < 4; ++v) { g4[v] = nx.g[v]; u4[v] = nx.u[v]; }
+      if (c0 + 32 < cb + BN / NH) load_gu_chunk(p, row, row_ok, c.out_col + c0 + 32, nx);
       uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_wait_ld();
