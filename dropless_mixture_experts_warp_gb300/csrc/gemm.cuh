@@ -266,6 +266,17 @@ __device__ __forceinline__ void acc_load_chunks(uint32_t tbase, int col0, int nc
   tmem_wait_ld();
 }
 
+// A 32 x 32 bf16 box (row `lane`, 32 fp32 values) into a 2 KB staging buffer in the
+// layout of a 64-byte-swizzled tensor store (16-byte chunk j of row r at j ^ ((r >> 1) & 3)).
+__device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int lane, const float (&v)[32]) {
+  const uint32_t row_addr = smem_u32(buf) + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(row_addr + ((j ^ sw) << 4), pack_bf16(v[8 * j + 0], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                 pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+}
+
 // Part 2: the chunks (columns x0 .. x0 + 32 nc of output rows y0 .. y0 + 31) leave as
 // bf16 through the warp's 2 KB staging buffer (64-byte swizzle, as store_tile_tma)
 // and one tensor store each, while the next tile accumulates.

@@ -30,8 +30,10 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
 // count (eight for SwiGLU', four for SwiGLU: measured faster than eight).
 __host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
 __host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
+// staging per epilogue warp: STORE 2 KB; SwiGLU 6 KB (its G, U and h boxes)
 __host__ __device__ constexpr int p_smem_bytes(int epi) {
-  return P_STAGES * P_STAGE_BYTES + (epi == 0 ? pair_epi_warps(epi) * 2048 : 0) + 1024;
+  return P_STAGES * P_STAGE_BYTES + (epi == 0 ? pair_epi_warps(epi) * 2048 : 0) +
+         (epi == 1 ? pair_epi_warps(epi) * 6144 : 0) + 1024;
 }
 
 struct PairTile {
@@ -95,7 +97,8 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                             const GemmParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[P_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[P_STAGES];
@@ -143,7 +146,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_STORE) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) { tmem_alloc_pair(&s_tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
   tc_fence_before();
@@ -239,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
-    uint8_t* stg = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * 2048;
+    uint8_t* stg = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * (EPI == EPI_SWIGLU_FWD ? 6144 : 2048);
     for (int tile = pair; tile < total; tile += npairs) {
       const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
@@ -262,15 +266,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
         }
         continue;
       }
-      if (!tile_epilogue<EPI, pair_epi_warps(EPI) / 4>(p, t.c, tbase, row, row < t.row_end, BN, (warp - 2) >> 2, q,
-                                                       row_in_tile, hand))
+      if (EPI == EPI_SWIGLU_FWD) {
+        // G | U (tmC) and h (tmD) through three 2 KB staging boxes and tensor stores: the
+        // warp's 32 rows, h columns out_col + c0 .. + 31 (G at c0, U at BN / 2 + c0)
+        const bool row_ok = row < t.row_end;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+        const bool blk_ok = t.c.out_row + q * 32 < t.row_end;  // 32-row blocks never straddle it
+        const int y0 = static_cast<int>(t.c.out_row + q * 32);
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c0, g);
+          tmem_ld32(tbase + BN / 2 + c0, u);
+          tmem_wait_ld();
+          float gv[32], uv[32], hv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            gv[i] = __uint_as_float(g[i]);
+            uv[i] = __uint_as_float(u[i]);
+            hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
+          }
+          if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the boxes
+          __syncwarp();
+          stage_row_bf16(stg, lane, gv);
+          stage_row_bf16(stg + 2048, lane, uv);
+          stage_row_bf16(stg + 4096, lane, hv);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && blk_ok) {
+            tma_store_2d(&tmC, stg, t.c.out_col + c0, y0);
+            tma_store_2d(&tmC, stg + 2048, p.f + t.c.out_col + c0, y0);
+            tma_store_2d(&tmD, stg + 4096, t.c.out_col + c0, y0);
+            bulk_commit();
+          }
+        }
+      } else if (!tile_epilogue<EPI, pair_epi_warps(EPI) / 4>(p, t.c, tbase, row, row < t.row_end, BN,
+                                                              (warp - 2) >> 2, q, row_in_tile, hand)) {
         break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
-    if (EPI == EPI_STORE && lane == 0) bulk_wait_all();  // the tensor stores are complete
+    if ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && lane == 0) bulk_wait_all();  // tensor stores complete
   }
 
   tc_fence_before();

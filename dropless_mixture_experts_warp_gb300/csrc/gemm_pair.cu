@@ -5,8 +5,15 @@ namespace moe {
 
 cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                              cudaStream_t stream) {
-  CUtensorMap c = a;
-  if (kind != GEMM_ROWS_SWIGLU_FWD && kind != GEMM_ROWS_SWIGLU_BWD) {  // STORE: a map of the output
+  CUtensorMap c = a, dd = a;
+  if (kind == GEMM_ROWS_SWIGLU_FWD) {  // maps of G|U [rows][2f] and h [rows][f]
+    const uintptr_t al = reinterpret_cast<uintptr_t>(p.gu_out) | reinterpret_cast<uintptr_t>(p.h_out);
+    if (!p.gu_out || !p.h_out || (al & 15u) || p.f % 8 != 0) return cudaErrorInvalidValue;
+    const uint64_t rows = static_cast<uint64_t>(p.row_limit);
+    if (!make_tensor_map_store(&c, p.gu_out, 2ull * p.f, 2ull * p.f, rows) ||
+        !make_tensor_map_store(&dd, p.h_out, static_cast<uint64_t>(p.f), static_cast<uint64_t>(p.f), rows))
+      return cudaErrorInvalidValue;
+  } else if (kind != GEMM_ROWS_SWIGLU_BWD) {  // STORE: a map of the output
     if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
     const uint64_t rows = kind == GEMM_KGROUP_STORE ? static_cast<uint64_t>(p.E) * p.M
                                                     : static_cast<uint64_t>(p.row_limit);
@@ -14,19 +21,19 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
   }
   switch (kind) {
     case GEMM_ROWS_SWIGLU_FWD:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_FWD, false, false>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_FWD, false, false>(a, b, c, dd, p, stream);
     case GEMM_ROWS_STORE:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, false>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, false>(a, b, c, dd, p, stream);
     case GEMM_ROWS_STORE_BMN:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, true>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, false, true>(a, b, c, dd, p, stream);
     case GEMM_ROWS_SWIGLU_BWD:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_BWD, false, true>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_SWIGLU_BWD, false, true>(a, b, c, dd, p, stream);
     case GEMM_KGROUP_STORE:
-      return launch_gemm_pair_t<SCHED_KGROUP, EPI_STORE, true, true>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_KGROUP, EPI_STORE, true, true>(a, b, c, dd, p, stream);
     case GEMM_DENSE_AMN_BK:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, false>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, false>(a, b, c, dd, p, stream);
     case GEMM_DENSE_AMN_BMN:
-      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, true>(a, b, c, p, stream);
+      return launch_gemm_pair_t<SCHED_ROWS, EPI_STORE, true, true>(a, b, c, dd, p, stream);
     default:
       return cudaErrorInvalidValue;
   }

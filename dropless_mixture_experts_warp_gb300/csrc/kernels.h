@@ -79,15 +79,16 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
 // one per two SMs.
 int pair_grid(const void* kern, int threads, int smem_bytes);
 
-// c: tensor map of the bf16 output for the STORE epilogue (ignored otherwise)
+// c: tensor map of the bf16 output for the STORE epilogue, of G|U for the SwiGLU one;
+// dd: of h for the SwiGLU epilogue (unused otherwise)
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                               const GemmParams& p, cudaStream_t stream) {
+                               const CUtensorMap& dd, const GemmParams& p, cudaStream_t stream) {
   auto kern = grouped_gemm_pair_kernel<SCHED, EPI, A_MN, B_MN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(EPI));
   if (err != cudaSuccess) return err;
   static const int grid = pair_grid(reinterpret_cast<const void*>(kern), pair_threads(EPI), p_smem_bytes(EPI));
-  kern<<<grid, pair_threads(EPI), p_smem_bytes(EPI), stream>>>(a, b, c, p);
+  kern<<<grid, pair_threads(EPI), p_smem_bytes(EPI), stream>>>(a, b, c, dd, p);
   count_launch();
   return cudaGetLastError();
 }
