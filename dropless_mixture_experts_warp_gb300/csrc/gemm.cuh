@@ -384,16 +384,12 @@ __device__ __forceinline__ void load_gu_chunk(const GemmParams& p, long long row
   }
 }
 
-// One 32-column chunk: dH (fp32, accumulator columns of h columns col .. col + 31)
-// and the saved G, U -> dG = w dH U silu'(G), dU = w dH silu(G), quantised along the
-// row (dG at column col, dU at f + col of dG|dU) and down the columns (the warp's 32
-// rows form one block); dwp gathers the row's sum of silu(G) U dH.
-__device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row, bool row_ok, bool blk_ok, float w,
-                                             int col, const uint32_t (&r)[32], const GuChunk& gu, float& dwp,
-                                             float* xbuf, int lane, long long rblk) {
-  const long long ld2 = 2ll * p.f;
-  float dg[32], du[32];
-  float part[4];  // the chunk's dw terms in four fixed-order partial sums
+// SwiGLU' of one 32-column chunk: dH (fp32 accumulator columns) and the saved G, U
+// (bf16) -> dG = w dH U silu'(G), dU = w dH silu(G); returns the chunk's share of the
+// row's sum of silu(G) U dH (four fixed-order partial sums).
+__device__ __forceinline__ float swiglu_bwd_values(const uint32_t (&r)[32], const GuChunk& gu, float w,
+                                                   float (&dg)[32], float (&du)[32]) {
+  float part[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint32_t gw[4] = {gu.g[v].x, gu.g[v].y, gu.g[v].z, gu.g[v].w};
@@ -412,7 +408,19 @@ __device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row,
       du[8 * v + i] = da * silu;
     }
   }
-  dwp += (part[0] + part[1]) + (part[2] + part[3]);
+  return (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+// One 32-column chunk: dH (fp32, accumulator columns of h columns col .. col + 31)
+// and the saved G, U -> dG, dU as above, quantised along the row (dG at column col,
+// dU at f + col of dG|dU) and down the columns (the warp's 32 rows form one block);
+// dwp gathers the row's sum of silu(G) U dH.
+__device__ __forceinline__ void bwd_mx_chunk(const GemmParams& p, long long row, bool row_ok, bool blk_ok, float w,
+                                             int col, const uint32_t (&r)[32], const GuChunk& gu, float& dwp,
+                                             float* xbuf, int lane, long long rblk) {
+  const long long ld2 = 2ll * p.f;
+  float dg[32], du[32];
+  dwp += swiglu_bwd_values(r, gu, w, dg, du);
   if (row_ok) {
     uint32_t q[8];
     uint32_t sb = quant_block32(dg, q);

@@ -30,10 +30,9 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
 // count (eight for SwiGLU', four for SwiGLU: measured faster than eight).
 __host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
 __host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
-// staging per epilogue warp: STORE 2 KB; SwiGLU 6 KB (its G, U and h boxes)
+// staging per epilogue warp: STORE and SwiGLU' 2 KB; SwiGLU 6 KB (its G, U and h boxes)
 __host__ __device__ constexpr int p_smem_bytes(int epi) {
-  return P_STAGES * P_STAGE_BYTES + (epi == 0 ? pair_epi_warps(epi) * 2048 : 0) +
-         (epi == 1 ? pair_epi_warps(epi) * 6144 : 0) + 1024;
+  return P_STAGES * P_STAGE_BYTES + pair_epi_warps(epi) * (epi == 1 ? 6144 : 2048) + 1024;
 }
 
 struct PairTile {
@@ -146,7 +145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmC);
     if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) { tmem_alloc_pair(&s_tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
@@ -299,6 +298,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             bulk_commit();
           }
         }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        // dG then dU (tmC, a map of dG|dU) through the warp's 2 KB staging box and tensor
+        // stores; this warp takes half of the tile's h columns
+        const bool row_ok = row < t.row_end;
+        const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
+        const bool blk_ok = t.c.out_row + q * 32 < t.row_end;
+        const int y0 = static_cast<int>(t.c.out_row + q * 32);
+        const int half = (warp - 2) >> 2;
+        const int cb = half * (BN / 2);
+        float dwp = 0.0f;
+        GuChunk nx;  // the saved G and U of the next chunk are fetched during this one
+        load_gu_chunk(p, row, row_ok, t.c.out_col + cb, nx);
+        for (int c0 = cb; c0 < cb + BN / 2; c0 += 32) {
+          const GuChunk cur = nx;
+          if (c0 + 32 < cb + BN / 2) load_gu_chunk(p, row, row_ok, t.c.out_col + c0 + 32, nx);
+          uint32_t r[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_wait_ld();
+          float dg[32], du[32];
+          dwp += swiglu_bwd_values(r, cur, w, dg, du);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous store has read the box
+            __syncwarp();
+            stage_row_bf16(stg, lane, j == 0 ? dg : du);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && blk_ok) {
+              tma_store_2d(&tmC, stg, (j == 0 ? 0 : p.f) + t.c.out_col + c0, y0);
+              bulk_commit();
+            }
+          }
+        }
+        if (!dw_combine<2>(p, t.c, row, row_ok, half, q, row_in_tile, hand, dwp)) break;
       } else if (!tile_epilogue<EPI, pair_epi_warps(EPI) / 4>(p, t.c, tbase, row, row < t.row_end, BN,
                                                               (warp - 2) >> 2, q, row_in_tile, hand)) {
         break;
@@ -308,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
-    if ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && lane == 0) bulk_wait_all();  // tensor stores complete
+    if (lane == 0) bulk_wait_all();  // tensor stores complete
   }
 
   tc_fence_before();
