@@ -273,6 +273,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// a *= s, b *= s in one packed fp32 multiply (round to nearest even, no flush: the
+// same result as two scalar multiplies)
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, uint64_t ss) {
+  asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%0, %1};\n\tmul.rn.f32x2 x, x, %2;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "l"(ss));
+}
+
 // Quantise 32 fp32 values (one block) into 8 words of codes; returns the scale byte.
 __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&codes)[8]) {
   float m[8];  // a tree of maxima: short dependency chains
@@ -281,12 +289,14 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
     m[j] = fmaxf(fmaxf(fabsf(v[4 * j]), fabsf(v[4 * j + 1])), fmaxf(fabsf(v[4 * j + 2]), fabsf(v[4 * j + 3])));
   const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
   const int e = mx_scale_exp(amax);
-  const float s = exp2_neg(e);
+  const uint32_t sb = __float_as_uint(exp2_neg(e));
+  const uint64_t ss = (static_cast<uint64_t>(sb) << 32) | sb;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const uint32_t a = cvt_e4m3x2(v[4 * w + 0] * s, v[4 * w + 1] * s);
-    const uint32_t b = cvt_e4m3x2(v[4 * w + 2] * s, v[4 * w + 3] * s);
-    codes[w] = a | (b << 16);
+    float x0 = v[4 * w + 0], x1 = v[4 * w + 1], x2 = v[4 * w + 2], x3 = v[4 * w + 3];
+    mul_f32x2(x0, x1, ss);
+    mul_f32x2(x2, x3, ss);
+    codes[w] = cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16);
   }
   return static_cast<uint32_t>(e + 127);
 }
