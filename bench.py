@@ -72,22 +72,31 @@ def config_json(cfg, prec="bf16"):
             "parallelism": "replicas"}
 
 
-def source_hash() -> str:
+# The files that define each precision's dominant GEMM kernel and its launch (tile
+# shape, schedule, tensor maps): recorded DRAM traffic stays valid while they are
+# unchanged.
+KERNEL_SOURCES = {
+    "bf16": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_pair.cu", "kernels.h", "api.cu"),
+    "mxfp8": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "kernels.h", "api_mx.cu"),
+}
+
+
+def source_hash(prec: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dropless_mixture_experts_warp_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in KERNEL_SOURCES[prec]:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
 def read_traffic(kernel_key: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernels have not changed since.
-    kernel_key is "<precision>:<config>:<gemm>"."""
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's sources have not
+    changed since.  kernel_key is "<precision>:<config>:<gemm>"."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = source_hash()
+    cur = source_hash(kernel_key.split(":")[0])
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key and parts[2] == cur:
