@@ -62,14 +62,15 @@ def l2_note(cfg) -> str:
     return "inputs smaller than L2 (a small case: not a bandwidth measurement)"
 
 
-def config_json(cfg, prec="bf16"):
+def config_json(cfg, prec="bf16", weights_cached=False):
     bias = {"normal": f"N(0,{cfg.bias_param})", "zipf": f"Zipf(s={cfg.bias_param})", "zero": "0"}[cfg.bias]
     return {"workload": workload_name(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
             "f_shared": cfg.f_shared, "routing": f"{cfg.score} top-{cfg.k}, router bias {bias}" +
             (f", group-limited ({cfg.topk_group} of {cfg.n_group} groups), routed scale {cfg.routed_scale}, "
              f"selection bias N(0,{cfg.sel_bias_std})" if cfg.n_group else ""),
             "precision": prec, "l2": l2_note(cfg),
-            "parallelism": "replicas"}
+            "parallelism": "replicas"} | ({"weights": "MXFP8 weights quantised once per optimiser step, "
+                                                   "before the timed micro-batches"} if weights_cached else {})
 
 
 # The files that define each precision's dominant GEMM kernel and its launch (tile
@@ -280,8 +281,10 @@ def run_native(args, cfg):
             B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
                              b.workspace, b.status, stream)
         if mx8:
-            # the 16-bit master weights are quantised every step; x is quantised in the dispatch
-            B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
+            # the 16-bit master weights are quantised every step (unless they are cached for
+            # the optimiser step's micro-batches); x is quantised in the dispatch
+            if not args.weights_cached:
+                B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
             B.moe_permute_mx(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.mx_ws,
                              b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
         else:
@@ -299,7 +302,8 @@ def run_native(args, cfg):
             B.moe_gemm_down(dm, b.h, b.row_offsets, w_d, b.y_rows, b.status, stream)
         mark(2)
         if cfg.f_shared and mx8:
-            B.moe_mx_quantize_shared_weights(dm, inp["w_gu_s"], inp["w_d_s"], b.wq_s, stream)
+            if not args.weights_cached:
+                B.moe_mx_quantize_shared_weights(dm, inp["w_gu_s"], inp["w_d_s"], b.wq_s, stream)
             B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.y_s, b.status, stream)
         elif cfg.f_shared:
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
@@ -342,6 +346,10 @@ def run_native(args, cfg):
             B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits,
                                  stream)
 
+    if args.weights_cached:
+        # once per optimiser step, outside the timed micro-batches
+        with torch.cuda.stream(stream):
+            layer.quantize_weights(bufs, w_gu, w_d, stream, inp.get("w_gu_s"), inp.get("w_d_s"))
     for _ in range(args.warmup):
         step()
     layer.check(bufs, stream)
@@ -422,7 +430,7 @@ def run_native(args, cfg):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3+e8m0 (MXFP8), fp32 acc" if mx8 else "bf16", "data": "synthetic",
-        "config": config_json(cfg, args.prec),
+        "config": config_json(cfg, args.prec, args.weights_cached),
         "tokens_per_s": world * cfg.T / (ms * 1e-3),
         "frac_of_peak": value / world / peak,
         "roofline": {"bound": "tensor", "kernel": f"{dom} ({(GEMM_KERNEL_MX if mx8 else GEMM_KERNEL)[dom]})", "achieved": achieved,
@@ -467,7 +475,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights-cached", action="store_true",
+                    help="MXFP8: quantise the weights once before timing (one optimiser step shared by "
+                         "micro-batches) instead of in every timed step")
     args = ap.parse_args()
+    if args.weights_cached and args.prec != "mxfp8":
+        ap.error("--weights-cached applies to --prec mxfp8")
     from dropless_mixture_experts_warp_gb300 import synth
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":

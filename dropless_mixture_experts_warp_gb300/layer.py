@@ -94,14 +94,31 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
     )
 
 
-def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None, grouped=None):
+def quantize_weights(b: Buffers, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None):
+    """MXFP8: the 16-bit master weights -> b.wq (and b.wq_s for the shared expert), codes and
+    scales in both contraction orientations.  The weights change once per optimiser step, so a
+    step of several micro-batches quantises them once and passes weights_cached=True to every
+    forward() of the step."""
+    dm = b.dims
+    if dm.prec != 1:
+        raise ValueError("quantize_weights: the layer is not MXFP8")
+    B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
+    if dm.f_shared:
+        B.moe_mx_quantize_shared_weights(dm, w_gu_s, w_d_s, b.wq_s, stream)
+
+
+def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None, grouped=None,
+            weights_cached=False):
     """grouped: {"n_group", "topk_group", "bias" (device [E] fp32 or None), "routed_scale"} selects the
-    group-limited sigmoid router instead of the plain top-k."""
+    group-limited sigmoid router instead of the plain top-k.  weights_cached (MXFP8): b.wq (and
+    b.wq_s) already hold this step's quantised weights (quantize_weights()), so they are not
+    quantised again."""
     dm = b.dims
     mx8 = dm.prec == 1
+    if mx8 and not weights_cached:
+        quantize_weights(b, w_gu, w_d, stream, w_gu_s, w_d_s)
     shared_out = None
     if dm.f_shared and mx8:
-        B.moe_mx_quantize_shared_weights(dm, w_gu_s, w_d_s, b.wq_s, stream)
         B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.y_s, b.status, stream)
         shared_out = b.y_s
     elif dm.f_shared:
@@ -115,8 +132,6 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
         B.moe_route_topk(dm, logits, b.topk_idx, b.topk_w, b.split_sizes, b.offsets, b.row_offsets,
                          b.workspace, b.status, stream)
     if mx8:
-        # the 16-bit master weights are quantised every step (they change every optimiser step)
-        B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
         B.moe_permute_mx(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.mx_ws,
                          b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
         B.moe_gemm_gate_up_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.status, stream)

@@ -200,3 +200,37 @@ def test_mx_zero_tokens():
     layer.check(b)
     assert host(b.split_sizes).sum() == 0 and host(b.row_offsets)[-1] == 0
     assert torch.count_nonzero(b.dw_gu) == 0 and torch.count_nonzero(b.dw_d) == 0
+
+
+@pytest.mark.parametrize("name", ["mx-ragged", "mx-shared"])
+def test_mx_weights_cached_across_micro_batches(name):
+    """Weights quantised once per optimiser step and reused by two micro-batches give the same
+    bits as quantising them in every forward(), and the cached codes are left untouched."""
+    need_gpu()
+    import dataclasses
+    from dropless_mixture_experts_warp_gb300 import layer
+    cfg = CASES[name]
+    w_gu_b, w_d_b = synth.all_expert_weights(cfg)
+    w_gu, w_d = bf16_dev(w_gu_b), bf16_dev(w_d_b)
+    sh = {}
+    if cfg.f_shared:
+        s_gu, s_d = synth.shared_weights(cfg)
+        sh = {"w_gu_s": bf16_dev(s_gu), "w_d_s": bf16_dev(s_d)}
+    micro = [synth.token_inputs(cfg), synth.token_inputs(dataclasses.replace(cfg, seed=cfg.seed + 100))]
+    dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, "mxfp8")
+    cached = layer.allocate(dims)
+    layer.quantize_weights(cached, w_gu, w_d, **sh)
+    wq0 = cached.wq.clone()
+    outs = ("y", "dx", "d_logits", "dw_gu", "dw_d")
+    for inp in micro:
+        x, logits, dy = bf16_dev(inp["x"]), f32_dev(inp["logits"]), bf16_dev(inp["dy"])
+        layer.forward(cached, x, logits, w_gu, w_d, weights_cached=True, **sh)
+        layer.backward(cached, dy, logits, w_gu, w_d, x=x, **sh)
+        layer.check(cached)
+        ref, _, _, _ = _run(cfg, inp)
+        for key in outs:
+            assert torch.equal(getattr(cached, key), getattr(ref, key)), key
+        if cfg.f_shared:
+            assert torch.equal(cached.dw_gu_s, ref.dw_gu_s) and torch.equal(cached.dw_d_s, ref.dw_d_s)
+    assert torch.equal(cached.wq, wq0)
+    assert not torch.equal(getattr(_run(cfg, micro[1])[0], "y"), getattr(_run(cfg, micro[0])[0], "y"))
