@@ -26,8 +26,9 @@ constexpr int P_B_BYTES_MAX = 128 * BK * 2;           // half of a 256-row B til
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
 // STORE runs eight epilogue warps (two per TMEM lane quarter, splitting the columns)
 // that read their accumulator columns at once and write them through 2 KB staging
-// buffers and tensor stores; the other epilogues keep the shared epilogue's warp
-// count (eight for SwiGLU', four for SwiGLU: measured faster than eight).
+// buffers and tensor stores; the SwiGLU epilogues keep the shared epilogue's warp
+// count (eight for SwiGLU', four for SwiGLU: measured faster than eight) and also
+// write through staging boxes and tensor stores.
 __host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
 __host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
 // staging per epilogue warp: STORE and SwiGLU' 2 KB; SwiGLU 6 KB (its G, U and h boxes)
