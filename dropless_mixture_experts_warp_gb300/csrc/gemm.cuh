@@ -102,8 +102,47 @@ struct TileCoord {
   long long out_base; // element offset of the group's output (SCHED_KGROUP)
 };
 
+// Ragged-K schedule (SCHED_KGROUP, the weight gradients): a tile's cost is its
+// expert's row count, which routing skew spreads over an order of magnitude.  When
+// one tile is a sizeable share of a worker's mean load (the longest above 5 %: few
+// tiles per expert, a few experts holding most rows), plain round robin leaves some
+// workers with the long end of every round, so the experts are visited in decreasing
+// row count (ties: lower index first) and the workers deal the tiles in a snake:
+// round r gives worker w tile r * W + w (r even) or r * W + W - 1 - w (r odd).
+// Otherwise the experts keep their index order and the deal stays round robin (with
+// many tiles per expert the sorted order measured slower: every worker then starts on
+// the hottest expert at once).  order[rank] = expert; per: tiles per expert; W:
+// workers.  Every thread of the block calls it once the row offsets are in shared
+// memory; all get the same answer (true: sorted snake).
+__device__ __forceinline__ bool kgroup_order(const int* s_ro, int E, int per, int W, int* order) {
+  int longest = 0;
+  for (int j = 0; j < E; ++j) longest = max(longest, s_ro[j + 1] - s_ro[j]);
+  const long long mean_load = static_cast<long long>(s_ro[E] - s_ro[0]) * per / W;  // rows per worker
+  const bool lpt = 20ll * longest > mean_load;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = s_ro[e + 1] - s_ro[e];
+    int rank = e;
+    if (lpt) {
+      rank = 0;
+      for (int j = 0; j < E; ++j) {
+        const int m = s_ro[j + 1] - s_ro[j];
+        rank += (m > n || (m == n && j < e)) ? 1 : 0;
+      }
+    }
+    order[rank] = e;
+  }
+  return lpt;
+}
+
+// The tile worker w of W takes in its round r (see kgroup_order).
+__device__ __forceinline__ int sched_tile(int r, int w, int W, bool snake) {
+  return r * W + ((snake && (r & 1)) ? W - 1 - w : w);
+}
+
+// order: the experts in their visiting order (SCHED_KGROUP, kgroup_order; unused for
+// SCHED_ROWS)
 template <int SCHED, int EPI, bool B_MN, int KB = BK>
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* s_ro, int E,
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* s_ro, const int* order, int E,
                                                 int n_tiles, int tile) {
   TileCoord c;
   if (SCHED == SCHED_ROWS) {
@@ -129,8 +168,8 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
   } else {
     const int mt = p.M / BM;
     const int per = mt * n_tiles;
-    const int e = tile / per;
-    const int local = tile - e * per;
+    const int e = order[tile / per];
+    const int local = tile - (tile / per) * per;
     if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
@@ -638,6 +677,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
+  __shared__ int s_order[SCHED == SCHED_KGROUP ? MAX_EXPERTS : 1];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -650,6 +690,12 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   const int dense_rows = (SCHED == SCHED_KGROUP) ? (p.K + BK - 1) / BK * BK : (p.M + BM - 1) / BM * BM;
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
+  bool snake = false;
+  if (SCHED == SCHED_KGROUP) {
+    __syncthreads();
+    const int per = (p.M / BM) * (p.N / p.BN);
+    snake = kgroup_order(s_ro, E, per, gridDim.x, s_order);  // complete at the barrier below
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], epi_warps(EPI)); }
@@ -677,8 +723,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+      for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); ok && tile < total;
+           tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, s_order, E, n_tiles, tile);
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
                                  WAIT_LIMIT_CYCLES)) { ok = false; break; }
@@ -721,8 +768,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+      for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); ok && tile < total;
+           tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+        const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, s_order, E, n_tiles, tile);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status,
                                WAIT_LIMIT_CYCLES)) break;
         tc_fence_after();
@@ -763,8 +811,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, E, n_tiles, tile);
+    for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); tile < total;
+         tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+      const TileCoord c = tile_coord<SCHED, EPI, B_MN>(p, s_ro, s_order, E, n_tiles, tile);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES))
         break;
       tc_fence_after();

@@ -41,7 +41,8 @@ struct PairTile {
   long long row_end;  // rows at or beyond this are not stored
 };
 
-// s_pt[e]: first pair tile of expert e (SCHED_ROWS); rank: 0 (leader) or 1; KB: K
+// s_pt[e]: first pair tile of expert e (SCHED_ROWS) or the experts in their visiting
+// order (SCHED_KGROUP, kgroup_order); rank: 0 (leader) or 1; KB: K
 // elements per stage.
 template <int SCHED, int EPI, bool B_MN, int KB = BK>
 __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_ro, const int* s_pt, int E,
@@ -76,8 +77,8 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
   } else {
     const int mt2 = p.M / (2 * BM);
     const int per = mt2 * n_tiles;
-    const int e = tile / per;
-    const int local = tile - e * per;
+    const int e = s_pt[tile / per];  // the experts in their visiting order
+    const int local = tile - (tile / per) * per;
     if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
@@ -128,14 +129,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
   const int BN = p.BN;  // 128 or 256
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   __syncthreads();
+  // SCHED_KGROUP: s_pt holds the experts in their visiting order (kgroup_order);
+  // complete at the cluster barrier below
+  const bool snake =
+      SCHED == SCHED_KGROUP && kgroup_order(s_ro, E, (p.M / (2 * BM)) * n_tiles, npairs, s_pt);
   if (threadIdx.x == 0) {
-    // pair tiles per expert, exclusive prefix (E <= 1024, once per launch)
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      s_pt[e] = run;
-      run += ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2 * n_tiles;
+    if (SCHED == SCHED_ROWS) {
+      // pair tiles per expert, exclusive prefix (E <= 1024, once per launch)
+      int run = 0;
+      for (int e = 0; e < E; ++e) {
+        s_pt[e] = run;
+        run += ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2 * n_tiles;
+      }
+      s_pt[E] = run;
     }
-    s_pt[E] = run;
     for (int s = 0; s < P_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 2 * pair_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
@@ -164,7 +171,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total; tile += npairs) {
+      for (int rnd = 0, tile = sched_tile(0, pair, npairs, snake); ok && tile < total;
+           tile = sched_tile(++rnd, pair, npairs, snake)) {
         const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
         const TileCoord& c = t.c;
         for (int kb = 0; kb < c.kblocks; ++kb) {
@@ -206,7 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total; tile += npairs) {
+      for (int rnd = 0, tile = sched_tile(0, pair, npairs, snake); ok && tile < total;
+           tile = sched_tile(++rnd, pair, npairs, snake)) {
         const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, 0);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
         tc_fence_after();
@@ -244,7 +253,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
     uint8_t* stg = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * (EPI == EPI_SWIGLU_FWD ? 6144 : 2048);
-    for (int tile = pair; tile < total; tile += npairs) {
+    for (int rnd = 0, tile = sched_tile(0, pair, npairs, snake); tile < total;
+         tile = sched_tile(++rnd, pair, npairs, snake)) {
       const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
       tc_fence_after();

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
+  __shared__ int s_order[SCHED == SCHED_KGROUP ? MAX_EXPERTS : 1];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -73,6 +74,12 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
       (SCHED == SCHED_KGROUP) ? (p.K + MX_BK - 1) / MX_BK * MX_BK : (p.M + BM - 1) / BM * BM;
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
     s_ro[i] = p.row_offsets ? p.row_offsets[i] : (i == 0 ? 0 : dense_rows);
+  bool snake = false;
+  if (SCHED == SCHED_KGROUP) {
+    __syncthreads();
+    const int per = (p.M / BM) * (p.N / p.BN);
+    snake = kgroup_order(s_ro, E, per, gridDim.x, s_order);  // complete at the barrier below
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < MX_MAX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], mx_epi_warps(EPI)); }
@@ -107,8 +114,9 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+      for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); ok && tile < total;
+           tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, s_order, E, n_tiles, tile);
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, p.status,
                                  WAIT_LIMIT_CYCLES)) { ok = false; break; }
@@ -153,8 +161,9 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+      for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); ok && tile < total;
+           tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+        const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, s_order, E, n_tiles, tile);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, p.status,
                                WAIT_LIMIT_CYCLES)) break;
         tc_fence_after();
@@ -198,8 +207,9 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
     float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
     uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 2048;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, E, n_tiles, tile);
+    for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); tile < total;
+         tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
+      const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, s_order, E, n_tiles, tile);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
