@@ -423,31 +423,67 @@ __device__ __forceinline__ void load_gu_chunk(const GemmParams& p, long long row
   }
 }
 
+// Two fp32 lanes for the packed Blackwell fp32 pipe (mul/fma .rn.f32x2: each lane
+// rounds as the scalar instruction would).
+struct F2 {
+  float x, y;
+};
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+  F2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+  return t;
+}
+
 // SwiGLU' of one 32-column chunk: dH (fp32 accumulator columns) and the saved G, U
-// (bf16) -> dG = w dH U silu'(G), dU = w dH silu(G); returns the chunk's share of the
-// row's sum of silu(G) U dH (four fixed-order partial sums).
+// (bf16) -> dG = w dH U silu'(G), dU = w dH silu(G), with sigmoid as sigmoidf_ and
+// silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g))); returns the chunk's share of the
+// row's sum of silu(G) U dH (eight fixed-order partial sums).  Neighbouring columns
+// go through the packed fp32 pipe together.
 __device__ __forceinline__ float swiglu_bwd_values(const uint32_t (&r)[32], const GuChunk& gu, float w,
                                                    float (&dg)[32], float (&du)[32]) {
-  float part[4];
+  const F2 half{0.5f, 0.5f}, one{1.0f, 1.0f}, mone{-1.0f, -1.0f}, w2{w, w};
+  F2 part[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint32_t gw[4] = {gu.g[v].x, gu.g[v].y, gu.g[v].z, gu.g[v].w};
     const uint32_t uw[4] = {gu.u[v].x, gu.u[v].y, gu.u[v].z, gu.u[v].w};
-    part[v] = 0.0f;
+    part[v] = F2{0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-      const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
-      const float dh = __uint_as_float(r[8 * v + i]);
-      const float sg = sigmoidf_(g);
-      const float silu = g * sg;
-      const float da = w * dh;
-      part[v] += silu * u * dh;
-      dg[8 * v + i] = da * u * sg * (1.0f + g * (1.0f - sg));
-      du[8 * v + i] = da * silu;
+    for (int q = 0; q < 4; ++q) {
+      const int i = 8 * v + 2 * q;
+      const F2 g{bf16_lo(gw[q]), bf16_hi(gw[q])};
+      const F2 u{bf16_lo(uw[q]), bf16_hi(uw[q])};
+      const F2 dh{__uint_as_float(r[i]), __uint_as_float(r[i + 1])};
+      const F2 hg = mul2(half, g);
+      const F2 sg = fma2(half, F2{tanh_approx(hg.x), tanh_approx(hg.y)}, half);
+      const F2 silu = mul2(g, sg);
+      const F2 da = mul2(w2, dh);
+      part[v] = fma2(mul2(silu, u), dh, part[v]);
+      const F2 d = mul2(mul2(mul2(da, u), sg), fma2(g, fma2(sg, mone, one), one));
+      const F2 e = mul2(da, silu);
+      dg[i] = d.x;
+      dg[i + 1] = d.y;
+      du[i] = e.x;
+      du[i + 1] = e.y;
     }
   }
-  return (part[0] + part[1]) + (part[2] + part[3]);
+  return ((part[0].x + part[0].y) + (part[1].x + part[1].y)) + ((part[2].x + part[2].y) + (part[3].x + part[3].y));
 }
 
 // One 32-column chunk: dH (fp32, accumulator columns of h columns col .. col + 31)
