@@ -266,9 +266,12 @@ def run_native(args, cfg):
     unit = R * cfg.d * cfg.f
     grouped = synth.grouped_options(cfg)
     sel_bias = torch.from_numpy(grouped["bias"]).to(dev) if grouped is not None else None
+    base_io = (x, logits, dy, bufs.y, bufs.dx, bufs.d_logits)
 
-    def step(ev=None):
+    def step(ev=None, io=None):
+        # io: (x, logits, dy, y, dx, d_logits) device tensors of this step (default: the base ones)
         b, dm = bufs, dims
+        x, logits, dy, y_out, dx_out, dl_out = io if io is not None else base_io
 
         def mark(i):
             if ev is not None:
@@ -307,7 +310,7 @@ def run_native(args, cfg):
             B.moe_shared_mlp_fwd_mx(dm, x, b.wq_s, b.mx_ws_s, b.gu_s, b.y_s, b.status, stream)
         elif cfg.f_shared:
             B.moe_shared_mlp_fwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, b.y_s, b.status, stream)
-        B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, b.y, stream)
+        B.moe_combine_fwd(dm, b.y_rows, b.token_to_row, b.y_s, y_out, stream)
         if mx8:
             B.moe_combine_bwd_mx(dm, dy, b.row_to_token, b.split_sizes, b.row_offsets, b.mx_ws, stream)
         else:
@@ -338,13 +341,12 @@ def run_native(args, cfg):
         elif cfg.f_shared:
             B.moe_shared_mlp_bwd(dm, x, inp["w_gu_s"], inp["w_d_s"], b.gu_s, b.h_s, dy, b.dgu_s, b.dx_s,
                                  b.dw_gu_s, b.dw_d_s, b.status, stream)
-        B.moe_combine_fwd(dm, b.dxp, b.token_to_row, b.dx_s, b.dx, stream)
+        B.moe_combine_fwd(dm, b.dxp, b.token_to_row, b.dx_s, dx_out, stream)
         if grouped is not None:
             B.moe_route_topk_bwd_scaled(dm, logits, b.topk_idx, b.topk_w, grouped["routed_scale"], b.dw_rows,
-                                        b.token_to_row, b.d_logits, stream)
+                                        b.token_to_row, dl_out, stream)
         else:
-            B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, b.d_logits,
-                                 stream)
+            B.moe_route_topk_bwd(dm, logits, b.topk_idx, b.topk_w, b.dw_rows, b.token_to_row, dl_out, stream)
 
     if args.weights_cached:
         # once per optimiser step, outside the timed micro-batches
@@ -387,34 +389,66 @@ def run_native(args, cfg):
     gemm_ms = {g: statistics.mean(evs[s][a].elapsed_time(evs[s][b]) for s in range(args.steps))
                for g, (a, b) in windows.items()}
 
-    # end to end through the same calls with host buffers: H2D of this step's inputs,
-    # D2H of its results (Y, dX, d_logits), inside the timed region
+    # end to end through the same calls with host buffers: every step's inputs (x, logits,
+    # dY) come from pinned host memory and its results (Y, dX, d_logits) go back to pinned
+    # host memory inside the timed region.  As an input pipeline does, a copy stream moves
+    # step s + 1's inputs in and step s's results out while the compute stream runs the
+    # neighbouring step; the step's device inputs and results are double-buffered.
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
     lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True).copy_(logits)
     dy_h = torch.empty(dy.shape, dtype=dy.dtype, pin_memory=True).copy_(dy)
-    y_h = torch.empty(bufs.y.shape, dtype=bufs.y.dtype, pin_memory=True)
-    dx_h = torch.empty(bufs.dx.shape, dtype=bufs.dx.dtype, pin_memory=True)
-    dl_h = torch.empty(bufs.d_logits.shape, dtype=bufs.d_logits.dtype, pin_memory=True)
+    outs = (bufs.y, bufs.dx, bufs.d_logits)
+    host_out = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs) for _ in range(2)]
+    dev_io = [base_io, tuple(torch.empty_like(t) for t in base_io)]
     h2d = x_h.nbytes + lg_h.nbytes + dy_h.nbytes
-    d2h = y_h.nbytes + dx_h.nbytes + dl_h.nbytes
-    e2e_steps = max(1, min(args.steps, 10))
+    d2h = sum(t.nbytes for t in host_out[0])
+    e2e_steps = max(2, min(args.steps, 10))
+    copy = torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+
+    def to_device(i):
+        with torch.cuda.stream(copy):
+            for d, h in zip(dev_io[i][:3], (x_h, lg_h, dy_h)):
+                d.copy_(h, non_blocking=True)
+            in_ready[i].record(copy)
+
+    def to_host(i):
+        with torch.cuda.stream(copy):
+            copy.wait_event(done[i])
+            for h, d in zip(host_out[i], dev_io[i][3:]):
+                h.copy_(d, non_blocking=True)
+            out_free[i].record(copy)
+
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     start.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            x.copy_(x_h, non_blocking=True)
-            logits.copy_(lg_h, non_blocking=True)
-            dy.copy_(dy_h, non_blocking=True)
-            step()
-            y_h.copy_(bufs.y, non_blocking=True)
-            dx_h.copy_(bufs.dx, non_blocking=True)
-            dl_h.copy_(bufs.d_logits, non_blocking=True)
+    copy.wait_stream(stream)
+    to_device(0)
+    for s in range(e2e_steps):
+        i = s % 2
+        if s + 1 < e2e_steps:
+            if s >= 1:
+                copy.wait_event(done[1 - i])  # step s - 1 has finished with buffer 1 - i
+            to_device(1 - i)
+        stream.wait_event(in_ready[i])
+        if s >= 2:
+            stream.wait_event(out_free[i])  # step s - 2's results have left buffer i
+        with torch.cuda.stream(stream):
+            step(io=dev_io[i])
+        done[i].record(stream)
+        to_host(i)
+    stream.wait_event(out_free[0])
+    stream.wait_event(out_free[1])
     end.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max([start.elapsed_time(end) / e2e_steps], dist, dev)[0]
     layer.check(bufs, stream)
+    for h, d in zip(host_out[(e2e_steps - 1) % 2], outs):  # the last step's results reached the host
+        if not torch.equal(h.to(dev), d):
+            raise RuntimeError("end-to-end results differ from the device-timed step's")
 
     peaks, peak_src = measured_peaks()
     flops = cfg.flops_fwd_bwd()
