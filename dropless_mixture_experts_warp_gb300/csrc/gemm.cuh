@@ -185,13 +185,43 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
   return c;
 }
 
-// Logistic sigmoid through the identity sigmoid(g) = (1 + tanh(g / 2)) / 2 on the
-// hardware tanh approximation: one special-function operation instead of an
-// exponential and a reciprocal (absolute error about 2^-12, below bf16 resolution).
-__device__ __forceinline__ float sigmoidf_(float g) {
+// Two fp32 lanes for the packed Blackwell fp32 pipe (mul/fma .rn.f32x2: each lane
+// rounds as the scalar instruction would).
+struct F2 {
+  float x, y;
+};
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+  F2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float tanh_approx(float x) {
   float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
-  return fmaf(0.5f, t, 0.5f);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+  return t;
+}
+
+// The logistic sigmoid in every SwiGLU epilogue goes through the identity
+// sigmoid(g) = (1 + tanh(g / 2)) / 2 on the hardware tanh approximation: one
+// special-function operation instead of an exponential and a reciprocal (absolute
+// error about 2^-12, below bf16 resolution), computed as fma(0.5, tanh(0.5 g), 0.5).
+// h = w silu(g) u = (w (g sigmoid(g))) u for two neighbouring columns.
+__device__ __forceinline__ F2 swiglu_pair(F2 g, F2 u, F2 w2) {
+  const F2 half{0.5f, 0.5f};
+  const F2 hg = mul2(half, g);
+  const F2 sg = fma2(half, F2{tanh_approx(hg.x), tanh_approx(hg.y)}, half);
+  return mul2(mul2(w2, mul2(g, sg)), u);
 }
 
 // Shared state of the epilogue warps: the hand-off of the dw partials between the
@@ -234,11 +264,16 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
     float a = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
     const int e = mx_scale_exp(a);
-    const float sc = exp2_neg(e);
+    const uint32_t sb = __float_as_uint(exp2_neg(e));
+    const uint64_t ss = (static_cast<uint64_t>(sb) << 32) | sb;
     uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      w[q] = cvt_e4m3x2(cv[4 * q] * sc, cv[4 * q + 1] * sc) | (cvt_e4m3x2(cv[4 * q + 2] * sc, cv[4 * q + 3] * sc) << 16);
+    for (int q = 0; q < 4; ++q) {
+      float x0 = cv[4 * q], x1 = cv[4 * q + 1], x2 = cv[4 * q + 2], x3 = cv[4 * q + 3];
+      mul_f32x2(x0, x1, ss);
+      mul_f32x2(x2, x3, ss);
+      w[q] = cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16);
+    }
     const int col = col0 + 16 * s + cc;
     if (ok) {
       *reinterpret_cast<uint4*>(codes + static_cast<long long>(col) * ld + rblk + hh * 16) =
@@ -362,9 +397,11 @@ __device__ __forceinline__ void fwd_mx_load(uint32_t tbase, int hw, int cb, floa
     tmem_ld32(tbase + hw + cb + 32 * i, u);
     tmem_wait_ld();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-      f.h[i][j] = w * (gv * sigmoidf_(gv)) * uv;
+    for (int j = 0; j < 32; j += 2) {
+      const F2 h = swiglu_pair(F2{__uint_as_float(g[j]), __uint_as_float(g[j + 1])},
+                               F2{__uint_as_float(u[j]), __uint_as_float(u[j + 1])}, F2{w, w});
+      f.h[i][j] = h.x;
+      f.h[i][j + 1] = h.y;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -423,35 +460,8 @@ __device__ __forceinline__ void load_gu_chunk(const GemmParams& p, long long row
   }
 }
 
-// Two fp32 lanes for the packed Blackwell fp32 pipe (mul/fma .rn.f32x2: each lane
-// rounds as the scalar instruction would).
-struct F2 {
-  float x, y;
-};
-__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
-  F2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
-  F2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float tanh_approx(float x) {
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
-  return t;
-}
-
 // SwiGLU' of one 32-column chunk: dH (fp32 accumulator columns) and the saved G, U
-// (bf16) -> dG = w dH U silu'(G), dU = w dH silu(G), with sigmoid as sigmoidf_ and
+// (bf16) -> dG = w dH U silu'(G), dU = w dH silu(G), with sigmoid as in swiglu_pair and
 // silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g))); returns the chunk's share of the
 // row's sum of silu(G) U dH (eight fixed-order partial sums).  Neighbouring columns
 // go through the packed fp32 pipe together.
@@ -594,10 +604,14 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
         for (int v = 0; v < 4; ++v) {
           float hv[8], gv[8], uv[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < 8; i += 2) {
             gv[i] = __uint_as_float(g[8 * v + i]);
+            gv[i + 1] = __uint_as_float(g[8 * v + i + 1]);
             uv[i] = __uint_as_float(u[8 * v + i]);
-            hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
+            uv[i + 1] = __uint_as_float(u[8 * v + i + 1]);
+            const F2 h = swiglu_pair(F2{gv[i], gv[i + 1]}, F2{uv[i], uv[i + 1]}, F2{w, w});
+            hv[i] = h.x;
+            hv[i + 1] = h.y;
           }
           gdst[v] = make_uint4(pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
                                pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
@@ -638,37 +652,22 @@ __device__ __forceinline__ bool tile_epilogue(const GemmParams& p, const TileCoo
     GuChunk nx;
     load_gu_chunk(p, row, row_ok, c.out_col + cb, nx);
     for (int c0 = cb; c0 < cb + BN / NH; c0 += 32) {
-      uint4 g4[4], u4[4];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) { g4[v] = nx.g[v]; u4[v] = nx.u[v]; }
+      const GuChunk cur = nx;
       if (c0 + 32 < cb + BN / NH) load_gu_chunk(p, row, row_ok, c.out_col + c0 + 32, nx);
       uint32_t r[32];
       tmem_ld32(tbase + c0, r);
       tmem_wait_ld();
+      float dg[32], du[32];
+      dwp += swiglu_bwd_values(r, cur, w, dg, du);
       if (row_ok) {
         uint4* gdst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + c.out_col + c0);
         uint4* udst = reinterpret_cast<uint4*>(p.dgu_out + row * ld2 + p.f + c.out_col + c0);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint32_t gw[4] = {g4[v].x, g4[v].y, g4[v].z, g4[v].w};
-          const uint32_t uw[4] = {u4[v].x, u4[v].y, u4[v].z, u4[v].w};
-          float dg[8], du[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-            const float u = (i & 1) ? bf16_hi(uw[i >> 1]) : bf16_lo(uw[i >> 1]);
-            const float dh = __uint_as_float(r[8 * v + i]);
-            const float sg = sigmoidf_(g);
-            const float silu = g * sg;
-            const float da = w * dh;
-            dwp += silu * u * dh;
-            dg[i] = da * u * sg * (1.0f + g * (1.0f - sg));
-            du[i] = da * silu;
-          }
-          gdst[v] = make_uint4(pack_bf16(dg[0], dg[1]), pack_bf16(dg[2], dg[3]),
-                               pack_bf16(dg[4], dg[5]), pack_bf16(dg[6], dg[7]));
-          udst[v] = make_uint4(pack_bf16(du[0], du[1]), pack_bf16(du[2], du[3]),
-                               pack_bf16(du[4], du[5]), pack_bf16(du[6], du[7]));
+          gdst[v] = make_uint4(pack_bf16(dg[8 * v], dg[8 * v + 1]), pack_bf16(dg[8 * v + 2], dg[8 * v + 3]),
+                               pack_bf16(dg[8 * v + 4], dg[8 * v + 5]), pack_bf16(dg[8 * v + 6], dg[8 * v + 7]));
+          udst[v] = make_uint4(pack_bf16(du[8 * v], du[8 * v + 1]), pack_bf16(du[8 * v + 2], du[8 * v + 3]),
+                               pack_bf16(du[8 * v + 4], du[8 * v + 5]), pack_bf16(du[8 * v + 6], du[8 * v + 7]));
         }
       }
     }

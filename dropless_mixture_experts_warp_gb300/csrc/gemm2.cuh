@@ -290,10 +290,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
           tmem_wait_ld();
           float gv[32], uv[32], hv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 32; i += 2) {
             gv[i] = __uint_as_float(g[i]);
+            gv[i + 1] = __uint_as_float(g[i + 1]);
             uv[i] = __uint_as_float(u[i]);
-            hv[i] = w * (gv[i] * sigmoidf_(gv[i])) * uv[i];
+            uv[i + 1] = __uint_as_float(u[i + 1]);
+            const F2 h = swiglu_pair(F2{gv[i], gv[i + 1]}, F2{uv[i], uv[i + 1]}, F2{w, w});
+            hv[i] = h.x;
+            hv[i + 1] = h.y;
           }
           if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the boxes
           __syncwarp();
