@@ -178,6 +178,12 @@ def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu32, w_d32, seconds: flo
     return flops / t_total, done_tok, t_total
 
 
+def oracle_chunk(args) -> int:
+    """Tokens per oracle sample: the MXFP8 oracle quantises every expert a sample touches
+    (both weight orientations), about eight times the bf16 oracle's cost per token."""
+    return max(1, args.ref_tokens if args.prec == "bf16" else args.ref_tokens // 8)
+
+
 def run_reference(args, cfg):
     """--impl reference: the CPU oracle, timed per step on a bounded token sample."""
     import numpy as np
@@ -190,12 +196,13 @@ def run_reference(args, cfg):
     w_gu32 = synth.bf16_to_f32(w_gu_b).reshape(w_gu_b.shape)
     w_d32 = synth.bf16_to_f32(w_d_b).reshape(w_d_b.shape)
     del w_gu_b, w_d_b
-    chunk = max(1, args.ref_tokens)
+    chunk = oracle_chunk(args)
     for _ in range(args.warmup):
-        oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk)
+        oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk, prec=args.prec)
     times, tok = [], 0
     for s in range(args.steps):
-        rate, n, t = oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk, seed=s + 1)
+        rate, n, t = oracle_sample_rate(cfg, inp["x"], inp["logits"], inp["dy"], w_gu32, w_d32, 0.0, chunk,
+                                        seed=s + 1, prec=args.prec)
         times.append(t)
         tok += n
     total = sum(times)
@@ -205,7 +212,7 @@ def run_reference(args, cfg):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_json(cfg, "fp32 oracle"),
+            "config": config_json(cfg, f"{args.prec} (fp32 oracle)"),
             "tokens_per_s": tok / total,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{chunk} random tokens of the {cfg.T}-token batch per step (fp32 NumPy)"},
@@ -487,7 +494,7 @@ def run_native(args, cfg):
         w_gu32 = w_gu.float().cpu().numpy()
         w_d32 = w_d.float().cpu().numpy()
         rate, ntok, secs = oracle_sample_rate(cfg, ex["x"], ex["logits"], ex["dy"], w_gu32, w_d32,
-                                              args.cpu_seconds, args.ref_tokens, prec=args.prec)
+                                              args.cpu_seconds, oracle_chunk(args), prec=args.prec)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{ntok} random tokens of the {cfg.T}-token batch, fp32 NumPy, "
                                           f"{secs:.1f} s"}
