@@ -24,6 +24,8 @@ CASES = {
     "many": synth.small_config("many", T=512, d=128, f=128, E=64, k=8, bias="zipf", bias_param=1.1,
                                forced_empty=3, seed=13),
     # DeepSeek-V3-like: sigmoid scores, Zipf load, forced-empty experts, shared expert
+    # the declared limits: E = 1024 experts, k = 32 (about 16 rows per expert, many empty)
+    "limits": synth.small_config("limits", T=512, d=128, f=64, E=1024, k=32, bias_param=1.0, seed=14),
     "shared": synth.small_config("shared", T=300, d=256, f=128, E=16, k=4, score=synth.SIGMOID,
                                  bias="zipf", bias_param=1.0, forced_empty=2, f_shared=192, seed=14),
 }

@@ -22,6 +22,8 @@ CASES = {
     "mx-ragged": synth.small_config("mx-ragged", T=1000, d=256, f=128, E=8, k=2, bias_param=0.7, seed=41),
     "mx-zipf": synth.small_config("mx-zipf", T=777, d=384, f=256, E=16, k=4, score=synth.SIGMOID, bias="zipf",
                                   bias_param=1.0, forced_empty=2, seed=42),
+    # the declared limits: E = 1024 experts, k = 32
+    "mx-limits": synth.small_config("mx-limits", T=512, d=128, f=128, E=1024, k=32, bias_param=1.0, seed=44),
     # DeepSeek-V3-like with the shared expert (T a multiple of 128 for its row blocks)
     "mx-shared": synth.small_config("mx-shared", T=384, d=256, f=128, E=16, k=4, score=synth.SIGMOID,
                                     bias="zipf", bias_param=1.0, forced_empty=2, f_shared=128, seed=43),
