@@ -30,7 +30,7 @@ baseline (one expert after another), with a library matmul as the only primitive
 The backward is the exact derivative of that forward (checked by finite
 differences in the tests).
 
-Readings where the pages are silent (each restated in the design doc):
+Readings where the pages are silent:
   R1  top-k ranks the raw logits (softmax and sigmoid are strictly increasing),
       ties go to the lower expert index; slot j holds the j-th best expert.
   R2  rows of one expert are ordered by token index (stable counting sort).
