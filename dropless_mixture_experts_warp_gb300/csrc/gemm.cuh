@@ -380,65 +380,53 @@ __device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const u
   }
 }
 
-// Quantising SwiGLU epilogue (EPI_SWIGLU_FWD_MX) with early release.  The warp owns
-// 32 rows and two chunks of 32 h columns (h column cb + 32 i; G at accumulator
-// column cb + 32 i, U at hw + cb + 32 i).  Part 1 reads them, forms h = w silu(G) U
-// in fp32 and rounds G and U to bf16; the caller then releases the accumulator.
-struct FwdMxChunks {
-  float h[2][32];
-  uint32_t g[2][16], u[2][16];  // bf16 pairs
+// Quantising SwiGLU epilogue (EPI_SWIGLU_FWD_MX) pieces, one 32-column chunk of a row
+// at a time (h column col; G and U read from the accumulator): h = w silu(G) U in fp32,
+// G and U rounded to bf16 pairs.
+struct FwdMxChunk {
+  float h[32];
+  uint32_t g[16], u[16];  // bf16 pairs
 };
 
-__device__ __forceinline__ void fwd_mx_load(uint32_t tbase, int hw, int cb, float w, FwdMxChunks& f) {
+__device__ __forceinline__ void fwd_mx_chunk(const uint32_t (&g)[32], const uint32_t (&u)[32], float w,
+                                             FwdMxChunk& f) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t g[32], u[32];
-    tmem_ld32(tbase + cb + 32 * i, g);
-    tmem_ld32(tbase + hw + cb + 32 * i, u);
-    tmem_wait_ld();
+  for (int j = 0; j < 32; j += 2) {
+    const F2 h = swiglu_pair(F2{__uint_as_float(g[j]), __uint_as_float(g[j + 1])},
+                             F2{__uint_as_float(u[j]), __uint_as_float(u[j + 1])}, F2{w, w});
+    f.h[j] = h.x;
+    f.h[j + 1] = h.y;
+  }
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const F2 h = swiglu_pair(F2{__uint_as_float(g[j]), __uint_as_float(g[j + 1])},
-                               F2{__uint_as_float(u[j]), __uint_as_float(u[j + 1])}, F2{w, w});
-      f.h[i][j] = h.x;
-      f.h[i][j + 1] = h.y;
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      f.g[i][j] = pack_bf16(__uint_as_float(g[2 * j]), __uint_as_float(g[2 * j + 1]));
-      f.u[i][j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
-    }
+  for (int j = 0; j < 16; ++j) {
+    f.g[j] = pack_bf16(__uint_as_float(g[2 * j]), __uint_as_float(g[2 * j + 1]));
+    f.u[j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
   }
 }
 
-// Part 2: G|U (bf16, saved for the backward pass), the row-wise codes of h (one
-// 32-column block per chunk) and its column-wise codes (the warp's 32 rows are one
-// 32-row block of every column).
-__device__ __forceinline__ void fwd_mx_store(const GemmParams& p, const TileCoord& c, long long row, bool row_ok,
-                                             int cb, int lane, float* xbuf, const FwdMxChunks& f) {
-  const long long ld2 = 2ll * p.f;
-  const long long rblk = row - lane;
-  const bool blk_ok = __all_sync(0xffffffffu, row_ok);
+// G|U (bf16, saved for the backward pass), the row-wise codes of h (one 32-column
+// block) and its column-wise codes (the warp's 32 rows, first row rblk, are one 32-row
+// block of every column).
+__device__ __forceinline__ void fwd_mx_store_chunk(const GemmParams& p, long long row, bool row_ok, bool blk_ok,
+                                                   long long rblk, int col, int lane, float* xbuf,
+                                                   const FwdMxChunk& f) {
+  if (row_ok) {
+    const long long ld2 = 2ll * p.f;
+    uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + col);
+    uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + col);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int col = c.out_col + cb + 32 * i;
-    if (row_ok) {
-      uint4* gdst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + col);
-      uint4* udst = reinterpret_cast<uint4*>(p.gu_out + row * ld2 + p.f + col);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        gdst[v] = make_uint4(f.g[i][4 * v], f.g[i][4 * v + 1], f.g[i][4 * v + 2], f.g[i][4 * v + 3]);
-        udst[v] = make_uint4(f.u[i][4 * v], f.u[i][4 * v + 1], f.u[i][4 * v + 2], f.u[i][4 * v + 3]);
-      }
-      uint32_t q[8];
-      const uint32_t sb = quant_block32(f.h[i], q);
-      uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * p.f + col);
-      qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
+    for (int v = 0; v < 4; ++v) {
+      gdst[v] = make_uint4(f.g[4 * v], f.g[4 * v + 1], f.g[4 * v + 2], f.g[4 * v + 3]);
+      udst[v] = make_uint4(f.u[4 * v], f.u[4 * v + 1], f.u[4 * v + 2], f.u[4 * v + 3]);
     }
-    quant_cols_chunk32(f.h[i], xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
+    uint32_t q[8];
+    const uint32_t sb = quant_block32(f.h, q);
+    uint4* qd = reinterpret_cast<uint4*>(p.q_rows + row * p.f + col);
+    qd[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
   }
+  quant_cols_chunk32(f.h, xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
 }
 
 // Quantising SwiGLU' epilogue (EPI_SWIGLU_BWD_MX) pieces.  The saved G and U of one

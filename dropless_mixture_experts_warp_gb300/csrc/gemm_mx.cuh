@@ -41,9 +41,9 @@ __host__ __device__ constexpr int mx_smem_bytes(int epi) {
 }
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
-// BN = 256 (four stages): the TMEM columns after the scale factors, 96 per epilogue
-// warp of a lane quarter, hold accumulator columns the SwiGLU' epilogue has yet to
-// process once it has released the accumulator
+// BN = 256 (four stages): the TMEM columns after the scale factors hold accumulator
+// columns the SwiGLU epilogues have yet to process once they have released the
+// accumulator (96 per epilogue warp of a lane quarter for SwiGLU', 64 for SwiGLU)
 constexpr int MX_SPARE_COL = MX_SF_TMEM_COL + 4 * MX_SF_COLS_PER_STAGE;
 
 template <int SCHED, int EPI>
@@ -229,17 +229,47 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         continue;
       }
       if (EPI == EPI_SWIGLU_FWD_MX) {
-        // this warp's quarter of the h columns (BN / 4 = 64): read, release, then store
+        // this warp's quarter of the h columns (BN / 4 = 64, two chunks; BN is 256 here):
+        // the second chunk's G and U go to spare TMEM columns, the first chunk's stay in
+        // registers, the accumulator is released, then the chunks are processed
         const bool row_ok = row < p.row_limit;
         const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
-        const int cb = ((warp - 2) >> 2) * (BN / 4);
-        FwdMxChunks f;
-        fwd_mx_load(tbase, BN / 2, cb, w, f);
+        const int half = (warp - 2) >> 2;
+        const int cb = half * (BN / 4);
+        const uint32_t sp = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + MX_SPARE_COL + half * 64;
+        {
+          uint32_t g1[32], u1[32];
+          tmem_ld32(tbase + cb + 32, g1);
+          tmem_ld32(tbase + BN / 2 + cb + 32, u1);
+          tmem_wait_ld();
+          tmem_st32(sp, g1);
+          tmem_st32(sp + 32, u1);
+        }
+        uint32_t g0[32], u0[32];
+        tmem_ld32(tbase + cb, g0);
+        tmem_ld32(tbase + BN / 2 + cb, u0);
+        tmem_wait_ld();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty_bar[acc]);
         if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
-        fwd_mx_store(p, c, row, row_ok, cb, lane, xbuf, f);
+        const long long rblk = row - lane;
+        const bool blk_ok = __all_sync(0xffffffffu, row_ok);
+        {
+          FwdMxChunk f;
+          fwd_mx_chunk(g0, u0, w, f);
+          fwd_mx_store_chunk(p, row, row_ok, blk_ok, rblk, c.out_col + cb, lane, xbuf, f);
+        }
+        {
+          uint32_t g1[32], u1[32];
+          tmem_ld32(sp, g1);
+          tmem_ld32(sp + 32, u1);
+          tmem_wait_ld();
+          FwdMxChunk f;
+          fwd_mx_chunk(g1, u1, w, f);
+          fwd_mx_store_chunk(p, row, row_ok, blk_ok, rblk, c.out_col + cb + 32, lane, xbuf, f);
+        }
         continue;
       }
       if (EPI == EPI_SWIGLU_BWD_MX && BN == 256) {
