@@ -115,9 +115,13 @@ def measured_peaks():
 # ---------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi samples of this GPU's clocks and throttle reasons every 25 ms; stop()
+    keeps the samples whose timestamps fall inside the timed window [t0, t1] (host
+    wall-clock seconds) and reports their median SM clock and every reason seen."""
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, uuid: str):
         self.uuid = uuid.lower().replace("gpu-", "")
@@ -126,11 +130,11 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                          "-lms", "25"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -139,16 +143,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
-        mine = [r for r in rows if self.uuid and self.uuid in r[0].lower()] or rows
-        if not mine:
+        return self.summarise(out, self.uuid, t0, t1)
+
+    @classmethod
+    def summarise(cls, out: str, uuid: str, t0=None, t1=None):
+        import datetime
+        rows = [[f.strip() for f in r.split(",")] for r in out.strip().splitlines() if r.count(",") >= 8]
+        mine = [r for r in rows if uuid and uuid in r[1].lower()] or rows
+
+        def when(r):
+            try:
+                return datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in mine if t0 is not None and when(r) is not None and t0 <= when(r) <= t1]
+        use = inside or mine
+        if not use:
             return None
-        sm = [float(r[1]) for r in mine if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in mine if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in mine for i in range(4) if r[4 + i].strip() == "Active"})
+        num = lambda v: float(v) if v.replace(".", "", 1).isdigit() else None  # noqa: E731
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        smax = [num(r[3]) for r in use if num(r[3]) is not None]
+        power = [num(r[4]) for r in use if num(r[4]) is not None]
+        reasons = sorted({cls.REASONS[i] for r in use for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(mine)}
+                "reasons": reasons, "samples": len(use), "in_timed_window": bool(inside),
+                "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
@@ -377,12 +396,14 @@ def run_native(args, cfg):
     launches0 = B.moe_launch_count()
     sampler.start()
     time.sleep(0.3)
+    t0 = time.time()
     start.record(stream)
     for s in range(args.steps):
         step(evs[s])
     end.record(stream)
     torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
     launches = B.moe_launch_count() - launches0
     if dist:
         dist.barrier()
