@@ -117,7 +117,8 @@ def measured_peaks():
 class ClockSampler:
     """nvidia-smi samples of this GPU's clocks and throttle reasons every 25 ms; stop()
     keeps the samples whose timestamps fall inside the timed window [t0, t1] (host
-    wall-clock seconds) and reports their median SM clock and every reason seen."""
+    wall-clock seconds) and reports their median SM clock and every reason seen (the
+    power column, an average over a longer window, is not reported)."""
     FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -163,11 +164,9 @@ class ClockSampler:
         num = lambda v: float(v) if v.replace(".", "", 1).isdigit() else None  # noqa: E731
         sm = [num(r[2]) for r in use if num(r[2]) is not None]
         smax = [num(r[3]) for r in use if num(r[3]) is not None]
-        power = [num(r[4]) for r in use if num(r[4]) is not None]
         reasons = sorted({cls.REASONS[i] for r in use for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(use), "in_timed_window": bool(inside),
-                "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(use), "in_timed_window": bool(inside)}
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
