@@ -28,8 +28,7 @@ int num_sms() {
 
 int pair_grid(const void* kern, int threads, int smem_bytes) {
   const int all = num_sms() & ~1;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(all), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
