@@ -281,13 +281,22 @@ __device__ __forceinline__ void mul_f32x2(float& a, float& b, uint64_t ss) {
       : "l"(ss));
 }
 
+// max(|a|, |b|, |c|) in one three-input instruction.
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Quantise 32 fp32 values (one block) into 8 words of codes; returns the scale byte.
 __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&codes)[8]) {
-  float m[8];  // a tree of maxima: short dependency chains
+  float m[11];  // a tree of three-input maxima: 11 + 4 + 2 instructions
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    m[j] = fmaxf(fmaxf(fabsf(v[4 * j]), fabsf(v[4 * j + 1])), fmaxf(fabsf(v[4 * j + 2]), fabsf(v[4 * j + 3])));
-  const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int j = 0; j < 10; ++j) m[j] = absmax3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+  m[10] = absmax3(v[30], v[31], v[31]);
+  const float n0 = absmax3(m[0], m[1], m[2]), n1 = absmax3(m[3], m[4], m[5]);
+  const float n2 = absmax3(m[6], m[7], m[8]), n3 = absmax3(m[9], m[10], m[10]);
+  const float amax = absmax3(absmax3(n0, n1, n2), n3, n3);
   const int e = mx_scale_exp(amax);
   const uint32_t sb = __float_as_uint(exp2_neg(e));
   const uint64_t ss = (static_cast<uint64_t>(sb) << 32) | sb;

@@ -255,13 +255,13 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
 #pragma unroll
     for (int j = 0; j < 16; ++j) xb[lane * 17 + j] = v[16 * s + j];
     __syncwarp();
-    float cv[16], m[4];
+    float cv[16], m[6];
 #pragma unroll
     for (int i = 0; i < 16; ++i) cv[i] = xb[(hh * 16 + i) * 17 + cc];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      m[j] = fmaxf(fmaxf(fabsf(cv[4 * j]), fabsf(cv[4 * j + 1])), fmaxf(fabsf(cv[4 * j + 2]), fabsf(cv[4 * j + 3])));
-    float a = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    for (int j = 0; j < 5; ++j) m[j] = absmax3(cv[3 * j], cv[3 * j + 1], cv[3 * j + 2]);
+    m[5] = absmax3(cv[15], cv[15], cv[15]);
+    float a = absmax3(absmax3(m[0], m[1], m[2]), m[3], absmax3(m[4], m[5], m[5]));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
     const int e = mx_scale_exp(a);
     const uint32_t sb = __float_as_uint(exp2_neg(e));
