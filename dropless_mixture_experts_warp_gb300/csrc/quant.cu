@@ -101,11 +101,20 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   const long long total = static_cast<long long>(batch) * rtiles * ctiles;
   const long long k_tiles = rows / 128;
 
+  // the source rows of this thread's eight rows of tile t (-1: a zero row); with a row
+  // map these are global loads, issued one tile ahead of the copies that use them
+  auto rows_of = [&](long long t, int (&sr)[8]) {
+    const long long rti = t < total ? (t / ctiles) % rtiles : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const long long r = rti * 128 + (threadIdx.x >> 4) + 16 * j;
+      sr[j] = (t >= total || r >= rows) ? -1 : (row_map ? row_map[r] : static_cast<int>(r));
+    }
+  };
   // issue the loads of tile t into input buffer `buf`
-  auto fetch = [&](long long t, int buf) {
+  auto fetch = [&](long long t, int buf, const int (&sr)[8]) {
     if (t < total) {
       const int cti = static_cast<int>(t % ctiles);
-      const long long rti = (t / ctiles) % rtiles;
       const long long b = t / (static_cast<long long>(ctiles) * rtiles);
       const uint16_t* s = src + (row_map ? 0 : b * rows * C);
       uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
@@ -113,21 +122,23 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
       for (int j = 0; j < 8; ++j) {  // 16 x 16 bytes per 128-column row, 8 per thread
         const int i = threadIdx.x + 256 * j;
         const int rr = i >> 4, q = i & 15;
-        long long sr = rti * 128 + rr;
-        if (sr >= rows) sr = -1;
-        else if (row_map) sr = row_map[sr];
-        const bool ok = sr >= 0;
-        cp_async16(&tile[rr][q * 8], s + (ok ? sr * C + cti * 128 + q * 8 : 0), ok);
+        const bool ok = sr[j] >= 0;
+        cp_async16(&tile[rr][q * 8], s + (ok ? static_cast<long long>(sr[j]) * C + cti * 128 + q * 8 : 0), ok);
       }
     }
     cp_async_commit();  // possibly empty: keeps one group per tile
   };
 
+  const long long gs = gridDim.x;
   long long t = blockIdx.x;
-  fetch(t, 0);
-  for (int it = 0; t < total; ++it, t += gridDim.x) {
+  int sr_next[8];
+  rows_of(t, sr_next);
+  fetch(t, 0, sr_next);
+  rows_of(t + gs, sr_next);
+  for (int it = 0; t < total; ++it, t += gs) {
     const int buf = it & 1;
-    fetch(t + gridDim.x, buf ^ 1);
+    fetch(t + gs, buf ^ 1, sr_next);
+    rows_of(t + 2 * gs, sr_next);  // in flight while this tile is quantised
     cp_async_wait_prev();  // this tile's group has landed
     __syncthreads();
     const uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<const uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
