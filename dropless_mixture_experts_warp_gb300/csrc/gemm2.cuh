@@ -20,7 +20,7 @@
 
 namespace moe {
 
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = 6;  // at most; pair_stages(epi) per epilogue
 constexpr int P_A_BYTES = BM * BK * 2;                // 16 KB
 constexpr int P_B_BYTES_MAX = 128 * BK * 2;           // half of a 256-row B tile
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
@@ -31,9 +31,13 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
 // write through staging boxes and tensor stores.
 __host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
 __host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
-// staging per epilogue warp: STORE and SwiGLU' 2 KB; SwiGLU 6 KB (its G, U and h boxes)
+// Operand stages: six, five for SwiGLU' (whose warps also hold a G/U box).
+__host__ __device__ constexpr int pair_stages(int epi) { return epi == 2 ? 5 : P_STAGES; }
+// per epilogue warp: STORE 2 KB (staging box); SwiGLU 6 KB (its G, U and h boxes);
+// SwiGLU' 6 KB (a dG/dU staging box and the 4 KB box of the saved G and U)
+__host__ __device__ constexpr int pair_epi_bytes(int epi) { return epi == 0 ? 2048 : 6144; }
 __host__ __device__ constexpr int p_smem_bytes(int epi) {
-  return P_STAGES * P_STAGE_BYTES + pair_epi_warps(epi) * (epi == 1 ? 6144 : 2048) + 1024;
+  return pair_stages(epi) * P_STAGE_BYTES + pair_epi_warps(epi) * pair_epi_bytes(epi) + 1024;
 }
 
 struct PairTile {
@@ -108,11 +112,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t dw_full_bar[4];
   __shared__ __align__(8) uint64_t dw_empty_bar[4];
+  __shared__ __align__(8) uint64_t gu_bar[EPI == EPI_SWIGLU_BWD ? 8 : 1];  // per epilogue warp
   __shared__ float s_dw[BM];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
   __shared__ int s_pt[MAX_EXPERTS + 1];
+  constexpr int STAGES = pair_stages(EPI);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -143,7 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       }
       s_pt[E] = run;
     }
-    for (int s = 0; s < P_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    if (EPI == EPI_SWIGLU_BWD)
+      for (int w = 0; w < 8; ++w) mbar_init(&gu_bar[w], 1);
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], 2 * pair_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
@@ -154,7 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (EPI == EPI_SWIGLU_FWD) tma_prefetch_desc(&tmD);
+    if (EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) { tmem_alloc_pair(&s_tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
   tc_fence_before();
@@ -199,11 +207,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             for (int i = 0; i < BN / 128; ++i)
               tma_load_2d_pair(sb + i * 8192, &tmB, bar, c.b_n + 64 * i, c.b_k + k0);
           }
-          if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
       if (rank == 0)
-        for (int s = 0; s < P_STAGES; ++s)
+        for (int s = 0; s < STAGES; ++s)
           if ((armed >> s) & 1u) mbar_drain(&full_bar[s], (armed_parity >> s) & 1u, WAIT_LIMIT_CYCLES);
     }
     __syncwarp();
@@ -235,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
-          if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         tc_commit_pair_mc(&tfull_bar[acc], 0x3);      // both halves of the accumulator ready
@@ -252,7 +260,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
-    uint8_t* stg = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * (EPI == EPI_SWIGLU_FWD ? 6144 : 2048);
+    uint8_t* stg = smem + STAGES * P_STAGE_BYTES + (warp - 2) * pair_epi_bytes(EPI);
+    uint32_t gu_phase = 0;
+    bool gu_inflight = false;  // a G/U box load not yet waited for
     for (int rnd = 0, tile = sched_tile(0, pair, npairs, snake); tile < total;
          tile = sched_tile(++rnd, pair, npairs, snake)) {
       const PairTile t = pair_tile<SCHED, EPI, B_MN>(p, s_ro, s_pt, E, n_tiles, tile, rank);
@@ -315,19 +325,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
         }
       } else if (EPI == EPI_SWIGLU_BWD) {
         // dG then dU (tmC, a map of dG|dU) through the warp's 2 KB staging box and tensor
-        // stores; this warp takes half of the tile's h columns
+        // stores; the saved G and U of each 32-column chunk arrive one chunk ahead by
+        // tensor loads (tmD, a map of G|U) in the warp's 4 KB G/U box, which keeps the
+        // row-by-row reads off the L1 path; this warp takes half of the tile's h columns
         const bool row_ok = row < t.row_end;
         const float w = !row_ok ? 0.0f : (p.w_rows ? p.w_rows[row] : 1.0f);
         const bool blk_ok = t.c.out_row + q * 32 < t.row_end;
         const int y0 = static_cast<int>(t.c.out_row + q * 32);
         const int half = (warp - 2) >> 2;
         const int cb = half * (BN / 2);
+        uint64_t* gbar = &gu_bar[warp - 2];
+        uint8_t* gub = stg + 2048;
+        const uint32_t grow = smem_u32(gub) + lane * 64;  // this lane's row of the G box
+        const int sw = (lane >> 1) & 3;                     // 64-byte swizzle of the box
+        if (lane == 0) {
+          mbar_arrive_expect_tx(gbar, 4096);
+          tma_load_2d(gub, &tmD, gbar, t.c.out_col + cb, y0);
+          tma_load_2d(gub + 2048, &tmD, gbar, p.f + t.c.out_col + cb, y0);
+        }
+        gu_inflight = true;
         float dwp = 0.0f;
-        GuChunk nx;  // the saved G and U of the next chunk are fetched during this one
-        load_gu_chunk(p, row, row_ok, t.c.out_col + cb, nx);
+        bool ok = true;
         for (int c0 = cb; c0 < cb + BN / 2; c0 += 32) {
-          const GuChunk cur = nx;
-          if (c0 + 32 < cb + BN / 2) load_gu_chunk(p, row, row_ok, t.c.out_col + c0 + 32, nx);
+          if (!mbar_wait_bounded(gbar, gu_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) { ok = false; break; }
+          gu_phase ^= 1u;
+          gu_inflight = false;
+          GuChunk cur;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            cur.g[v] = ld_shared_v4(grow + ((v ^ sw) << 4));
+            cur.u[v] = ld_shared_v4(grow + 2048 + ((v ^ sw) << 4));
+          }
+          __syncwarp();  // every lane has its rows: the box may be refilled
+          if (c0 + 32 < cb + BN / 2) {
+            if (lane == 0) {
+              fence_proxy_async_smem();
+              mbar_arrive_expect_tx(gbar, 4096);
+              tma_load_2d(gub, &tmD, gbar, t.c.out_col + c0 + 32, y0);
+              tma_load_2d(gub + 2048, &tmD, gbar, p.f + t.c.out_col + c0 + 32, y0);
+            }
+            gu_inflight = true;
+          }
           uint32_t r[32];
           tmem_ld32(tbase + c0, r);
           tmem_wait_ld();
@@ -346,6 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             }
           }
         }
+        if (!ok) break;
         if (!dw_combine<2>(p, t.c, row, row_ok, half, q, row_in_tile, hand, dwp)) break;
       } else if (!tile_epilogue<EPI, pair_epi_warps(EPI) / 4>(p, t.c, tbase, row, row < t.row_end, BN,
                                                               (warp - 2) >> 2, q, row_in_tile, hand)) {
@@ -356,6 +395,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    if (EPI == EPI_SWIGLU_BWD && gu_inflight)  // a G/U load left by an aborted tile lands first
+      mbar_drain(&gu_bar[warp - 2], gu_phase, WAIT_LIMIT_CYCLES);
     if (lane == 0) bulk_wait_all();  // tensor stores complete
   }
 

@@ -13,9 +13,12 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
     if (!make_tensor_map_store(&c, p.gu_out, 2ull * p.f, 2ull * p.f, rows) ||
         !make_tensor_map_store(&dd, p.h_out, static_cast<uint64_t>(p.f), static_cast<uint64_t>(p.f), rows))
       return cudaErrorInvalidValue;
-  } else if (kind == GEMM_ROWS_SWIGLU_BWD) {  // a map of dG|dU [rows][2f]
-    if (!p.dgu_out || (reinterpret_cast<uintptr_t>(p.dgu_out) & 15u) || p.f % 8 != 0) return cudaErrorInvalidValue;
-    if (!make_tensor_map_store(&c, p.dgu_out, 2ull * p.f, 2ull * p.f, static_cast<uint64_t>(p.row_limit)))
+  } else if (kind == GEMM_ROWS_SWIGLU_BWD) {  // maps of dG|dU and of the saved G|U, both [rows][2f]
+    const uintptr_t al = reinterpret_cast<uintptr_t>(p.dgu_out) | reinterpret_cast<uintptr_t>(p.gu_in);
+    if (!p.dgu_out || !p.gu_in || (al & 15u) || p.f % 32 != 0) return cudaErrorInvalidValue;
+    const uint64_t rows = static_cast<uint64_t>(p.row_limit);
+    if (!make_tensor_map_store(&c, p.dgu_out, 2ull * p.f, 2ull * p.f, rows) ||
+        !make_tensor_map_store(&dd, p.gu_in, 2ull * p.f, 2ull * p.f, rows))
       return cudaErrorInvalidValue;
   } else {  // STORE: a map of the output
     if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;

@@ -79,8 +79,9 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
 // one per two SMs.
 int pair_grid(const void* kern, int threads, int smem_bytes);
 
-// c: tensor map of the bf16 output for the STORE epilogue, of G|U for the SwiGLU one;
-// dd: of h for the SwiGLU epilogue (unused otherwise)
+// c: tensor map of the bf16 output for the STORE epilogue, of G|U for the SwiGLU one,
+// of dG|dU for the SwiGLU' one; dd: of h for the SwiGLU epilogue, of the saved G|U
+// (read) for the SwiGLU' one (unused otherwise)
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                                const CUtensorMap& dd, const GemmParams& p, cudaStream_t stream) {
