@@ -31,6 +31,11 @@ cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmPa
       !make_tensor_map_u8(&tb, b.codes, b.inner, b.outer, 128, b_box))
     return cudaErrorInvalidValue;
   tc = ta;
+  if (kind == GEMM_ROWS_SWIGLU_BWD_MXQ && p.BN == 256) {  // the SwiGLU' epilogue reads G|U by tensor loads
+    if (!p.gu_in || (reinterpret_cast<uintptr_t>(p.gu_in) & 15u) || p.f % 32 != 0) return cudaErrorInvalidValue;
+    if (!make_tensor_map_store(&tc, p.gu_in, 2ull * p.f, 2ull * p.f, static_cast<uint64_t>(p.row_limit)))
+      return cudaErrorInvalidValue;
+  }
   if (store) {  // the STORE epilogue writes through a tensor map of the output
     if (!p.out || p.ldo % 8 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u)) return cudaErrorInvalidValue;
     const uint64_t rows = kgroup ? static_cast<uint64_t>(p.E) * p.M : static_cast<uint64_t>(p.row_limit);

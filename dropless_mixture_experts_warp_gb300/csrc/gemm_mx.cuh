@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
   __shared__ int s_order[SCHED == SCHED_KGROUP ? MAX_EXPERTS : 1];
+  __shared__ __align__(8) uint64_t gu_bar[EPI == EPI_SWIGLU_BWD_MX ? 8 : 1];  // per epilogue warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -82,6 +83,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < MX_MAX_STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    if (EPI == EPI_SWIGLU_BWD_MX)
+      for (int w = 0; w < 8; ++w) mbar_init(&gu_bar[w], 1);
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], mx_epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
     for (int q = 0; q < 4; ++q) { mbar_init(&dw_full_bar[q], 1); mbar_init(&dw_empty_bar[q], 1); }
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_STORE) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD_MX) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) { tmem_alloc(&s_tmem_base, TMEM_COLS); tmem_relinquish(); }
   tc_fence_before();
@@ -102,7 +105,10 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   const int BN = p.BN;                       // 128 or 256
   const int num_acc = BN <= 128 ? 2 : 1;
   const int stage_bytes = MX_A_BYTES + BN * MX_BK;
-  const int stages = MX_CODE_BYTES / stage_bytes;  // 4 or 6
+  // 4 or 6 operand stages; the SwiGLU' GEMM at BN = 256 keeps 3 and holds its warps'
+  // G/U boxes in the fourth stage's memory
+  const bool gu_boxes = EPI == EPI_SWIGLU_BWD_MX && BN == 256;
+  const int stages = gu_boxes ? 3 : MX_CODE_BYTES / stage_bytes;
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
@@ -207,6 +213,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
     float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
     uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 2048;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
+    uint32_t gu_phase = 0;
+    bool gu_inflight = false;  // a G/U box load not yet waited for
     for (int rnd = 0, tile = sched_tile(0, blockIdx.x, gridDim.x, snake); tile < total;
          tile = sched_tile(++rnd, blockIdx.x, gridDim.x, snake)) {
       const TileCoord c = tile_coord<SCHED, EPI, false, MX_BK>(p, s_ro, s_order, E, n_tiles, tile);
@@ -274,7 +282,10 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
       }
       if (EPI == EPI_SWIGLU_BWD_MX && BN == 256) {
         // this warp's 128 dH columns: three chunks go to spare TMEM columns, one stays in
-        // registers, the accumulator is released, then the chunks are processed
+        // registers, the accumulator is released, then the chunks are processed; the
+        // saved G and U of each chunk arrive one chunk ahead by tensor loads (tmC, a map
+        // of G|U) in the warp's 4 KB G/U box, which keeps the row-by-row reads off the
+        // L1 path
         const int half = (warp - 2) >> 2;
         const int cb = half * 128;
         const bool row_ok = row < p.row_limit;
@@ -282,8 +293,33 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         const long long rblk = row - lane;
         const bool blk_ok = __all_sync(0xffffffffu, row_ok);
         const uint32_t spare = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + MX_SPARE_COL + half * 96;
-        GuChunk nx;
-        load_gu_chunk(p, row, row_ok, c.out_col + cb + 96, nx);
+        uint64_t* gbar = &gu_bar[warp - 2];
+        uint8_t* gub = smem + 3 * stage_bytes + (warp - 2) * 4096;
+        const uint32_t grow = smem_u32(gub) + lane * 64;  // this lane's row of the G box
+        const int sw = (lane >> 1) & 3;                     // 64-byte swizzle of the box
+        const int y0 = static_cast<int>(c.out_row + q * 32);
+        auto gu_issue = [&](int col) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(gbar, 4096);
+            tma_load_2d(gub, &tmC, gbar, col, y0);
+            tma_load_2d(gub + 2048, &tmC, gbar, p.f + col, y0);
+          }
+          gu_inflight = true;
+        };
+        auto gu_take = [&](GuChunk& x) -> bool {
+          if (!mbar_wait_bounded(gbar, gu_phase, abort_flag, p.status, WAIT_LIMIT_CYCLES)) return false;
+          gu_phase ^= 1u;
+          gu_inflight = false;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            x.g[v] = ld_shared_v4(grow + ((v ^ sw) << 4));
+            x.u[v] = ld_shared_v4(grow + 2048 + ((v ^ sw) << 4));
+          }
+          __syncwarp();  // every lane has its rows: the box may be refilled
+          return true;
+        };
+        gu_issue(c.out_col + cb + 96);  // the kept chunk's G and U, processed first
         uint32_t keep[32];
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
@@ -300,20 +336,26 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         if (lane == 0) mbar_arrive(&tempty_bar[acc]);
         if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
         float dwp = 0.0f;
+        bool ok;
         {
-          const GuChunk cur = nx;
-          load_gu_chunk(p, row, row_ok, c.out_col + cb, nx);
-          bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + cb + 96, keep, cur, dwp, xbuf, lane, rblk);
+          GuChunk cur;
+          ok = gu_take(cur);
+          if (ok) {
+            gu_issue(c.out_col + cb);
+            bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + cb + 96, keep, cur, dwp, xbuf, lane, rblk);
+          }
         }
 #pragma unroll 1
-        for (int i = 0; i < 3; ++i) {
-          const GuChunk cur = nx;
-          if (i < 2) load_gu_chunk(p, row, row_ok, c.out_col + cb + 32 * (i + 1), nx);
+        for (int i = 0; ok && i < 3; ++i) {
+          GuChunk cur;
+          if (!gu_take(cur)) { ok = false; break; }
+          if (i < 2) gu_issue(c.out_col + cb + 32 * (i + 1));
           uint32_t r[32];
           tmem_ld32(spare + 32 * i, r);
           tmem_wait_ld();
           bwd_mx_chunk(p, row, row_ok, blk_ok, w, c.out_col + cb + 32 * i, r, cur, dwp, xbuf, lane, rblk);
         }
+        if (!ok) break;
         if (!dw_combine<2>(p, c, row, row_ok, half, q, row_in_tile, hand, dwp)) break;
         continue;
       }
@@ -324,6 +366,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
       if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
     }
+    if (EPI == EPI_SWIGLU_BWD_MX && gu_inflight)  // a G/U load left by an aborted tile lands first
+      mbar_drain(&gu_bar[warp - 2], gu_phase, WAIT_LIMIT_CYCLES);
     if (EPI == EPI_STORE && lane == 0) bulk_wait_all();  // the tensor stores are complete
   }
 
