@@ -283,45 +283,6 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
   }
 }
 
-// STORE epilogue through shared memory and the tensor store: the warp owns 32 rows
-// of the tile (output rows y0 .. y0 + 31).  Each 32-column chunk is read from TMEM,
-// rounded to bf16 and written by row into one of the warp's two 2 KB buffers
-// (64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3), which
-// keeps the writes free of bank conflicts); one lane then stores the 32 x 32 box.
-// The accumulator columns are free once read: the stores drain while the next tile
-// accumulates.  `stg` is 1024-byte aligned; `nstore` counts the warp's stores.
-__device__ __forceinline__ void store_tile_tma(const CUtensorMap* tmC, const TileCoord& c, uint32_t tbase, int BN,
-                                               int lane, int y0, uint8_t* stg, uint32_t& nstore) {
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t r[32];
-    if (c.kblocks > 0) {
-      tmem_ld32(tbase + c0, r);
-      tmem_wait_ld();
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = 0u;
-    }
-    uint8_t* buf = stg + (nstore & 1u) * 2048;
-    if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two chunks ago has read it
-    __syncwarp();
-    const uint32_t row_addr = smem_u32(buf) + lane * 64;
-    const int sw = (lane >> 1) & 3;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      st_shared_v4(row_addr + ((j ^ sw) << 4), pack_bf16(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
-                   pack_bf16(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                   pack_bf16(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                   pack_bf16(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tmC, buf, c.out_col + c0, y0);
-      bulk_commit();
-    }
-    ++nstore;
-  }
-}
-
 // STORE epilogue with early release.  Part 1: the warp's nc (<= 4) chunks of 32
 // accumulator columns from col0 into registers (zeros for a tile without K blocks);
 // the caller then hands the accumulator back to the MMA warp.
@@ -352,7 +313,8 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int lane, const flo
 }
 
 // Part 2: the chunks (columns x0 .. x0 + 32 nc of output rows y0 .. y0 + 31) leave as
-// bf16 through the warp's 2 KB staging buffer (64-byte swizzle, as store_tile_tma)
+// bf16 through the warp's 2 KB staging buffer (64-byte swizzle: 16-byte chunk j of row r
+// at chunk j ^ ((r >> 1) & 3), free of bank conflicts)
 // and one tensor store each, while the next tile accumulates.
 __device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const uint32_t (&r)[4][32], int nc, int x0,
                                                  int y0, int lane, uint8_t* stg) {
