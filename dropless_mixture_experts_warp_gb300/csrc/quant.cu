@@ -172,9 +172,11 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
       sft[sf_byte_offset(2 * cp + 1, g * 32, 1)] = static_cast<uint8_t>(sb);
     }
     if (codes_rows) {
-      // row-wise codes of the same tile: thread t takes row t/2, 64 columns (16-byte loads)
-      const int rr = threadIdx.x >> 1;
-      const int cc = (threadIdx.x & 1) * 64;
+      // row-wise codes of the same tile: thread t takes row t % 128, columns 64 (t / 128)
+      // onwards (16-byte loads; the eight lanes of a load phase read eight consecutive
+      // rows, which the padded row pitch puts on distinct banks)
+      const int rr = threadIdx.x & 127;
+      const int cc = (threadIdx.x >> 7) * 64;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         float v[32];
