@@ -1,4 +1,5 @@
-"""MXFP8 (E4M3 elements, one E8M0 scale per 32 consecutive elements) for the oracle.
+"""MXFP8 (E4M3 elements, one E8M0 scale per 32 consecutive elements) for the oracle,
+and FP4 weights (E2M1 elements, same scales) for FP8 x FP4 experts (end of the file).
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
@@ -141,14 +142,17 @@ def mx_matmul(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:
 # ----------------------------------------------------------------------------------
 
 def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=None,
-                   dtype=np.float64, matmul=mx_matmul, grouped=None):
+                   dtype=np.float64, matmul=mx_matmul, grouped=None, wmatmul=None):
     """Forward of the layer with every GEMM operand quantised along its contraction axis.
 
     Same steps as moe_oracle.moe_forward; the two GEMMs of each expert become
     G|U = mx(X_e, W_gu[e]) (both along d) and Y = mx(H_e, W_d[e]) (both along f).
     ``matmul`` is the GEMM used (identity quantisation gives back the plain forward);
-    ``grouped`` selects the group-limited router as in moe_oracle.moe_forward.
+    ``wmatmul`` (default: ``matmul``) is the one for these products, whose second
+    operand is a weight (mx_matmul_w4 for FP8 x FP4 experts); ``grouped`` selects the
+    group-limited router as in moe_oracle.moe_forward.
     """
+    wmatmul = matmul if wmatmul is None else wmatmul
     from . import moe_oracle as om
     x = np.asarray(x, dtype)
     T, d = x.shape
@@ -168,10 +172,10 @@ def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=
             continue
         wg = np.asarray(w_gu[e], dtype)
         wd = np.asarray(w_d[e], dtype)
-        gu = matmul(x[t_sel], wg, dtype)
+        gu = wmatmul(x[t_sel], wg, dtype)
         g, u = gu[:, :f], gu[:, f:]
         h = w[t_sel, j_sel][:, None] * (g * om._sigmoid(g) * u)
-        y_slot[t_sel, j_sel] = matmul(h, wd, dtype)
+        y_slot[t_sel, j_sel] = wmatmul(h, wd, dtype)
         g_slot[t_sel, j_sel] = g
         u_slot[t_sel, j_sel] = u
     y = np.zeros((T, d), dtype)
@@ -180,24 +184,25 @@ def moe_forward_mx(x, logits, w_gu, w_d, k, score="softmax", w_gu_s=None, w_d_s=
     out = {"Y": y, "idx": idx, "w": w, "g": g_slot, "u": u_slot}
     if w_gu_s is not None:
         fs = w_d_s.shape[1]
-        gu = matmul(x, np.asarray(w_gu_s, dtype), dtype)
+        gu = wmatmul(x, np.asarray(w_gu_s, dtype), dtype)
         g, u = gu[:, :fs], gu[:, fs:]
-        out["Y"] = y + matmul(g * om._sigmoid(g) * u, np.asarray(w_d_s, dtype), dtype)
+        out["Y"] = y + wmatmul(g * om._sigmoid(g) * u, np.asarray(w_d_s, dtype), dtype)
         out["g_s"], out["u_s"] = g, u
     return out
 
 
 def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=None, w_d_s=None,
-                    dtype=np.float64, matmul=mx_matmul, grouped=None):
+                    dtype=np.float64, matmul=mx_matmul, grouped=None, wmatmul=None):
     """Backward with MXFP8 GEMM operands (quantisation treated as identity in the chain rule).
 
     Per expert e, rows in token order (its segment):
-      dH = mx(dY_e, W_d[e]^T)         both along d
-      dX_e = mx(dGU_e, W_gu[e]^T)     both along 2f
+      dH = mx(dY_e, W_d[e]^T)         both along d           (wmatmul: weight operand)
+      dX_e = mx(dGU_e, W_gu[e]^T)     both along 2f          (wmatmul: weight operand)
       dW_d[e] = mx(dY_e^T, H_e^T)     both along the rows of e
       dW_gu[e] = mx(dGU_e^T, X_e^T)   both along the rows of e
     The SwiGLU' step, dw and the router gradient are as in moe_oracle.moe_backward.
     """
+    wmatmul = matmul if wmatmul is None else wmatmul
     from . import moe_oracle as om
     x = np.asarray(x, dtype)
     dy = np.asarray(dy, dtype)
@@ -221,11 +226,11 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
         a = g * sg * u
         we = w[t_sel, j_sel][:, None]
         dye = dy[t_sel]
-        dh = matmul(dye, wd.T, dtype)
+        dh = wmatmul(dye, wd.T, dtype)
         dw[t_sel, j_sel] = (a * dh).sum(axis=1)
         da = we * dh
         dgu = np.concatenate([da * u * sg * (1.0 + g * (1.0 - sg)), da * g * sg], axis=1)
-        dx_slot[t_sel, j_sel] = matmul(dgu, wg.T, dtype)
+        dx_slot[t_sel, j_sel] = wmatmul(dgu, wg.T, dtype)
         dw_d[e] = matmul(dye.T, (we * a).T, dtype)
         dw_gu[e] = matmul(dgu.T, x[t_sel].T, dtype)
     dx = np.zeros((T, d), dtype)
@@ -240,9 +245,9 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
         wd = np.asarray(w_d_s, dtype)
         g, u = fwd["g_s"], fwd["u_s"]
         sg = om._sigmoid(g)
-        dh = matmul(dy, wd.T, dtype)
+        dh = wmatmul(dy, wd.T, dtype)
         dgu = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg], axis=1)
-        out["dX"] = dx + matmul(dgu, wg.T, dtype)
+        out["dX"] = dx + wmatmul(dgu, wg.T, dtype)
         out["dW_d_s"] = matmul(dy.T, (g * sg * u).T, dtype)
         out["dW_gu_s"] = matmul(dgu.T, x.T, dtype)
     return out
@@ -291,3 +296,90 @@ def expert_wgrad_sampled_mx(x, logits, dy, w_gu_e, w_d_e, e, k, gu_rows, d_cols,
     sel = np.where((gu_rows < f)[None, :], dg, du)
     dw_gu_rows = qdq(sel.T) @ qdq(xe.T).T
     return {"dW_gu_rows": dw_gu_rows.astype(dtype), "dW_d_cols": dw_d_cols.astype(dtype)}
+
+
+# ----------------------------------------------------------------------------------
+# FP4 weights for FP8 x FP4 expert GEMMs (E2M1 elements, one E8M0 scale per 32)
+# ----------------------------------------------------------------------------------
+# The DeepGEMM Mega MoE page (itsolotime.com, Thai; section "ทิศทางการปรับปรุงใน
+# ระดับลึกยิ่งขึ้น") names FP8 x FP4 mixed-precision computation as a direction and
+# gives no recipe.  Readings taken here:
+#   * the weights (the operand shared by every token of an expert) are E2M1: a sign,
+#     two exponent bits with bias 1 and one mantissa bit, magnitudes 0, 0.5, 1, 1.5,
+#     2, 3, 4, 6, no infinities or NaN; a code is the 4-bit pattern sign<<3 | exp<<1 |
+#     mantissa, held in a uint8 here;
+#   * one E8M0 scale per 32 consecutive elements along the contraction axis, the
+#     MXFP8 block, with the same rule: 2^(floor(log2(amax)) - 2), 2 being E2M1's
+#     largest exponent, clamped to [-127, 127]; an all-zero block gets byte 0;
+#   * elements round to the nearest value, ties to the even code, saturating at +-6;
+#   * activations and gradients stay MXFP8, so the products with a weight operand
+#     (gate/up and down forward, their input gradients) are FP8 x FP4 and the weight
+#     gradients (activation x gradient) stay FP8 x FP8.
+
+E2M1_MAX = 6.0
+EMAX_E2M1 = 2
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])   # codes 0..7
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    mag = E2M1_VALUES[codes & 7]
+    return np.where(codes & 8, -mag, mag)
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value (ties to the even code, saturating at 6) as a 4-bit code."""
+    v = np.asarray(v, np.float64)
+    if not np.all(np.isfinite(v)):
+        raise ValueError("e2m1_encode: non-finite input")
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    hi = np.minimum(np.searchsorted(E2M1_VALUES, a, side="left"), 7)   # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - E2M1_VALUES[lo]
+    d_hi = E2M1_VALUES[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(E2M1_VALUES[hi] == a, hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    return (code | (np.signbit(v).astype(np.uint8) << 3)).astype(np.uint8)
+
+
+def scale_exponent_e2m1(amax: np.ndarray) -> np.ndarray:
+    """floor(log2(amax)) - 2, clamped to [-127, 127]; -127 for amax = 0."""
+    amax = np.asarray(amax, np.float64)
+    _, ex = np.frexp(amax)                       # amax = m 2^ex, m in [0.5, 1)
+    e = ex.astype(np.int64) - 1 - EMAX_E2M1
+    e = np.where(amax > 0, e, -127)
+    return np.clip(e, -127, 127)
+
+
+def mx4_quantize(x: np.ndarray):
+    """Quantise along the last axis (a multiple of 32) to E2M1 codes and E8M0 scale bytes."""
+    x = np.asarray(x, np.float64)
+    K = x.shape[-1]
+    if K % BLOCK:
+        raise ValueError("last axis must be a multiple of 32")
+    blocks = x.reshape(*x.shape[:-1], K // BLOCK, BLOCK)
+    e = scale_exponent_e2m1(np.abs(blocks).max(axis=-1))
+    codes = e2m1_encode(blocks * np.exp2(-e)[..., None])     # exact power-of-two scaling
+    return codes.reshape(x.shape), (e + 127).astype(np.uint8)
+
+
+def mx4_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    K = codes.shape[-1]
+    v = e2m1_decode(codes).reshape(*codes.shape[:-1], K // BLOCK, BLOCK)
+    return (v * np.exp2(scales.astype(np.float64) - 127)[..., None]).reshape(codes.shape)
+
+
+def qdq4(x: np.ndarray) -> np.ndarray:
+    """E2M1 quantise-dequantise along the last axis, zero-padding it to a multiple of 32."""
+    x = np.asarray(x, np.float64)
+    K = x.shape[-1]
+    pad = (-K) % BLOCK
+    if pad:
+        x = np.concatenate([x, np.zeros((*x.shape[:-1], pad))], axis=-1)
+    return mx4_dequantize(*mx4_quantize(x))[..., :K]
+
+
+def mx_matmul_w4(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """a [M,K] (activations, MXFP8) x b [N,K]^T (weights, E2M1), both blocked along K."""
+    return qdq(a).astype(dtype) @ qdq4(b).astype(dtype).T
