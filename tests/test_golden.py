@@ -29,9 +29,9 @@ def _lines(name):
             yield line
 
 
-def _mx_cases():
+def _mx_cases(name="mx_blocks.txt"):
     cases, cur = [], None
-    for line in _lines("mx_blocks.txt"):
+    for line in _lines(name):
         key, _, rest = line.partition(" ")
         if key == "case":
             cur = {"name": rest, "values": np.zeros(32), "codes": np.zeros(32, np.uint8)}
@@ -52,6 +52,13 @@ def _mx_cases():
 @pytest.mark.parametrize("case", _mx_cases(), ids=lambda c: c["name"])
 def test_mx_block_by_hand(case):
     codes, scales = mx.mx_quantize(case["values"].reshape(1, 32))
+    assert int(scales[0, 0]) == case["scale"]
+    assert np.array_equal(codes[0], case["codes"]), [hex(c) for c in codes[0]]
+
+
+@pytest.mark.parametrize("case", _mx_cases("mx4_blocks.txt"), ids=lambda c: c["name"])
+def test_mx4_block_by_hand(case):
+    codes, scales = mx.mx4_quantize(case["values"].reshape(1, 32))
     assert int(scales[0, 0]) == case["scale"]
     assert np.array_equal(codes[0], case["codes"]), [hex(c) for c in codes[0]]
 
