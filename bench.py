@@ -257,6 +257,60 @@ def job_rate(world, flops_per_replica, ms):
     return world * flops_per_replica / (ms * 1e-3) / 1e12
 
 
+def _mlp_bytes(N, d, w, G, mx8, quantise_weights):
+    """Algorithmic bytes of the six GEMMs of N rows through G experts of width w (each
+    kernel reads its operands once and writes its results once)."""
+    q = 1.0 + 1.0 / 32                  # an MXFP8 element with its share of a block scale
+    a = q if mx8 else 2.0               # a GEMM operand element (activation or weight)
+    wgu, wd = 2.0 * w * d * G, 1.0 * d * w * G
+    h_out = 2.0 * N * w * q if mx8 else N * w * 2.0        # h: both code orientations in MXFP8
+    dgu_out = 2.0 * N * 2 * w * q if mx8 else N * 2 * w * 2.0
+    b = 0.0
+    if mx8 and quantise_weights:        # both weights, read once, both orientations written
+        b += (wgu + wd) * 2.0 + 2.0 * (wgu + wd) * q
+    b += N * d * a + wgu * a + N * 2 * w * 2.0 + h_out      # gate/up + SwiGLU: G|U saved in bf16
+    b += N * w * a + wd * a + N * d * 2.0                   # down
+    b += N * d * a + wd * a + N * 2 * w * 2.0 + dgu_out     # down dgrad + SwiGLU'
+    b += N * d * a + N * w * a + wd * 2.0                   # down wgrad
+    b += N * 2 * w * a + wgu * a + N * d * 2.0              # gate/up dgrad
+    b += N * 2 * w * a + N * d * a + wgu * 2.0              # gate/up wgrad
+    return b
+
+
+def step_bytes(cfg, prec="bf16", weights_cached=False) -> float:
+    """Algorithmic HBM bytes of one layer step (forward and backward): every kernel reads
+    its inputs once and writes its outputs once; x and dY count once although a token's
+    k routed rows are gathered from them.  Index maps, routing weights and dw partials
+    (well under 1 %) are left out."""
+    T, d, f, E, k, fs = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared
+    R = T * k
+    mx8 = prec == "mxfp8"
+    q = 1.0 + 1.0 / 32
+    b = T * E * 4.0 + T * k * 8.0                           # route
+    b += T * d * 2.0 + (2.0 * R * d * q if mx8 else R * d * 2.0)   # dispatch of x
+    b += _mlp_bytes(R, d, f, E, mx8, not weights_cached)
+    b += R * d * 2.0 + T * d * 2.0                          # combine
+    b += T * d * 2.0 + (2.0 * R * d * q if mx8 else R * d * 2.0)   # combine backward (dY rows)
+    b += R * d * 2.0 + T * d * 2.0                          # un-permute (dX)
+    b += T * E * 4.0 * 2 + T * k * 12.0                     # router backward
+    if fs:
+        if mx8:                                             # x and dY quantised for the shared GEMMs
+            b += 2 * (T * d * 2.0 + 2.0 * T * d * q)
+        b += _mlp_bytes(T, d, fs, 1, mx8, not weights_cached)
+        b += 2 * T * d * 2.0                                # its output read by combine, its dX by un-permute
+    return b
+
+
+def step_bound(cfg, prec, weights_cached, ms, peak_tflops, hbm_gbs):
+    """The step's combined roofline: max(FLOPs / tensor peak, bytes / HBM bandwidth)."""
+    flop_ms = cfg.flops_fwd_bwd() / (peak_tflops * 1e12) * 1e3
+    nbytes = step_bytes(cfg, prec, weights_cached)
+    byte_ms = nbytes / (hbm_gbs * 1e9) * 1e3
+    bound_ms = max(flop_ms, byte_ms)
+    return {"bound": "tensor" if flop_ms >= byte_ms else "hbm", "flop_ms": flop_ms, "byte_ms": byte_ms,
+            "bytes": nbytes, "bound_ms": bound_ms, "frac": bound_ms / ms}
+
+
 # ---------------------------------------------------------------------------- native
 
 def run_native(args, cfg):
@@ -505,6 +559,7 @@ def run_native(args, cfg):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clocks,
+        "step_bound": step_bound(cfg, args.prec, args.weights_cached, ms, peak, peaks["hbm_gbs"]),
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

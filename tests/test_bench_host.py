@@ -62,3 +62,51 @@ def test_weights_cached_needs_mxfp8():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--weights-cached"], capture_output=True,
                        text=True, cwd=ROOT)
     assert r.returncode != 0 and "--weights-cached applies to --prec mxfp8" in r.stderr
+
+
+def _dense_cfg(**kw):
+    from dropless_mixture_experts_warp_gb300 import synth
+    base = dict(T=128, d=128, f=64, E=1, k=1, score="softmax", bias="zero", seed=1)
+    base.update(kw)
+    return synth.MoEConfig("hand", **base)
+
+
+def test_step_bytes_of_a_small_dense_step_by_hand():
+    # T = R = 128 rows, d = 128, f = 64, one expert; bf16 elements are 2 bytes:
+    # route 128*1*4 + 128*1*8 = 1536; dispatch 2 * 128*128*2 = 65536;
+    # gate/up: x 32768 + W_gu (128x128) 32768 + G|U 32768 + h 16384 = 114688;
+    # down: h 16384 + W_d 16384 + y 32768 = 65536;
+    # down dgrad: dY rows 32768 + W_d 16384 + G|U 32768 + dG|dU 32768 = 114688;
+    # down wgrad: 32768 + 16384 + dW_d 16384 = 65536;
+    # gate/up dgrad: dG|dU 32768 + W_gu 32768 + dX rows 32768 = 98304;
+    # gate/up wgrad: 32768 + 32768 + dW_gu 32768 = 98304;
+    # combine, combine backward, un-permute 65536 each; router backward 1024 + 1536 = 2560
+    cfg = _dense_cfg()
+    assert bench.step_bytes(cfg, "bf16") == 1536 + 65536 + 557056 + 3 * 65536 + 2560
+
+
+def test_step_bytes_weight_quantisation_term():
+    # MXFP8: cached weights save reading both bf16 weights once (2 bytes an element) and
+    # writing their codes in two orientations (1 + 1/32 bytes an element each)
+    cfg = _dense_cfg()
+    w = 3 * 128 * 64
+    saved = bench.step_bytes(cfg, "mxfp8") - bench.step_bytes(cfg, "mxfp8", weights_cached=True)
+    assert saved == w * 2 + 2 * w * (1 + 1 / 32)
+    sh = _dense_cfg(f_shared=64)
+    saved_sh = bench.step_bytes(sh, "mxfp8") - bench.step_bytes(sh, "mxfp8", weights_cached=True)
+    assert saved_sh == 2 * saved                       # the shared expert's weights too
+
+
+def test_step_bound_picks_the_slower_roof():
+    from dropless_mixture_experts_warp_gb300 import synth
+    mix = synth.CONFIGS["mixtral"]
+    b = bench.step_bound(mix, "bf16", False, 10.0, 1719.5, 6764.0)
+    assert b["bound"] == "tensor" and b["bound_ms"] == b["flop_ms"] > b["byte_ms"]
+    assert abs(b["flop_ms"] - mix.flops_fwd_bwd() / 1719.5e12 * 1e3) < 1e-12
+    assert abs(b["frac"] - b["bound_ms"] / 10.0) < 1e-12
+    probe = synth.CONFIGS["hbm-probe"]
+    b = bench.step_bound(probe, "bf16", False, 2.0, 1719.5, 6764.0)
+    assert b["bound"] == "hbm" and b["bound_ms"] == b["byte_ms"] == b["bytes"] / 6764e9 * 1e3
+    for cfg in synth.CONFIGS.values():
+        for prec in ("bf16", "mxfp8"):
+            assert bench.step_bytes(cfg, prec) > 0

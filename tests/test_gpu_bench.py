@@ -30,5 +30,7 @@ def test_bench_line(prec):
         roof["achieved"] / roof["peak"])
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    sb = line["step_bound"]
+    assert sb["bound"] in ("tensor", "hbm") and sb["bound_ms"] == max(sb["flop_ms"], sb["byte_ms"]) > 0
     per_step = 13 if prec == "bf16" else 16
     assert line["gpu_launches"] == 3 * per_step
