@@ -76,3 +76,31 @@ def test_argument_errors_are_returned_without_launching(lib):
         B.moe_gemm_bf16(16, 16, 16, 128, 100, 64, 0, 0, 16, stream=0)   # N % 64
     assert e.value.status == 2
     assert B.moe_launch_count() == before
+
+
+def test_grouped_routing_and_mxfp8_argument_checks(lib):
+    from dropless_mixture_experts_warp_gb300 import binding as B
+    before = B.moe_launch_count()
+    sig = B.make_dims(256, 128, 64, 16, 4, score="sigmoid")
+    p = 16                                      # any aligned non-null pointer: nothing is launched
+
+    def grouped(dims, n_group, topk_group, scale):
+        with pytest.raises(B.MoeError) as e:
+            B.moe_route_topk_grouped(dims, p, None, n_group, topk_group, scale, p, p, p, p, p, p, p, stream=0)
+        return e.value.status
+
+    assert grouped(sig, 3, 2, 1.0) == 1         # 16 experts do not split into 3 groups
+    assert grouped(sig, 4, 5, 1.0) == 1         # more eligible groups than groups
+    assert grouped(sig, 8, 1, 1.0) == 1         # k = 4 > 1 group of 2 experts
+    assert grouped(sig, 4, 2, 0.0) == 1         # routed scale must be positive
+    assert grouped(sig, 16, 4, 1.0) == 1        # groups of one expert
+    soft = B.make_dims(256, 128, 64, 16, 4)
+    assert grouped(soft, 4, 2, 1.0) == 1        # group-limited routing is sigmoid-only
+    mx = B.make_dims(256, 128, 64, 8, 2, prec="mxfp8")
+    assert B.moe_check_dims(mx) == 2            # MXFP8 needs f % 128
+    assert B.moe_mx_weights_size(mx) == 0 and B.moe_mx_workspace_size(mx) == 0
+    ok = B.make_dims(256, 128, 128, 8, 2, prec="mxfp8")
+    assert B.moe_check_dims(ok) == 0
+    # codes (1 byte) and scales (1/32) of both weights in both orientations
+    assert B.moe_mx_weights_size(ok) >= 2 * 3 * 8 * 128 * 128 * (1 + 1 / 32)
+    assert B.moe_launch_count() == before
