@@ -233,7 +233,8 @@ def run_reference(args, cfg):
             "config": config_json(cfg, f"{args.prec} (fp32 oracle)"),
             "tokens_per_s": tok / total,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{chunk} random tokens of the {cfg.T}-token batch per step (fp32 NumPy)"},
+                             "sample": f"{chunk} random tokens of the {cfg.T}-token batch per step (fp32 NumPy)",
+                             "extrapolated_full_step_s": cfg.flops_fwd_bwd() / (value * 1e12)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -572,7 +573,8 @@ def run_native(args, cfg):
                                               args.cpu_seconds, oracle_chunk(args), prec=args.prec)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{ntok} random tokens of the {cfg.T}-token batch, fp32 NumPy, "
-                                          f"{secs:.1f} s"}
+                                          f"{secs:.1f} s",
+                                "extrapolated_full_step_s": flops / rate}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

@@ -110,3 +110,22 @@ def test_step_bound_picks_the_slower_roof():
     for cfg in synth.CONFIGS.values():
         for prec in ("bf16", "mxfp8"):
             assert bench.step_bytes(cfg, prec) > 0
+
+
+def test_reference_arm_line_on_the_tiny_workload():
+    """--impl reference times the CPU oracle (no GPU involved) and prints one line with the
+    contract's keys, its own cpu_baseline and an e2e without host copies."""
+    import json
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    for key in ("metric", "value", "unit", "n_gpus", "ms_per_step", "higher_is_better", "config", "cpu_baseline",
+                "e2e"):
+        assert key in line, key
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] > 0 and cb["cores"] >= 1
+    from dropless_mixture_experts_warp_gb300 import synth
+    assert abs(cb["extrapolated_full_step_s"] - synth.CONFIGS["tiny"].flops_fwd_bwd() / (cb["value"] * 1e12)) < 1e-9
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
