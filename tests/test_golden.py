@@ -114,3 +114,36 @@ def test_swiglu_one_token_by_hand():
     close(bwd["dW_d"][0], names["dW_d0"])
     close(bwd["dW_d"][1], names["dW_d1"])
     close(bwd["d_logits"][0], names["d_logits"])
+
+
+def _grouped_blocks():
+    blocks, cur = [], None
+    for line in _lines("routing_grouped.txt"):
+        key, _, rest = line.partition(" ")
+        if key == "grouped":
+            f = rest.split()
+            cur = {"k": int(f[1]), "E": int(f[3]), "n_group": int(f[5]), "topk_group": int(f[7]),
+                   "scale": float(f[9]), "logits": [], "idx": [], "w": []}
+            blocks.append(cur)
+        elif key == "bias":
+            cur["bias"] = [float(t) for t in rest.split()]
+        elif key == "token":
+            lg, _, out = rest.partition("->")
+            idx, _, w = out.partition("|")
+            cur["logits"].append([_expr(t) for t in lg.split()])
+            cur["idx"].append([int(t) for t in idx.split()])
+            cur["w"].append([_expr(t) for t in w.split()])
+        elif key == "split_sizes":
+            cur["split"] = [int(t) for t in rest.split()]
+    return blocks
+
+
+@pytest.mark.parametrize("block", _grouped_blocks())
+def test_grouped_routing_by_hand(block):
+    logits = np.array(block["logits"], np.float32)
+    idx, w = om.route_grouped(logits, block["k"], block["n_group"], block["topk_group"], np.array(block["bias"]),
+                              block["scale"], np.float64)
+    assert np.array_equal(idx, np.array(block["idx"]))
+    np.testing.assert_allclose(w, np.array(block["w"]), rtol=0, atol=1e-6)   # fp32 logits
+    split, _, _, _ = om.dispatch(idx, block["E"])
+    assert list(split) == block["split"]
