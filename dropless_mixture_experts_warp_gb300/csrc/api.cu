@@ -160,8 +160,8 @@ static bool pair_ok(GemmKind kind, const GemmParams& p) {
   return true;
 }
 
-static cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
-                               const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
+                        const GemmParams& p, cudaStream_t s) {
   if (pair_ok(kind, p)) return launch_gemm_pair(kind, a, b, p, s);
   return bwd ? launch_gemm_bwd(kind, a, b, p, s) : launch_gemm_fwd(kind, a, b, p, s);
 }

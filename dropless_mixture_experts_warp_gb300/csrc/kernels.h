@@ -74,6 +74,12 @@ cudaError_t launch_gemm_bwd(GemmKind kind, const CUtensorMap& a, const CUtensorM
 cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmParams& p, cudaStream_t stream);
 
+// The CTA-pair kernel where the product allows it (tiles at least 128 columns wide;
+// weight gradients in 256-row pairs), else the single-CTA kernel (bwd selects the
+// translation unit holding the backward instantiations).
+cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
+                        const GemmParams& p, cudaStream_t stream);
+
 // Grid of a persistent CTA-pair kernel: as many pairs as can be resident at once
 // (an SM whose TPC neighbour is unavailable cannot host half of a pair), at most
 // one per two SMs.

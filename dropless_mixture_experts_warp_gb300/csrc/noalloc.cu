@@ -82,7 +82,8 @@ extern "C" moe_status moe_gemm_down_dgrad_noalloc(const moe_dims* dims, const mo
   p.b_k_per_expert = d.d; p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu; p.dgu_out = dgu; p.dw_part = scratch;
   p.dw_stride = n_tiles; p.status = dev_status;
-  if (launch_gemm_bwd(GEMM_ROWS_SWIGLU_BWD, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the same kernel choice as moe_gemm_down_dgrad, so both give the same bits
+  if (launch_best(GEMM_ROWS_SWIGLU_BWD, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_dw_reduce(scratch, n_tiles, row_offsets, d.E, dw_rows, static_cast<int>(R_cap), s) ==
                  cudaSuccess
              ? MOE_OK

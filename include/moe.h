@@ -204,8 +204,11 @@ moe_status moe_combine_fwd(const moe_dims* dims, const moe_bf16* rows,
                            moe_bf16* out, void* stream);
 
 /*
- * Backward of step 6 (the adjoint of the combine sum): dy_rows[r] = dY[token of r],
- * padding rows set to 0.
+ * Backward of step 6 (the adjoint of the combine sum) [BIO "צמצום הזיכרון ותקורות
+ * הכימות": the fused grouped-MLP operation has a backward counterpart; MEGA "Mega MoE
+ * คืออะไร?": combine returns expert outputs to their tokens, so its adjoint hands each
+ * token's output gradient back to every row it was combined from]:
+ * dy_rows[r] = dY[token of r], padding rows set to 0.
  *   dy [T][d] bf16, token_to_row [T][k], split_sizes, row_offsets, dy_rows [rows][d].
  */
 moe_status moe_combine_bwd(const moe_dims* dims, const moe_bf16* dy,
@@ -280,7 +283,10 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
                               void* stream);
 
 /*
- * Backward of step 1: router-logit gradient from the routing-weight gradient.
+ * Backward of step 1 [DROPLESS "A dropless MoE minden tokent feldolgoz": the router is
+ * learned, so the loss reaches its logits through the top-K routing weights; PRIME
+ * "Mit csinált a Prime Intellect?": a backward pass for the fused MoE layer]:
+ * router-logit gradient from the routing-weight gradient.
  * dw[t][j] = dw_rows[token_to_row[t][j]];  c = sum_j w dw;
  *   softmax: dl[e_j] = w_j (dw_j - c)
  *   sigmoid: dl[e_j] = (dw_j - c) / sum_j s_j * s_j (1 - s_j),  s = sigmoid(logit)
@@ -307,8 +313,10 @@ moe_status moe_route_topk_bwd_scaled(const moe_dims* dims, const float* logits, 
  * synchronisation they may bring are not allowed).  The pages have no counterpart:
  * this is an interface convenience, not a step of the method.
  *
- * Same arguments, results and kernels as moe_gemm_down_dgrad minus `workspace`: the
- * per-tile partial sums of dw go to a static device array of
+ * Same arguments, kernels (the CTA-pair kernel where f allows it, else the single-CTA
+ * one, chosen exactly as moe_gemm_down_dgrad chooses) and therefore the same bits as
+ * moe_gemm_down_dgrad minus `workspace`: the per-tile partial sums of dw go to a
+ * static device array of
  * moe_noalloc_scratch_bytes() bytes (8 MiB) that every GPU loading the library holds
  * until the process exits.  Requires moe_row_capacity(dims) * (f / BN) <= 2^21,
  * BN = 256, 128 or 64 (the largest dividing f); larger problems get
@@ -316,7 +324,10 @@ moe_status moe_route_topk_bwd_scaled(const moe_dims* dims, const float* logits, 
  * cudaMalloc, cudaFree or allocating library call.
  *
  * The first call on a device looks up the array's device address (once per device,
- * with that device current); make that first call before any stream capture.  All
+ * with that device current) and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not use this call after cudaDeviceReset (or
+ * anything else that destroys and recreates the device's primary context): the kept
+ * address would then be stale.  All
  * calls share the one array, which keeps the last call's contents (nothing in it has
  * to start at zero); calls that overlap on the GPU race on it and give wrong dw_rows.
  */

@@ -19,5 +19,6 @@ from .moe_oracle import (  # noqa: F401
     route_backward,
     expert_wgrad,
     expert_wgrad_sampled,
+    expert_rows,
 )
 from . import mx  # noqa: F401,E402

@@ -196,6 +196,38 @@ def swiglu_expert_forward(x_rows: np.ndarray, w_gu: np.ndarray, w_d: np.ndarray,
     return {"g": g, "u": u, "a": a, "h": h, "y": y}
 
 
+def expert_rows(x_rows, w_rows, dy_rows, w_gu_e, w_d_e, dtype=np.float64, full: bool = True):
+    """One expert's share of the layer, forward and backward, on rows routed to it.
+
+    The loop bodies of moe_forward and moe_backward for a single expert e, for callers
+    that go through the experts themselves (one at a time, or several side by side):
+      x_rows [n,d], dy_rows [n,d]: X and dY of the tokens routed to e (token order);
+      w_rows [n]: their routing weights for e.
+    Returns per row: y (the term combine adds for this slot), g, u, dw (dL/d routing
+    weight), dGU = [dG | dU], dx (the term the un-permute adds); with full=True (the rows
+    are all of e's rows) also dW_gu [2f,d] and dW_d [d,f].
+    """
+    x = np.asarray(x_rows, dtype)
+    dy = np.asarray(dy_rows, dtype)
+    wg = np.asarray(w_gu_e, dtype)
+    wd = np.asarray(w_d_e, dtype)
+    f = wd.shape[1]
+    we = np.asarray(w_rows, dtype)[:, None]
+    r = swiglu_expert_forward(x, wg, wd, np.asarray(w_rows, dtype))
+    g, u, a = r["g"], r["u"], r["a"]
+    sg = _sigmoid(g)
+    dh = dy @ wd
+    da = we * dh
+    dg = da * u * sg * (1.0 + g * (1.0 - sg))
+    du = da * g * sg
+    out = {"y": r["y"], "g": g, "u": u, "dw": (a * dh).sum(axis=1), "dGU": np.concatenate([dg, du], axis=1),
+           "dx": dg @ wg[:f] + du @ wg[f:]}
+    if full:
+        out["dW_d"] = dy.T @ (we * a)
+        out["dW_gu"] = np.concatenate([dg.T @ x, du.T @ x], axis=0)
+    return out
+
+
 def moe_forward(x, logits, w_gu, w_d, k: int, score: str = SOFTMAX,
                 w_gu_s=None, w_d_s=None, dtype=np.float64, grouped: Optional[dict] = None) -> Dict[str, np.ndarray]:
     """Forward of the layer on token-major inputs.
@@ -274,7 +306,7 @@ def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
     Per expert e and each of its rows (token t, slot j):
       dH = dY[t] W_d[e]          dw[t,j] = sum_f A * dH
       dA = w dH                  dG = dA * U * silu'(G),   dU = dA * silu(G)
-      dX[t] += dG W_gate[e] + dU W_up[e]
+      dX[t] += dG W_gate[e] + dU W_up[e]       (dGU[t,j] = [dG | dU] is returned too)
       dW_d[e] += dY[t]^T H,  dW_gate[e] += dG^T X[t],  dW_up[e] += dU^T X[t]
     with silu'(g) = sigmoid(g) (1 + g (1 - sigmoid(g))).
     """
@@ -285,6 +317,7 @@ def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
     f = w_d.shape[2]
     idx, w = fwd["idx"], fwd["w"]
     dx_slot = np.zeros((T, k, d), dtype)
+    dgu_slot = np.zeros((T, k, 2 * f), dtype)
     dw = np.zeros((T, k), dtype)
     dw_gu = np.zeros((E, 2 * f, d), dtype)
     dw_d = np.zeros((E, d, f), dtype)
@@ -304,6 +337,8 @@ def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
         da = we * dh
         dg = da * u * sg * (1.0 + g * (1.0 - sg))
         du = da * g * sg
+        dgu_slot[t_sel, j_sel, :f] = dg
+        dgu_slot[t_sel, j_sel, f:] = du
         dx_slot[t_sel, j_sel] = dg @ wg[:f] + du @ wg[f:]
         dw_d[e] = dy[t_sel].T @ (we * a)
         dw_gu[e, :f] = dg.T @ x[t_sel]
@@ -311,7 +346,7 @@ def moe_backward(x, logits, w_gu, w_d, dy, fwd: Dict[str, np.ndarray], k: int,
     dx = np.zeros((T, d), dtype)
     for j in range(k):
         dx += dx_slot[:, j]
-    out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw,
+    out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw, "dGU": dgu_slot,
            "d_logits": route_backward(logits, idx, w, dw, SIGMOID if grouped is not None else score, dtype,
                                       1.0 if grouped is None else grouped.get("routed_scale", 1.0))}
     if w_gu_s is not None:

@@ -211,6 +211,7 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
     f = w_d.shape[2]
     idx, w = fwd["idx"], fwd["w"]
     dx_slot = np.zeros((T, k, d), dtype)
+    dgu_slot = np.zeros((T, k, 2 * f), dtype)
     dw = np.zeros((T, k), dtype)
     dw_gu = np.zeros((E, 2 * f, d), dtype)
     dw_d = np.zeros((E, d, f), dtype)
@@ -230,13 +231,14 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
         dw[t_sel, j_sel] = (a * dh).sum(axis=1)
         da = we * dh
         dgu = np.concatenate([da * u * sg * (1.0 + g * (1.0 - sg)), da * g * sg], axis=1)
+        dgu_slot[t_sel, j_sel] = dgu
         dx_slot[t_sel, j_sel] = wmatmul(dgu, wg.T, dtype)
         dw_d[e] = matmul(dye.T, (we * a).T, dtype)
         dw_gu[e] = matmul(dgu.T, x[t_sel].T, dtype)
     dx = np.zeros((T, d), dtype)
     for j in range(k):
         dx += dx_slot[:, j]
-    out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw,
+    out = {"dX": dx, "dW_gu": dw_gu, "dW_d": dw_d, "dw": dw, "dGU": dgu_slot,
            "d_logits": om.route_backward(logits, idx, w, dw, om.SIGMOID if grouped is not None else score, dtype,
                                          1.0 if grouped is None else grouped.get("routed_scale", 1.0))}
     if w_gu_s is not None:
@@ -250,6 +252,40 @@ def moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, k, score="softmax", w_gu_s=No
         out["dX"] = dx + wmatmul(dgu, wg.T, dtype)
         out["dW_d_s"] = matmul(dy.T, (g * sg * u).T, dtype)
         out["dW_gu_s"] = matmul(dgu.T, x.T, dtype)
+    return out
+
+
+def expert_rows_mx(x_rows, w_rows, dy_rows, w_gu_e, w_d_e, dtype=np.float64, full=True, matmul=mx_matmul,
+                   wmatmul=None):
+    """One expert's share of the MXFP8 layer, forward and backward, on rows routed to it.
+
+    The loop bodies of moe_forward_mx and moe_backward_mx for a single expert (arguments
+    and results as moe_oracle.expert_rows): every GEMM operand quantised along that
+    GEMM's contraction; with full=True the rows are all of the expert's rows, in token
+    order, so the weight gradients' row blocks start at the segment's first row.
+    ``wmatmul`` (default ``matmul``) is the product whose second operand is a weight.
+    """
+    from . import moe_oracle as om
+    wmatmul = matmul if wmatmul is None else wmatmul
+    x = np.asarray(x_rows, dtype)
+    dy = np.asarray(dy_rows, dtype)
+    wg = np.asarray(w_gu_e, dtype)
+    wd = np.asarray(w_d_e, dtype)
+    f = wd.shape[1]
+    we = np.asarray(w_rows, dtype)[:, None]
+    gu = wmatmul(x, wg, dtype)
+    g, u = gu[:, :f], gu[:, f:]
+    sg = om._sigmoid(g)
+    a = g * sg * u
+    h = we * a
+    dh = wmatmul(dy, wd.T, dtype)
+    da = we * dh
+    dgu = np.concatenate([da * u * sg * (1.0 + g * (1.0 - sg)), da * g * sg], axis=1)
+    out = {"y": wmatmul(h, wd, dtype), "g": g, "u": u, "dw": (a * dh).sum(axis=1), "dGU": dgu,
+           "dx": wmatmul(dgu, wg.T, dtype)}
+    if full:
+        out["dW_d"] = matmul(dy.T, h.T, dtype)
+        out["dW_gu"] = matmul(dgu.T, x.T, dtype)
     return out
 
 

@@ -1,45 +1,21 @@
 """Group-limited sigmoid routing (a DeepSeek-V3 router variant) on the GPU against the
 oracle.  Selection is decided in fp32 on both sides, but the two sigmoids may round
 differently in the last bit, so indices are compared bit for bit on every token whose
-group and expert decisions clear a margin of a few fp32 ulps; the others (rare, counted)
-are only checked for validity."""
+group and expert decisions clear a margin of a few fp32 ulps (at least 98 % of the
+tokens); every other token's choice must be one that lies within that margin of both
+cuts (route_util.assert_valid_near_ties)."""
 import numpy as np
 import pytest
 import torch
 
 from gpu_util import bf16_dev, f32_dev, host, need_gpu, rel_err
+from route_util import assert_valid_near_ties, decision_margins
 from oracle import moe_oracle as om
 from dropless_mixture_experts_warp_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 MARGIN = 2e-6
 TOL_BF16 = 2e-2
-
-
-def _decision_margins(logits, k, n_group, topk_group, bias):
-    """Per token: the gap at the group cut and at the expert cut of the fp32 decision."""
-    T, E = logits.shape
-    gs = E // n_group
-    one = np.float32(1.0)
-    c = (one / (one + np.exp(-logits.astype(np.float32)))) + bias.astype(np.float32)[None, :]
-    top2 = -np.sort(-c.reshape(T, n_group, gs), axis=2)[:, :, :2]
-    gsc = np.sort((top2[:, :, 0] + top2[:, :, 1]).astype(np.float64), axis=1)[:, ::-1]
-    g_gap = gsc[:, topk_group - 1] - gsc[:, topk_group] if topk_group < n_group else np.full(T, np.inf)
-    eligible_c = np.where(np.repeat(_eligible(c, n_group, topk_group), gs, axis=1), c, -np.inf)
-    cs = np.sort(eligible_c.astype(np.float64), axis=1)[:, ::-1]
-    e_gap = cs[:, k - 1] - cs[:, k] if k < topk_group * gs else np.full(T, np.inf)
-    return np.minimum(g_gap, e_gap)
-
-
-def _eligible(c, n_group, topk_group):
-    T, E = c.shape
-    gs = E // n_group
-    top2 = -np.sort(-c.reshape(T, n_group, gs), axis=2)[:, :, :2]
-    gsc = (top2[:, :, 0] + top2[:, :, 1]).astype(np.float64)
-    order = np.lexsort((np.broadcast_to(np.arange(n_group), (T, n_group)), -gsc), axis=-1)
-    el = np.zeros((T, n_group), bool)
-    np.put_along_axis(el, order[:, :topk_group], True, axis=1)
-    return el
 
 
 def _route_gpu(T, E, k, logits, bias, n_group, topk_group, scale):
@@ -62,14 +38,13 @@ def test_grouped_route_matches_oracle(T, E, k, n_group, topk_group):
     bias = (rng.standard_normal(E) * 0.2).astype(np.float32)
     idx, w, split = _route_gpu(T, E, k, logits, bias, n_group, topk_group, 2.5)
     ref_idx, ref_w = om.route_grouped(logits, k, n_group, topk_group, bias, 2.5)
-    decided = _decision_margins(logits, k, n_group, topk_group, bias) > MARGIN
+    decided = decision_margins(logits, k, n_group, topk_group, bias) > MARGIN
+    print(f"T={T} E={E}: {int((~decided).sum())} tokens within {MARGIN} of a cut")
     assert decided.mean() > 0.98
     assert np.array_equal(idx[decided], ref_idx[decided])
     assert np.abs(w[decided] - ref_w[decided]).max() <= 1e-5 * np.abs(ref_w).max()
-    # the undecided tokens still pick k distinct experts from topk_group groups
-    gs = E // n_group
-    for t in np.nonzero(~decided)[0]:
-        assert len(set(idx[t])) == k and len(set(idx[t] // gs)) <= topk_group
+    # the other tokens: a choice an exact router could make, within the margin of both cuts
+    assert_valid_near_ties(idx, logits, k, n_group, topk_group, bias, MARGIN, np.nonzero(~decided)[0])
     assert np.array_equal(split, np.bincount(idx.ravel(), minlength=E))
     np.testing.assert_allclose(w.sum(axis=1), 2.5, rtol=1e-5)
 
@@ -83,7 +58,7 @@ def test_grouped_layer_fwd_bwd_matches_oracle():
     rng = np.random.default_rng(62)
     bias = (rng.standard_normal(cfg.E) * 0.1).astype(np.float32)
     n_group, topk_group, scale = 4, 2, 2.5
-    assert (_decision_margins(inp["logits"], cfg.k, n_group, topk_group, bias) > MARGIN).all()
+    assert (decision_margins(inp["logits"], cfg.k, n_group, topk_group, bias) > MARGIN).all()
     w_gu_b, w_d_b = synth.all_expert_weights(cfg)
     dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, 0, cfg.score)
     b = layer.allocate(dims)

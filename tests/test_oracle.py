@@ -266,6 +266,58 @@ def test_token_subset_equals_full_batch():
     np.testing.assert_allclose(b["d_logits"], full_b["d_logits"][sub], rtol=1e-13, atol=1e-13)
 
 
+def _assemble_expert_rows(fn, x, logits, w_gu, w_d, dy, k, score, full=True):
+    """Y, dX, dw, dGU, d_logits and the weight gradients put together from per-expert calls."""
+    idx, w = om.route(logits, k, score)
+    T, d = x.shape
+    E, f2 = w_gu.shape[0], w_gu.shape[1]
+    y_slot, dx_slot = np.zeros((T, k, d)), np.zeros((T, k, d))
+    dgu, dw = np.zeros((T, k, f2)), np.zeros((T, k))
+    dW_gu, dW_d = np.zeros_like(w_gu), np.zeros_like(w_d)
+    for e in range(E):
+        t_sel, j_sel = np.nonzero(idx == e)
+        if t_sel.size == 0:
+            continue
+        r = fn(x[t_sel], w[t_sel, j_sel], dy[t_sel], w_gu[e], w_d[e], full=full)
+        y_slot[t_sel, j_sel], dx_slot[t_sel, j_sel] = r["y"], r["dx"]
+        dgu[t_sel, j_sel], dw[t_sel, j_sel] = r["dGU"], r["dw"]
+        if full:
+            dW_gu[e], dW_d[e] = r["dW_gu"], r["dW_d"]
+    return {"Y": y_slot.sum(axis=1), "dX": dx_slot.sum(axis=1), "dw": dw, "dGU": dgu, "dW_gu": dW_gu,
+            "dW_d": dW_d, "d_logits": om.route_backward(logits, idx, w, dw, score)}
+
+
+@pytest.mark.parametrize("score", [om.SOFTMAX, om.SIGMOID])
+def test_expert_rows_assemble_the_layer(score):
+    """The per-expert form (used to spread full-size checks over threads) gives the layer
+    oracle's forward and backward, and the layer's dGU reassembles its dW_gu and dX."""
+    x, logits, w_gu, w_d, dy, _ = _small_problem(43, E=6, k=3)
+    fwd = om.moe_forward(x, logits, w_gu, w_d, 3, score)
+    bwd = om.moe_backward(x, logits, w_gu, w_d, dy, fwd, 3, score)
+    got = _assemble_expert_rows(om.expert_rows, x, logits, w_gu, w_d, dy, 3, score)
+    for key, ref in (("Y", fwd["Y"]), ("dX", bwd["dX"]), ("dw", bwd["dw"]), ("dGU", bwd["dGU"]),
+                     ("dW_gu", bwd["dW_gu"]), ("dW_d", bwd["dW_d"]), ("d_logits", bwd["d_logits"])):
+        np.testing.assert_allclose(got[key], ref, rtol=1e-12, atol=1e-12, err_msg=key)
+    idx = fwd["idx"]
+    for e in range(6):                              # dW_gu[e] = dGU_e^T X_e, dX = sum_j dGU W_gu
+        t_sel, j_sel = np.nonzero(idx == e)
+        np.testing.assert_allclose(bwd["dGU"][t_sel, j_sel].T @ x[t_sel], bwd["dW_gu"][e], rtol=1e-12, atol=1e-12)
+    dx = sum(np.einsum("tf,tfd->td", bwd["dGU"][:, j], w_gu[idx[:, j]]) for j in range(3))
+    np.testing.assert_allclose(dx, bwd["dX"], rtol=1e-12, atol=1e-12)
+
+
+def test_expert_rows_of_a_row_subset_equal_those_of_all_rows():
+    """Per-row results depend on their own row only (sampled full-size checks rely on it)."""
+    x, logits, w_gu, w_d, dy, _ = _small_problem(44, E=3, k=2)
+    idx, w = om.route(logits, 2, om.SOFTMAX)
+    t_sel, j_sel = np.nonzero(idx == 1)
+    full = om.expert_rows(x[t_sel], w[t_sel, j_sel], dy[t_sel], w_gu[1], w_d[1])
+    sub = np.array([0, 2, len(t_sel) - 1])
+    part = om.expert_rows(x[t_sel[sub]], w[t_sel[sub], j_sel[sub]], dy[t_sel[sub]], w_gu[1], w_d[1], full=False)
+    for key in ("y", "dx", "dw", "dGU"):
+        np.testing.assert_allclose(part[key], full[key][sub], rtol=1e-13, atol=1e-13, err_msg=key)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _dense_forward_error(score=om.SOFTMAX):

@@ -168,3 +168,28 @@ def test_fast_qdq_equals_code_table_path():
     assert np.array_equal(mx.qdq(x32).astype(np.float64), mx.qdq(x32.astype(np.float64)))
     y32 = y.astype(np.float32)
     assert np.array_equal(mx.qdq(y32).astype(np.float64), mx.qdq(y32.astype(np.float64)))
+
+
+def test_mx_expert_rows_assemble_the_mx_layer():
+    """The per-expert MXFP8 form gives exactly the MXFP8 layer oracle's results (the same
+    quantised products on the same operands), and per-row results do not depend on the
+    other rows present."""
+    x, logits, w_gu, w_d, dy, _ = _small(seed=8, T=64, E=4, k=2)
+    fwd = mx.moe_forward_mx(x, logits, w_gu, w_d, 2)
+    bwd = mx.moe_backward_mx(x, logits, w_gu, w_d, dy, fwd, 2)
+    idx, w = fwd["idx"], fwd["w"]
+    y_slot, dx_slot, dw = np.zeros((64, 2, 64)), np.zeros((64, 2, 64)), np.zeros((64, 2))
+    for e in range(4):
+        t_sel, j_sel = np.nonzero(idx == e)
+        r = mx.expert_rows_mx(x[t_sel], w[t_sel, j_sel], dy[t_sel], w_gu[e], w_d[e])
+        y_slot[t_sel, j_sel], dx_slot[t_sel, j_sel], dw[t_sel, j_sel] = r["y"], r["dx"], r["dw"]
+        np.testing.assert_array_equal(r["dW_gu"], bwd["dW_gu"][e])
+        np.testing.assert_array_equal(r["dW_d"], bwd["dW_d"][e])
+        sub = np.array([0, len(t_sel) // 2, len(t_sel) - 1])
+        part = mx.expert_rows_mx(x[t_sel[sub]], w[t_sel[sub], j_sel[sub]], dy[t_sel[sub]], w_gu[e], w_d[e],
+                                 full=False)
+        for key in ("y", "dx", "dw", "dGU"):
+            np.testing.assert_array_equal(part[key], r[key][sub], err_msg=key)
+    np.testing.assert_array_equal(y_slot[:, 0] + y_slot[:, 1], fwd["Y"])
+    np.testing.assert_array_equal(dx_slot[:, 0] + dx_slot[:, 1], bwd["dX"])
+    np.testing.assert_array_equal(dw, bwd["dw"])
