@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd TFLOPS & tokens/s on 1 GB300; % of bf16/MXFP8 tensor peak"
 UNIT = "TFLOP/s"
+MX_PRECS = ("mxfp8", "mxfp8-w4")   # block-scaled precisions: the MXFP8 layer calls
 GEMMS = ["gate_up", "down", "down_dgrad", "down_wgrad", "gate_up_dgrad", "gate_up_wgrad"]
 GEMM_FLOP_FACTOR = {"gate_up": 4, "down": 2, "down_dgrad": 2, "down_wgrad": 2, "gate_up_dgrad": 4,
                     "gate_up_wgrad": 4}   # x R*d*f
@@ -86,6 +87,7 @@ def config_json(cfg, prec="bf16", weights_cached=False):
 KERNEL_SOURCES = {
     "bf16": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_pair.cu", "kernels.h", "api.cu"),
     "mxfp8": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "kernels.h", "api_mx.cu"),
+    "mxfp8-w4": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "kernels.h", "api_mx.cu", "api.cu"),
 }
 
 
@@ -201,7 +203,7 @@ class ExpertPool:
         return self.shape[0]
 
 
-def weight_cached_wmatmul():
+def weight_cached_wmatmul(fp4=False):
     """The MXFP8 oracle's weight product (mx.mx_matmul) with each weight operand's
     quantisation done once and kept: the layer quantises its weights once per step, not
     once per token chunk, so the timed chunks must not pay it again and again.  Keyed by
@@ -215,26 +217,27 @@ def weight_cached_wmatmul():
         key = (b.__array_interface__["data"][0], b.strides, b.shape, np.dtype(dtype).str)
         q = cache.get(key)
         if q is None:
-            q = cache[key] = mx.qdq(b).astype(dtype)
+            q = cache[key] = (mx.qdq4(b) if fp4 else mx.qdq(b)).astype(dtype)
         return mx.qdq(a).astype(dtype) @ q.T
     return wmatmul
 
 
-def weight_quant_seconds(w_gu, w_d, w_gu_s=None, w_d_s=None) -> float:
+def weight_quant_seconds(w_gu, w_d, w_gu_s=None, w_d_s=None, fp4=False) -> float:
     """Host time of one full step's MXFP8 weight quantisation by the oracle's qdq: every
     routed expert's W_gu and W_d in both of their contraction orientations (timed on one
     pool expert, times E) plus the shared expert's."""
     from oracle import mx
+    qdq = mx.qdq4 if fp4 else mx.qdq
     t0 = time.perf_counter()
     for m in (w_gu[0], w_d[0]):
-        mx.qdq(m)
-        mx.qdq(m.T)
+        qdq(m)
+        qdq(m.T)
     t = (time.perf_counter() - t0) * len(w_gu)
     if w_gu_s is not None:
         t0 = time.perf_counter()
         for m in (w_gu_s, w_d_s):
-            mx.qdq(m)
-            mx.qdq(m.T)
+            qdq(m)
+            qdq(m.T)
         t += time.perf_counter() - t0
     return t
 
@@ -270,7 +273,7 @@ def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu, w_d, seconds: float, 
     from oracle import moe_oracle as om
     from oracle import mx
     from dropless_mixture_experts_warp_gb300 import synth
-    mx8 = prec == "mxfp8"
+    mx8 = prec in MX_PRECS
     fwd_fn, bwd_fn = (mx.moe_forward_mx, mx.moe_backward_mx) if mx8 else (om.moe_forward, om.moe_backward)
     kw = {"wmatmul": wmatmul} if mx8 and wmatmul is not None else {}
     if shared is not None:
@@ -294,10 +297,10 @@ def oracle_sample_rate(cfg, x_bits, logits, dy_bits, w_gu, w_d, seconds: float, 
 def oracle_setup(cfg, prec, w_gu, w_d, shared):
     """(wmatmul, wq_seconds) for oracle_sample_rate: MXFP8 weights quantised once, untimed,
     and the host time of one full step's weight quantisation; (None, 0) for bf16."""
-    if prec != "mxfp8":
+    if prec not in MX_PRECS:
         return None, 0.0
-    wq_s = weight_quant_seconds(w_gu, w_d, *(shared or ()))
-    wm = weight_cached_wmatmul()
+    wq_s = weight_quant_seconds(w_gu, w_d, *(shared or ()), fp4=prec == "mxfp8-w4")
+    wm = weight_cached_wmatmul(fp4=prec == "mxfp8-w4")
     prequantise_pool(cfg, w_gu, w_d, shared, wm)
     return wm, wq_s
 
@@ -313,7 +316,7 @@ def sample_note(cfg, prec, ntok, secs, wq_seconds) -> str:
             f"{min(cfg.E, ORACLE_POOL)} distinct sets reused cyclically over the {cfg.E} experts (timing only)")
     if cfg.f_shared:
         note += "; the shared expert runs and is counted"
-    if prec == "mxfp8":
+    if prec in MX_PRECS:
         note += (f"; weights quantised once, each sample charged its token share of one full step's weight "
                  f"quantisation ({wq_seconds:.1f} s on the host)")
     return note
@@ -376,22 +379,23 @@ def job_rate(world, flops_per_replica, ms):
     return world * flops_per_replica / (ms * 1e-3) / 1e12
 
 
-def _mlp_bytes(N, d, w, G, mx8, quantise_weights):
+def _mlp_bytes(N, d, w, G, mx8, quantise_weights, w4=False):
     """Algorithmic bytes of the six GEMMs of N rows through G experts of width w (each
-    kernel reads its operands once and writes its results once)."""
+    kernel reads its operands once and writes its results once); w4: MXFP4 weights."""
     q = 1.0 + 1.0 / 32                  # an MXFP8 element with its share of a block scale
-    a = q if mx8 else 2.0               # a GEMM operand element (activation or weight)
+    a = q if mx8 else 2.0               # a GEMM operand element (activation)
+    qw = (0.5 + 1.0 / 32) if w4 else a  # a weight element as the GEMMs read it
     wgu, wd = 2.0 * w * d * G, 1.0 * d * w * G
     h_out = 2.0 * N * w * q if mx8 else N * w * 2.0        # h: both code orientations in MXFP8
     dgu_out = 2.0 * N * 2 * w * q if mx8 else N * 2 * w * 2.0
     b = 0.0
     if mx8 and quantise_weights:        # both weights, read once, both orientations written
-        b += (wgu + wd) * 2.0 + 2.0 * (wgu + wd) * q
-    b += N * d * a + wgu * a + N * 2 * w * 2.0 + h_out      # gate/up + SwiGLU: G|U saved in bf16
-    b += N * w * a + wd * a + N * d * 2.0                   # down
-    b += N * d * a + wd * a + N * 2 * w * 2.0 + dgu_out     # down dgrad + SwiGLU'
+        b += (wgu + wd) * 2.0 + 2.0 * (wgu + wd) * qw
+    b += N * d * a + wgu * qw + N * 2 * w * 2.0 + h_out     # gate/up + SwiGLU: G|U saved in bf16
+    b += N * w * a + wd * qw + N * d * 2.0                  # down
+    b += N * d * a + wd * qw + N * 2 * w * 2.0 + dgu_out    # down dgrad + SwiGLU'
     b += N * d * a + N * w * a + wd * 2.0                   # down wgrad
-    b += N * 2 * w * a + wgu * a + N * d * 2.0              # gate/up dgrad
+    b += N * 2 * w * a + wgu * qw + N * d * 2.0             # gate/up dgrad
     b += N * 2 * w * a + N * d * a + wgu * 2.0              # gate/up wgrad
     return b
 
@@ -403,11 +407,12 @@ def step_bytes(cfg, prec="bf16", weights_cached=False) -> float:
     (well under 1 %) are left out."""
     T, d, f, E, k, fs = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared
     R = T * k
-    mx8 = prec == "mxfp8"
+    mx8 = prec in MX_PRECS
+    w4 = prec == "mxfp8-w4"
     q = 1.0 + 1.0 / 32
     b = T * E * 4.0 + T * k * 8.0                           # route
     b += T * d * 2.0 + (2.0 * R * d * q if mx8 else R * d * 2.0)   # dispatch of x
-    b += _mlp_bytes(R, d, f, E, mx8, not weights_cached)
+    b += _mlp_bytes(R, d, f, E, mx8, not weights_cached, w4)
     b += R * d * 2.0 + T * d * 2.0                          # combine
     b += T * d * 2.0 + (2.0 * R * d * q if mx8 else R * d * 2.0)   # combine backward (dY rows)
     b += R * d * 2.0 + T * d * 2.0                          # un-permute (dX)
@@ -415,7 +420,7 @@ def step_bytes(cfg, prec="bf16", weights_cached=False) -> float:
     if fs:
         if mx8:                                             # x and dY quantised for the shared GEMMs
             b += 2 * (T * d * 2.0 + 2.0 * T * d * q)
-        b += _mlp_bytes(T, d, fs, 1, mx8, not weights_cached)
+        b += _mlp_bytes(T, d, fs, 1, mx8, not weights_cached, w4)
         b += 2 * T * d * 2.0                                # its output read by combine, its dX by un-permute
     return b
 
@@ -452,7 +457,7 @@ def make_step(ctx, bufs, dims, prec, weights_cached):
     import torch
     from dropless_mixture_experts_warp_gb300 import binding as B, synth
     cfg, stream, inp = ctx.cfg, ctx.stream, ctx.inp
-    mx8 = prec == "mxfp8"
+    mx8 = prec in MX_PRECS
     w_gu, w_d = inp["w_gu"], inp["w_d"]
     grouped = synth.grouped_options(cfg)
     sel_bias = torch.from_numpy(grouped["bias"]).to(ctx.dev) if grouped is not None else None
@@ -616,7 +621,7 @@ def measure(ctx, args, prec, weights_cached):
     import torch
     from dropless_mixture_experts_warp_gb300 import binding as B, layer
     cfg, dev, stream, dist, world = ctx.cfg, ctx.dev, ctx.stream, ctx.dist, ctx.world
-    mx8 = prec == "mxfp8"
+    mx8 = prec in MX_PRECS
     dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, prec)
     bufs = layer.allocate(dims, dev)
     torch.cuda.synchronize(dev)
@@ -677,11 +682,14 @@ def measure(ctx, args, prec, weights_cached):
     # sustained one.  MXFP8 has no measured peak: bf16's measured burst figure times the
     # nominal 2x ratio of the dense MXFP8 and bf16 tensor rates
     peak = peaks["bf16_tflops"] * (2.0 if mx8 else 1.0)
-    src = (f"{peak_src} bf16_tflops (burst) x 2, the nominal MXFP8/bf16 ratio" if mx8 else
+    src = (f"{peak_src} bf16_tflops (burst) x 2, the nominal MXFP8/bf16 ratio (FP8 x FP4 runs the same "
+           f"MMA kind at the same rate)" if prec == "mxfp8-w4" else
+           f"{peak_src} bf16_tflops (burst) x 2, the nominal MXFP8/bf16 ratio" if mx8 else
            f"{peak_src} bf16_tflops (burst: the timed region lasts {args.steps * ms / 1e3:.2f} s)")
     return {
         "value": value, "ms_per_step": ms, "tokens_per_s": world * cfg.T / (ms * 1e-3),
-        "dtype": "e4m3+e8m0 (MXFP8), fp32 acc" if mx8 else "bf16",
+        "dtype": ("e4m3 x e2m1, e8m0 scales (MXFP8 x MXFP4), fp32 acc" if prec == "mxfp8-w4" else
+                  "e4m3+e8m0 (MXFP8), fp32 acc" if mx8 else "bf16"),
         "precision": prec,
         "frac_of_peak": value / world / peak,
         "roofline": {"bound": "tensor", "kernel": f"{dom} ({(GEMM_KERNEL_MX if mx8 else GEMM_KERNEL)[dom]})",
@@ -774,8 +782,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="dsv3")
-    ap.add_argument("--prec", default="bf16", choices=["bf16", "mxfp8"])
-    ap.add_argument("--second-prec", default="mxfp8", choices=["bf16", "mxfp8", "none"],
+    ap.add_argument("--prec", default="bf16", choices=["bf16", "mxfp8", "mxfp8-w4"],
+                    help="mxfp8-w4: FP8 x FP4 experts (MXFP8 activations, MXFP4 weights)")
+    ap.add_argument("--second-prec", default="mxfp8", choices=["bf16", "mxfp8", "mxfp8-w4", "none"],
                     help="also measure the same workload in this precision and report it in the same line "
                          "under its name (per-step weight quantisation); 'none' or the headline's own "
                          "precision skips it")
@@ -786,7 +795,7 @@ def main():
                     help="MXFP8: quantise the weights once before timing (one optimiser step shared by "
                          "micro-batches) instead of in every timed step")
     args = ap.parse_args()
-    if args.weights_cached and args.prec != "mxfp8":
+    if args.weights_cached and args.prec not in MX_PRECS:
         ap.error("--weights-cached applies to --prec mxfp8")
     from dropless_mixture_experts_warp_gb300 import synth
     cfg = synth.CONFIGS[args.config]

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_INVARIANT",
                 8: "MOE_ERR_SCRATCH_LIMIT"}
 SCORE = {"softmax": 0, "sigmoid": 1}
-PREC = {"bf16": 0, "mxfp8": 1}
+PREC = {"bf16": 0, "mxfp8": 1, "mxfp8-w4": 2}
 
 
 class MoeError(RuntimeError):
@@ -94,6 +94,10 @@ SIGNATURES = {
     "moe_gemm_down_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 5),
     "moe_gemm_gate_up_dgrad_mx": (ctypes.c_int32, [_D] + [_P] * 6),
     "moe_gemm_gate_up_wgrad_mx": (ctypes.c_int32, [_D] + [_P] * 5),
+    "moe_gemm_mxf8f4": (ctypes.c_int32, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_mx4_quantize_cols": (ctypes.c_int32, [_P, _I, ctypes.c_int64, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_mlp_fwd_mx": (ctypes.c_int32, [_D] + [_P] * 7),
+    "moe_grouped_mlp_bwd_mx": (ctypes.c_int32, [_D] + [_P] * 11),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -357,6 +361,29 @@ def moe_gemm_gate_up_dgrad_mx(dims, row_offsets, wq, mx_ws, dxp, dev_status, str
 def moe_gemm_gate_up_wgrad_mx(dims, row_offsets, mx_ws, dw_gu, dev_status, stream=None):
     return _call("moe_gemm_gate_up_wgrad_mx", _d(dims), _ptr(row_offsets), _ptr(mx_ws), _ptr(dw_gu),
                  _ptr(dev_status), _stream(stream))
+
+
+def moe_gemm_mxf8f4(a, a_sf, b4, b_sf, c, M, N, K, dev_status, stream=None):
+    return _call("moe_gemm_mxf8f4", _ptr(a), _ptr(a_sf), _ptr(b4), _ptr(b_sf), _ptr(c), M, N, K, _ptr(dev_status),
+                 _stream(stream))
+
+
+def moe_mx4_quantize_cols(src, batch, rows, C, codes_t, scales_t, codes, scales, stream=None):
+    return _call("moe_mx4_quantize_cols", _ptr(src), batch, rows, C, _ptr(codes_t), _ptr(scales_t), _ptr(codes),
+                 _ptr(scales), _stream(stream))
+
+
+def moe_grouped_mlp_fwd_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, y_rows, dev_status, stream=None):
+    return _call("moe_grouped_mlp_fwd_mx", _d(dims), _ptr(row_offsets), _ptr(w_rows), _ptr(wq), _ptr(mx_ws),
+                 _ptr(gu), _ptr(y_rows), _ptr(dev_status), _stream(stream))
+
+
+def moe_grouped_mlp_bwd_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dxp, dw_gu, dw_d, dw_rows, workspace,
+                           dev_status, stream=None):
+    return _call("moe_grouped_mlp_bwd_mx", _d(dims), _ptr(row_offsets), _ptr(w_rows), _ptr(wq), _ptr(mx_ws),
+                 _ptr(gu), _ptr(dxp), _ptr(dw_gu), _ptr(dw_d), _ptr(dw_rows), _ptr(workspace), _ptr(dev_status),
+                 _stream(stream))
+
 
 def moe_mx_shared_weights_size(dims) -> int:
     return lib().moe_mx_shared_weights_size(_d(dims))

@@ -83,6 +83,21 @@ bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed E2M1 codes [outer][inner / 2] bytes (inner in elements): every 16 codes (8 bytes)
+// land in 16 bytes of shared memory, so a 128-element row of the box fills 128 bytes laid
+// out as an E4M3 row; 128B swizzle, box 128 elements x box_outer rows.
+bool make_tensor_map_fp4(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner / 2};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same encoder, for the other translation units of the library.
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer) {
@@ -202,8 +217,8 @@ moe_status moe_check_dims(const moe_dims* dims) {
     return MOE_ERR_INVALID_ARG;
   if (d.k > d.E || d.k > 32) return MOE_ERR_INVALID_ARG;
   if (d.score != MOE_SCORE_SOFTMAX && d.score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-  if (d.prec != MOE_PREC_BF16 && d.prec != MOE_PREC_MXFP8) return MOE_ERR_INVALID_ARG;
-  if (d.prec == MOE_PREC_MXFP8 && (d.f % 128 != 0 || d.f_shared % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (d.prec != MOE_PREC_BF16 && d.prec != MOE_PREC_MXFP8 && d.prec != MOE_PREC_MXFP8_W4) return MOE_ERR_INVALID_ARG;
+  if (d.prec != MOE_PREC_BF16 && (d.f % 128 != 0 || d.f_shared % 128 != 0)) return MOE_ERR_UNSUPPORTED;
   if (d.E > MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
   if (d.d % 128 != 0 || d.f % 64 != 0 || d.f_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (row_capacity(d) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;

@@ -49,6 +49,34 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_gemm_mxf8f4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b4, const uint8_t* b_sf,
+                           moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream) {
+  if (!a || !a_sf || !b4 || !b_sf || !c || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (M < 128 || N < 128 || K < 128 || M % 128 || N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!al16(a) || !al16(c) || !al16(a_sf) || !al16(b_sf)) return MOE_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(b4) & 31u) return MOE_ERR_ALIGNMENT;   // 4-bit tensor loads want 32 bytes
+  const int bn = N % 256 == 0 ? 256 : 128;
+  const MxMat ma{a, a_sf, static_cast<uint64_t>(K), static_cast<uint64_t>(M), false};
+  const MxMat mb{b4, b_sf, static_cast<uint64_t>(K), static_cast<uint64_t>(N), true};
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.BN = bn; p.N = N; p.K = K; p.M = M; p.E = 1; p.row_offsets = nullptr; p.m_fastest = 1;
+  p.out = c; p.ldo = N; p.row_limit = M; p.status = dev_status;
+  p.a_sf_ktiles = K / 128; p.b_sf_ktiles = K / 128;
+  return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_mx4_quantize_cols(const moe_bf16* src, int32_t batch, int64_t rows, int32_t C, uint8_t* codes_t,
+                                 uint8_t* scales_t, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (batch < 0 || rows < 0 || C <= 0) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || C % 128) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0 || batch == 0) return MOE_OK;
+  if (!src || !codes_t || !scales_t || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  if (!al16(src) || !al16(codes_t) || !al16(codes) || !al16(scales_t) || !al16(scales)) return MOE_ERR_ALIGNMENT;
+  return cuda_st(launch_quant_cols_t(src, batch, rows, C, nullptr, codes_t, scales_t,
+                                     static_cast<cudaStream_t>(stream), nullptr, codes, scales, true));
+}
+
 }  // extern "C"
 
 // ============================================================================ layer path
@@ -64,19 +92,27 @@ struct MxOp {
   uint8_t* sf;
 };
 
-static size_t op_bytes(size_t elems) { return a256(elems) + a256(elems / 32); }
+static size_t op_bytes(size_t elems, bool fp4 = false) { return a256(fp4 ? elems / 2 : elems) + a256(elems / 32); }
 
-static MxOp carve_op(uint8_t*& p, size_t elems) {
+static MxOp carve_op(uint8_t*& p, size_t elems, bool fp4 = false) {
   MxOp o;
   o.codes = p;
-  p += a256(elems);
+  p += a256(fp4 ? elems / 2 : elems);
   o.sf = p;
   p += a256(elems / 32);
   return o;
 }
 
+// FP8 x FP4 experts: the weights are E2M1 codes (MXFP4), the activations stay E4M3.
+static bool w4(const moe_dims& d) { return d.prec == MOE_PREC_MXFP8_W4; }
+// Quantised weights are read by 4-bit tensor loads (FP4) that want 32-byte alignment.
+static bool wq_aligned(const moe_dims& d, const void* wq) {
+  return (reinterpret_cast<uintptr_t>(wq) & (w4(d) ? 31u : 15u)) == 0;
+}
+
 // Quantised weights: W_gu along d ([E*2f][d]), W_gu along 2f ([E][d][2f]),
-// W_d along f ([E*d][f]), W_d along d ([E][f][d]).
+// W_d along f ([E*d][f]), W_d along d ([E][f][d]); E2M1 codes packed two a byte when
+// the weights are FP4.
 struct MxWeights {
   MxOp gu_rows, gu_cols, d_rows, d_cols;
 };
@@ -85,11 +121,12 @@ static MxWeights carve_weights(const moe_dims& d, void* base) {
   uint8_t* p = static_cast<uint8_t*>(base);
   const size_t n = static_cast<size_t>(d.E) * 2 * d.f * d.d;
   const size_t m = static_cast<size_t>(d.E) * d.f * d.d;
+  const bool f4 = w4(d);
   MxWeights w;
-  w.gu_rows = carve_op(p, n);
-  w.gu_cols = carve_op(p, n);
-  w.d_rows = carve_op(p, m);
-  w.d_cols = carve_op(p, m);
+  w.gu_rows = carve_op(p, n, f4);
+  w.gu_cols = carve_op(p, n, f4);
+  w.d_rows = carve_op(p, m, f4);
+  w.d_cols = carve_op(p, m, f4);
   return w;
 }
 
@@ -113,8 +150,8 @@ static MxActs carve_acts(const moe_dims& d, int64_t R_cap, void* base) {
   return a;
 }
 
-static MxMat mat(const MxOp& o, int64_t inner, int64_t outer) {
-  return MxMat{o.codes, o.sf, static_cast<uint64_t>(inner), static_cast<uint64_t>(outer)};
+static MxMat mat(const MxOp& o, int64_t inner, int64_t outer, bool fp4 = false) {
+  return MxMat{o.codes, o.sf, static_cast<uint64_t>(inner), static_cast<uint64_t>(outer), fp4};
 }
 
 static moe_status mx_common(const moe_dims* dims) {
@@ -138,7 +175,7 @@ size_t moe_mx_weights_size(const moe_dims* dims) {
   if (mx_common(dims) != MOE_OK) return 0;
   const size_t n = static_cast<size_t>(dims->E) * 2 * dims->f * dims->d;
   const size_t m = static_cast<size_t>(dims->E) * dims->f * dims->d;
-  return 2 * op_bytes(n) + 2 * op_bytes(m);
+  return 2 * op_bytes(n, w4(*dims)) + 2 * op_bytes(m, w4(*dims));
 }
 
 size_t moe_mx_workspace_size(const moe_dims* dims) {
@@ -154,14 +191,14 @@ moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, c
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!w_gu || !w_d || !wq) return MOE_ERR_INVALID_ARG;
-  if (!al16(w_gu) || !al16(w_d) || !al16(wq)) return MOE_ERR_ALIGNMENT;
+  if (!al16(w_gu) || !al16(w_d) || !wq_aligned(d, wq)) return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, wq);
   // one read of each weight: column-wise codes per expert and row-wise codes of the same tiles
   if (launch_quant_cols_t(w_gu, d.E, 2ll * d.f, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s, nullptr,
-                          w.gu_rows.codes, w.gu_rows.sf) != cudaSuccess ||
+                          w.gu_rows.codes, w.gu_rows.sf, w4(d)) != cudaSuccess ||
       launch_quant_cols_t(w_d, d.E, d.d, d.f, nullptr, w.d_cols.codes, w.d_cols.sf, s, nullptr, w.d_rows.codes,
-                          w.d_rows.sf) != cudaSuccess)
+                          w.d_rows.sf, w4(d)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -214,12 +251,12 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets,
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!row_offsets || !w_rows || !wq || !mx_ws || !gu || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
+  if (!wq_aligned(d, wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   MxMat ma = mat(a.xp_rows, d.d, R_cap);
-  MxMat mb = mat(w.gu_rows, d.d, 2ll * d.f * d.E);
+  MxMat mb = mat(w.gu_rows, d.d, 2ll * d.f * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = 256; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = 2 * d.f;
   p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
@@ -236,13 +273,13 @@ moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, co
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!row_offsets || !wq || !mx_ws || !y_rows || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(wq) || !al16(mx_ws) || !al16(y_rows)) return MOE_ERR_ALIGNMENT;
+  if (!wq_aligned(d, wq) || !al16(mx_ws) || !al16(y_rows)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   const int bn = bn_mx(d.d);
   MxMat ma = mat(a.h_rows, d.f, R_cap);
-  MxMat mb = mat(w.d_rows, d.f, static_cast<uint64_t>(d.d) * d.E);
+  MxMat mb = mat(w.d_rows, d.f, static_cast<uint64_t>(d.d) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
@@ -258,7 +295,7 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   const moe_dims& d = *dims;
   if (!row_offsets || !w_rows || !wq || !mx_ws || !gu || !dw_rows || !dev_status) return MOE_ERR_INVALID_ARG;
   if (!workspace) return MOE_ERR_WORKSPACE;
-  if (!al16(wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
+  if (!wq_aligned(d, wq) || !al16(mx_ws) || !al16(gu)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
@@ -266,7 +303,7 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   float* dw_part = workspace_dw_part(d, workspace);
   const int bn = bn_mx(d.f);
   MxMat ma = mat(a.dy_rows, d.d, R_cap);
-  MxMat mb = mat(w.d_cols, d.d, static_cast<uint64_t>(d.f) * d.E);
+  MxMat mb = mat(w.d_cols, d.d, static_cast<uint64_t>(d.f) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.f;
   p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
@@ -305,13 +342,13 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_of
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!row_offsets || !wq || !mx_ws || !dxp || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(wq) || !al16(mx_ws) || !al16(dxp)) return MOE_ERR_ALIGNMENT;
+  if (!wq_aligned(d, wq) || !al16(mx_ws) || !al16(dxp)) return MOE_ERR_ALIGNMENT;
   const int64_t R_cap = moe_row_capacity(dims), R = static_cast<int64_t>(d.T) * d.k;
   MxWeights w = carve_weights(d, const_cast<void*>(wq));
   MxActs a = carve_acts(d, R_cap, mx_ws);
   const int bn = bn_mx(d.d);
   MxMat ma = mat(a.dgu_rows, 2ll * d.f, R_cap);
-  MxMat mb = mat(w.gu_cols, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E);
+  MxMat mb = mat(w.gu_cols, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
   p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
@@ -341,6 +378,34 @@ moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const int32_t* row_of
   return cuda_st(launch_gemm_mx(GEMM_KGROUP_STORE, ma, mb, p, s));
 }
 
+// Steps 3-5 and their backward as one call each, MXFP8 operands: the per-GEMM calls above
+// in order (the composites of moe_grouped_mlp_fwd / moe_grouped_mlp_bwd).
+moe_status moe_grouped_mlp_fwd_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* y_rows, int32_t* dev_status,
+                                  void* stream) {
+  if (!y_rows) return MOE_ERR_INVALID_ARG;   // checked before anything is enqueued
+  if (!al16(y_rows)) return MOE_ERR_ALIGNMENT;
+  moe_status st = moe_gemm_gate_up_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dev_status, stream);
+  if (st != MOE_OK) return st;
+  return moe_gemm_down_mx(dims, row_offsets, wq, mx_ws, y_rows, dev_status, stream);
+}
+
+moe_status moe_grouped_mlp_bwd_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, const moe_bf16* gu, moe_bf16* dxp, moe_bf16* dw_gu,
+                                  moe_bf16* dw_d, float* dw_rows, void* workspace, int32_t* dev_status,
+                                  void* stream) {
+  if (!dxp || !dw_gu || !dw_d) return MOE_ERR_INVALID_ARG;   // checked before anything is enqueued
+  if (!al16(dxp) || !al16(dw_gu) || !al16(dw_d)) return MOE_ERR_ALIGNMENT;
+  moe_status st = moe_gemm_down_dgrad_mx(dims, row_offsets, w_rows, wq, mx_ws, gu, dw_rows, workspace, dev_status,
+                                         stream);
+  if (st != MOE_OK) return st;
+  st = moe_gemm_down_wgrad_mx(dims, row_offsets, mx_ws, dw_d, dev_status, stream);
+  if (st != MOE_OK) return st;
+  st = moe_gemm_gate_up_dgrad_mx(dims, row_offsets, wq, mx_ws, dxp, dev_status, stream);
+  if (st != MOE_OK) return st;
+  return moe_gemm_gate_up_wgrad_mx(dims, row_offsets, mx_ws, dw_gu, dev_status, stream);
+}
+
 }  // extern "C"
 
 // ============================================================================ shared expert
@@ -352,11 +417,12 @@ namespace moe {
 static MxWeights carve_shared_weights(const moe_dims& d, void* base) {
   uint8_t* p = static_cast<uint8_t*>(base);
   const size_t n = 2ull * d.f_shared * d.d, m = static_cast<size_t>(d.f_shared) * d.d;
+  const bool f4 = w4(d);
   MxWeights w;
-  w.gu_rows = carve_op(p, n);
-  w.gu_cols = carve_op(p, n);
-  w.d_rows = carve_op(p, m);
-  w.d_cols = carve_op(p, m);
+  w.gu_rows = carve_op(p, n, f4);
+  w.gu_cols = carve_op(p, n, f4);
+  w.d_rows = carve_op(p, m, f4);
+  w.d_cols = carve_op(p, m, f4);
   return w;
 }
 
@@ -391,7 +457,7 @@ extern "C" {
 size_t moe_mx_shared_weights_size(const moe_dims* dims) {
   if (mx_shared_common(dims) != MOE_OK) return 0;
   const size_t n = 2ull * dims->f_shared * dims->d, m = static_cast<size_t>(dims->f_shared) * dims->d;
-  return 2 * op_bytes(n) + 2 * op_bytes(m);
+  return 2 * op_bytes(n, w4(*dims)) + 2 * op_bytes(m, w4(*dims));
 }
 
 size_t moe_mx_shared_workspace_size(const moe_dims* dims) {
@@ -406,14 +472,14 @@ moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* 
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!w_gu_s || !w_d_s || !wq_s) return MOE_ERR_INVALID_ARG;
-  if (!al16(w_gu_s) || !al16(w_d_s) || !al16(wq_s)) return MOE_ERR_ALIGNMENT;
+  if (!al16(w_gu_s) || !al16(w_d_s) || !wq_aligned(d, wq_s)) return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, wq_s);
   const int fs = d.f_shared;
   if (launch_quant_cols_t(w_gu_s, 1, 2ll * fs, d.d, nullptr, w.gu_cols.codes, w.gu_cols.sf, s, nullptr,
-                          w.gu_rows.codes, w.gu_rows.sf) != cudaSuccess ||
+                          w.gu_rows.codes, w.gu_rows.sf, w4(d)) != cudaSuccess ||
       launch_quant_cols_t(w_d_s, 1, d.d, fs, nullptr, w.d_cols.codes, w.d_cols.sf, s, nullptr, w.d_rows.codes,
-                          w.d_rows.sf) != cudaSuccess)
+                          w.d_rows.sf, w4(d)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -425,7 +491,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   const moe_dims& d = *dims;
   if (d.T == 0) return MOE_OK;
   if (!x || !wq_s || !mx_ws_s || !gu_s || !y_s || !dev_status) return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(y_s)) return MOE_ERR_ALIGNMENT;
+  if (!al16(x) || !wq_aligned(d, wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(y_s)) return MOE_ERR_ALIGNMENT;
   const int fs = d.f_shared, T = d.T;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MxWeights w = carve_shared_weights(d, const_cast<void*>(wq_s));
@@ -437,7 +503,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
                           a.xp_rows.sf) != cudaSuccess)
     return MOE_ERR_CUDA;
   ma = mat(a.xp_rows, d.d, T);
-  mb = mat(w.gu_rows, d.d, 2ll * fs);
+  mb = mat(w.gu_rows, d.d, 2ll * fs, w4(d));
   p = mx_params();
   p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1; p.f = fs;
   p.row_limit = T; p.gu_out = gu_s; p.status = dev_status;
@@ -447,7 +513,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
   ma = mat(a.h_rows, fs, T);
-  mb = mat(w.d_rows, fs, d.d);
+  mb = mat(w.d_rows, fs, d.d, w4(d));
   p = mx_params();
   p.BN = bn; p.N = d.d; p.K = fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
   p.out = y_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
@@ -471,7 +537,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
     return MOE_OK;
   }
   if (!mx_ws_s || !gu_s || !dy || !dx_s) return MOE_ERR_INVALID_ARG;
-  if (!al16(wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(dy) || !al16(dx_s) || !al16(dw_gu_s) ||
+  if (!wq_aligned(d, wq_s) || !al16(mx_ws_s) || !al16(gu_s) || !al16(dy) || !al16(dx_s) || !al16(dw_gu_s) ||
       !al16(dw_d_s))
     return MOE_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -485,7 +551,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
     return MOE_ERR_CUDA;
   int bn = bn_mx(fs);
   ma = mat(a.dy_rows, d.d, T);
-  mb = mat(w.d_cols, d.d, fs);
+  mb = mat(w.d_cols, d.d, fs, w4(d));
   p = mx_params();
   p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = 1; p.f = fs;
   p.row_limit = T; p.gu_in = gu_s; p.status = dev_status;
@@ -504,7 +570,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
   // dx_s = dgu_s W_gu_s (K = 2fs)
   bn = bn_mx(d.d);
   ma = mat(a.dgu_rows, 2ll * fs, T);
-  mb = mat(w.gu_cols, 2ll * fs, d.d);
+  mb = mat(w.gu_cols, 2ll * fs, d.d, w4(d));
   p = mx_params();
   p.BN = bn; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
   p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;

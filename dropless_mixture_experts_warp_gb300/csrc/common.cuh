@@ -251,8 +251,10 @@ __device__ __forceinline__ size_t sf_byte_offset(long long r, long long k, long 
   return static_cast<size_t>(tile) * 512 + word * 4 + static_cast<int>((k & 127) >> 5);
 }
 
-// floor(log2(a)) - 8 clamped to [-127, 127] for a finite a >= 0 (-127 for a = 0).
-__device__ __forceinline__ int mx_scale_exp(float a) {
+// floor(log2(a)) - EMAX clamped to [-127, 127] for a finite a >= 0 (-127 for a = 0);
+// EMAX is the element format's largest exponent (8 for E4M3, 2 for E2M1).
+template <int EMAX>
+__device__ __forceinline__ int mx_scale_exp_t(float a) {
   const uint32_t b = __float_as_uint(a);
   const int ef = static_cast<int>((b >> 23) & 0xFF);
   int fl;
@@ -263,8 +265,9 @@ __device__ __forceinline__ int mx_scale_exp(float a) {
     if (m == 0) return -127;
     fl = (31 - __clz(m)) - 149;
   }
-  return max(-127, min(127, fl - 8));
+  return max(-127, min(127, fl - EMAX));
 }
+__device__ __forceinline__ int mx_scale_exp(float a) { return mx_scale_exp_t<8>(a); }
 
 // 2^-e as an fp32 for e in [-127, 127] (2^-127 .. 2^127; 2^-127 is subnormal).
 __device__ __forceinline__ float exp2_neg(int e) {
@@ -312,6 +315,49 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
     mul_f32x2(x0, x1, ss);
     mul_f32x2(x2, x3, ss);
     codes[w] = cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16);
+  }
+  return static_cast<uint32_t>(e + 127);
+}
+
+// Eight fp32 -> eight E2M1 (FP4) codes in one word, element i in bits 4i..4i+3: round to
+// nearest even, saturating at +-6 (hardware cvt; the first source of each cvt goes to
+// the upper four bits of its byte).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float x0, float x1, float x2, float x3, float x4, float x5,
+                                               float x6, float x7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(x4), "f"(x5), "f"(x6), "f"(x7));
+  return r;
+}
+
+// One 32-element block as E2M1 codes (16 bytes, two codes a byte, the lower element in
+// the lower four bits) with its E8M0 scale byte, returned: the OCP MX rule with E2M1's
+// largest exponent, e = floor(log2(amax)) - 2.
+__device__ __forceinline__ uint32_t quant_block32_e2m1(const float (&v)[32], uint32_t (&codes)[4]) {
+  float m[11];
+#pragma unroll
+  for (int j = 0; j < 10; ++j) m[j] = absmax3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+  m[10] = absmax3(v[30], v[31], v[31]);
+  const float n0 = absmax3(m[0], m[1], m[2]), n1 = absmax3(m[3], m[4], m[5]);
+  const float n2 = absmax3(m[6], m[7], m[8]), n3 = absmax3(m[9], m[10], m[10]);
+  const float amax = absmax3(absmax3(n0, n1, n2), n3, n3);
+  const int e = mx_scale_exp_t<2>(amax);
+  const uint32_t sb = __float_as_uint(exp2_neg(e));
+  const uint64_t ss = (static_cast<uint64_t>(sb) << 32) | sb;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = v[8 * w + i];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) mul_f32x2(x[i], x[i + 1], ss);
+    codes[w] = cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
   }
   return static_cast<uint32_t>(e + 127);
 }
@@ -431,13 +477,16 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Instruction descriptor for kind::mxf8f6f4 with E4M3 A/B, UE8M0 scales, fp32 D:
-//   bits 4-5 B scale-factor id, 7-9 A format (0 = E4M3), 10-12 B format, 15/16
-//   majorness (0 = K-major), 17-22 N>>3, bit 23 scale type (1 = UE8M0), 24-28 M>>4,
-//   29-30 A scale-factor id (which byte of each 32-bit scale word).
-__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
-  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-         (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+// Instruction descriptor for kind::mxf8f6f4 with an E4M3 A, UE8M0 scales, fp32 D:
+//   bits 4-5 B scale-factor id, 7-9 A format (0 = E4M3), 10-12 B format (0 = E4M3,
+//   5 = E2M1), 15/16 majorness (0 = K-major), 17-22 N>>3, bit 23 scale type (1 =
+//   UE8M0), 24-28 M>>4, 29-30 A scale-factor id (which byte of each 32-bit scale word).
+constexpr int MX_FMT_E4M3 = 0;
+constexpr int MX_FMT_E2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id, int b_fmt = MX_FMT_E4M3) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(b_fmt) << 10) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         (static_cast<uint32_t>(sf_id) << 29);
 }
 
 }  // namespace moe

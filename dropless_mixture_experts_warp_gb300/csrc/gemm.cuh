@@ -82,6 +82,7 @@ struct GemmParams {
   const uint8_t* sfb;
   int a_sf_ktiles;
   int b_sf_ktiles;
+  int b_fmt;                    // B element format: MX_FMT_E4M3 (0) or MX_FMT_E2M1 (FP4 weights)
   // fused MXFP8 outputs of the *_MX epilogues: row-wise codes [rows][width] with SF
   // tiles (K = width), and column-wise codes [width][q_cols_ld] with SF tiles
   // (K = rows, q_cols_ktiles = q_cols_ld / 128); width = f (h) or 2f (dG|dU)

@@ -27,9 +27,14 @@ cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmPa
   // B box: the gate (or up) half of the BN rows for the split epilogue, else BN
   const int b_box = split ? p.BN / 2 : p.BN;
   CUtensorMap ta, tb, tc;
-  if (!make_tensor_map_u8(&ta, a.codes, a.inner, a.outer, 128, BM) ||
-      !make_tensor_map_u8(&tb, b.codes, b.inner, b.outer, 128, b_box))
-    return cudaErrorInvalidValue;
+  if (a.fp4 || !make_tensor_map_u8(&ta, a.codes, a.inner, a.outer, 128, BM)) return cudaErrorInvalidValue;
+  if (b.fp4) {  // E2M1 weights: 4-bit codes, MMA B format E2M1
+    if (!make_tensor_map_fp4(&tb, b.codes, b.inner, b.outer, b_box)) return cudaErrorInvalidValue;
+    p.b_fmt = MX_FMT_E2M1;
+  } else {
+    if (!make_tensor_map_u8(&tb, b.codes, b.inner, b.outer, 128, b_box)) return cudaErrorInvalidValue;
+    p.b_fmt = MX_FMT_E4M3;
+  }
   tc = ta;
   if (kind == GEMM_ROWS_SWIGLU_BWD_MXQ && p.BN == 256) {  // the SwiGLU' epilogue reads G|U by tensor loads
     if (!p.gu_in || (reinterpret_cast<uintptr_t>(p.gu_in) & 15u) || p.f % 32 != 0) return cudaErrorInvalidValue;

@@ -2,7 +2,9 @@
 //
 // Same roles and schedule as the bf16 kernel (gemm.cuh): warp 0 loads, warp 1 issues,
 // the warps after them run the shared epilogue.  Differences:
-//   * operands are E4M3 codes, both K-major, 128 codes (128 bytes) per stage row;
+//   * operands are E4M3 codes, both K-major, 128 codes (128 bytes) per stage row; B may
+//     instead hold E2M1 codes (FP4 weights), packed two a byte in memory and spread by
+//     the tensor load to the same 128 bytes a row in shared memory;
 //   * each stage also has the E8M0 scale tiles of its A rows (512 B) and B rows
 //     (512 B per 128 rows), fetched with contiguous bulk copies into a region after
 //     the code stages; the MMA warp moves
@@ -39,6 +41,9 @@ __host__ __device__ constexpr int mx_smem_bytes(int epi) {
   return MX_XBUF_OFF + (epi_quantises(epi) ? mx_epi_warps(epi) * XBUF_FLOATS * 4 : 0) +
          (epi == 0 ? mx_epi_warps(epi) * 2048 : 0) + 1024;
 }
+// Bytes a TMA load of one 128-element E2M1 row counts on its mbarrier: the 128 bytes it
+// fills in shared memory (16 codes in 8 bytes, then 8 bytes of gap), not the 64 it reads.
+constexpr int MX_W4_TX_ROW_BYTES = 128;
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
 // BN = 256 (four stages): the TMEM columns after the scale factors hold accumulator
@@ -116,7 +121,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t stage_tx = MX_A_BYTES + BN * MX_BK + 512 + (BN / 128) * 512;
+      const uint32_t b_row_tx = p.b_fmt == MX_FMT_E2M1 ? MX_W4_TX_ROW_BYTES : MX_BK;
+      const uint32_t stage_tx = MX_A_BYTES + BN * b_row_tx + 512 + (BN / 128) * 512;
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
           for (int kk = 0; kk < MX_BK / 32; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, kk, p.b_fmt), sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == stages) { stage = 0; phase ^= 1; }

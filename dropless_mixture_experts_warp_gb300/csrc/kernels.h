@@ -100,11 +100,13 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const
   return cudaGetLastError();
 }
 
-// One MXFP8 operand, K-major: E4M3 codes [outer][inner] (inner = K) and their SF tiles.
+// One MXFP8 operand, K-major: E4M3 codes [outer][inner] (inner = K) and their SF tiles;
+// fp4 (B operands only): E2M1 codes packed two a byte ([outer][inner / 2] bytes).
 struct MxMat {
   const uint8_t* codes;
   const uint8_t* sf;
   uint64_t inner, outer;
+  bool fp4;
 };
 // MXFP8 grouped GEMM; kind is one of GEMM_ROWS_STORE, GEMM_KGROUP_STORE,
 // GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  p.sfa/p.sfb are taken from a
@@ -118,7 +120,7 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map = nullptr,
-                                uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr);
+                                uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr, bool fp4 = false);
 RouteScratch route_scratch(const moe_dims& d, void* ws);
 float* workspace_dw_part(const moe_dims& d, void* ws);
 bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);
@@ -126,6 +128,10 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint
                           uint32_t box_inner, uint32_t box_outer);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
+// Packed 4-bit codes [outer][inner / 2] bytes loaded as 16-element groups padded to 16
+// bytes in shared memory (the layout the block-scaled MMA reads for E2M1 under
+// kind::mxf8f6f4), 128B swizzle; box_inner must be 128 elements.
+bool make_tensor_map_fp4(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer);
 
 template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,

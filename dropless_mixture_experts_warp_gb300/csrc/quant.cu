@@ -70,6 +70,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 // codes of a tile and its scales (exactly one 512-byte SF tile per orientation) are
 // assembled in shared memory and leave as whole 128-byte lines.  Column blocks are
 // read two columns at a time (32-bit shared loads), row blocks 16 bytes at a time.
+// FP4 = true writes E2M1 codes instead (MXFP4 weights of FP8 x FP4 experts): two codes
+// a byte, the lower element in the lower four bits, lines of 64 bytes, the scale rule
+// with E2M1's largest exponent; the SF tiles are laid out as for E4M3.
 constexpr int QC_IN_LD = 128 + 8;  // padded bf16 input rows
 constexpr int QC_LD = 128 + 16;    // padded code rows (bytes)
 constexpr int QC_IN_BYTES = 128 * QC_IN_LD * 2;
@@ -83,6 +86,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+template <bool FP4>
 __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __restrict__ src, int batch,
                                                            long long rows, int C,
                                                            const int32_t* __restrict__ nrows_dev,
@@ -158,18 +162,28 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
         v0[i] = bf16_lo(w);
         v1[i] = bf16_hi(w);
       }
-      uint32_t w[8];
-      uint32_t sb = quant_block32(v0, w);
       // ct line cp holds column 2 cp, line 64 + cp column 2 cp + 1 (no bank conflicts)
-      uint4* d4 = reinterpret_cast<uint4*>(ct + cp * QC_LD + g * 32);
-      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sft[sf_byte_offset(2 * cp, g * 32, 1)] = static_cast<uint8_t>(sb);
-      sb = quant_block32(v1, w);
-      d4 = reinterpret_cast<uint4*>(ct + (64 + cp) * QC_LD + g * 32);
-      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sft[sf_byte_offset(2 * cp + 1, g * 32, 1)] = static_cast<uint8_t>(sb);
+      if constexpr (FP4) {
+        uint32_t w[4];
+        uint32_t sb = quant_block32_e2m1(v0, w);
+        *reinterpret_cast<uint4*>(ct + cp * QC_LD + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        sft[sf_byte_offset(2 * cp, g * 32, 1)] = static_cast<uint8_t>(sb);
+        sb = quant_block32_e2m1(v1, w);
+        *reinterpret_cast<uint4*>(ct + (64 + cp) * QC_LD + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        sft[sf_byte_offset(2 * cp + 1, g * 32, 1)] = static_cast<uint8_t>(sb);
+      } else {
+        uint32_t w[8];
+        uint32_t sb = quant_block32(v0, w);
+        uint4* d4 = reinterpret_cast<uint4*>(ct + cp * QC_LD + g * 32);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        sft[sf_byte_offset(2 * cp, g * 32, 1)] = static_cast<uint8_t>(sb);
+        sb = quant_block32(v1, w);
+        d4 = reinterpret_cast<uint4*>(ct + (64 + cp) * QC_LD + g * 32);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        sft[sf_byte_offset(2 * cp + 1, g * 32, 1)] = static_cast<uint8_t>(sb);
+      }
     }
     if (codes_rows) {
       // row-wise codes of the same tile: thread t takes row t % 128, columns 64 (t / 128)
@@ -190,23 +204,32 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
             v[q * 8 + 2 * i + 1] = bf16_hi(ww[i]);
           }
         }
-        uint32_t w[8];
-        const uint32_t sb = quant_block32(v, w);
-        uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+        if constexpr (FP4) {
+          uint32_t w[4];
+          const uint32_t sb = quant_block32_e2m1(v, w);
+          *reinterpret_cast<uint4*>(rt + rr * QC_LD + (cc + blk * 32) / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+          sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+        } else {
+          uint32_t w[8];
+          const uint32_t sb = quant_block32(v, w);
+          uint4* d4 = reinterpret_cast<uint4*>(rt + rr * QC_LD + cc + blk * 32);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          sft[512 + sf_byte_offset(rr, cc + blk * 32, 1)] = static_cast<uint8_t>(sb);
+        }
       }
     }
     __syncthreads();
-    // column-wise codes: 128 lines of 128 bytes at codes + (c0 + column) * rows + r0
-    uint8_t* cb = codes + b * static_cast<long long>(C) * rows;
+    // column-wise codes: 128 lines of 128 (FP4: 64) bytes at codes + ((c0 + column) * rows + r0) / EPB
+    constexpr int EPB = FP4 ? 2 : 1;      // elements per code byte
+    constexpr int QPL = 8 / EPB;          // 16-byte pieces per line
+    uint8_t* cb = codes + b * static_cast<long long>(C) * rows / EPB;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 4 / EPB; ++j) {
       const int i = threadIdx.x + 256 * j;
-      const int line = i >> 3, q = i & 7;
+      const int line = i / QPL, q = i % QPL;
       const int col = line < 64 ? 2 * line : 2 * (line - 64) + 1;
-      *reinterpret_cast<uint4*>(cb + static_cast<long long>(c0 + col) * rows + r0 + q * 16) =
+      *reinterpret_cast<uint4*>(cb + (static_cast<long long>(c0 + col) * rows + r0) / EPB + q * 16) =
           *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
     }
     if (threadIdx.x < 32) {
@@ -216,10 +239,10 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
     if (codes_rows) {
       const long long grow0 = b * rows + r0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 4 / EPB; ++j) {
         const int i = threadIdx.x + 256 * j;
-        const int line = i >> 3, q = i & 7;
-        *reinterpret_cast<uint4*>(codes_rows + (grow0 + line) * C + c0 + q * 16) =
+        const int line = i / QPL, q = i % QPL;
+        *reinterpret_cast<uint4*>(codes_rows + ((grow0 + line) * C + c0) / EPB + q * 16) =
             *reinterpret_cast<const uint4*>(rt + line * QC_LD + q * 16);
       }
       if (threadIdx.x >= 32 && threadIdx.x < 64) {
@@ -297,14 +320,15 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
 
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map,
-                                uint8_t* codes_rows, uint8_t* sf_rows) {
+                                uint8_t* codes_rows, uint8_t* sf_rows, bool fp4) {
   if (rows == 0 || batch == 0) return cudaSuccess;  // callers pass rows % 128 == 0, C % 128 == 0
-  const cudaError_t e = cudaFuncSetAttribute(quant_cols_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
+  auto kern = fp4 ? quant_cols_t_kernel<true> : quant_cols_t_kernel<false>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(batch) * (rows / 128) * (C / 128);
   const int grid = static_cast<int>(tiles < 2ll * num_sms() ? tiles : 2ll * num_sms());  // two blocks per SM
-  quant_cols_t_kernel<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), batch, rows, C, nrows_dev,
-                                                      codes, sf, row_map, codes_rows, sf_rows);
+  kern<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), batch, rows, C, nrows_dev, codes, sf,
+                                       row_map, codes_rows, sf_rows);
   count_launch();
   return cudaGetLastError();
 }

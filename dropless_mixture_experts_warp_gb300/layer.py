@@ -74,7 +74,7 @@ def allocate(dims: B.moe_dims, device="cuda") -> Buffers:
         fs = dims.f_shared
         shared = dict(gu_s=e(T, 2 * fs), h_s=e(T, fs), y_s=e(T, d), dgu_s=e(T, 2 * fs), dx_s=e(T, d),
                       dw_gu_s=e(2 * fs, d), dw_d_s=e(d, fs))
-    if dims.prec == 1:
+    if dims.prec in (1, 2):
         shared["wq"] = torch.empty(B.moe_mx_weights_size(dims), dtype=torch.uint8, device=device)
         shared["mx_ws"] = torch.empty(B.moe_mx_workspace_size(dims), dtype=torch.uint8, device=device)
         if dims.f_shared:
@@ -100,7 +100,7 @@ def quantize_weights(b: Buffers, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=None
     step of several micro-batches quantises them once and passes weights_cached=True to every
     forward() of the step."""
     dm = b.dims
-    if dm.prec != 1:
+    if dm.prec not in (1, 2):
         raise ValueError("quantize_weights: the layer is not MXFP8")
     B.moe_mx_quantize_weights(dm, w_gu, w_d, b.wq, stream)
     if dm.f_shared:
@@ -114,7 +114,7 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
     b.wq_s) already hold this step's quantised weights (quantize_weights()), so they are not
     quantised again."""
     dm = b.dims
-    mx8 = dm.prec == 1
+    mx8 = dm.prec in (1, 2)   # MXFP8, or FP8 x FP4 (MXFP4 weights)
     if mx8 and not weights_cached:
         quantize_weights(b, w_gu, w_d, stream, w_gu_s, w_d_s)
     shared_out = None
@@ -134,8 +134,7 @@ def forward(b: Buffers, x, logits, w_gu, w_d, stream=None, w_gu_s=None, w_d_s=No
     if mx8:
         B.moe_permute_mx(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.mx_ws,
                          b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
-        B.moe_gemm_gate_up_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.status, stream)
-        B.moe_gemm_down_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status, stream)
+        B.moe_grouped_mlp_fwd_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.y_rows, b.status, stream)
     else:
         B.moe_permute(dm, x, b.topk_idx, b.topk_w, b.split_sizes, b.row_offsets, b.workspace, b.xp,
                       b.row_to_token, b.token_to_row, b.w_rows, b.status, stream)
@@ -149,7 +148,7 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
     """x (the forward's input) is needed by the shared expert and by the MXFP8 path; grouped as in
     forward()."""
     dm = b.dims
-    mx8 = dm.prec == 1
+    mx8 = dm.prec in (1, 2)   # MXFP8, or FP8 x FP4 (MXFP4 weights)
     shared_dx = None
     if dm.f_shared and mx8:
         B.moe_shared_mlp_bwd_mx(dm, b.wq_s, b.mx_ws_s, b.gu_s, dy, b.dx_s, b.dw_gu_s, b.dw_d_s, b.status,
@@ -161,11 +160,8 @@ def backward(b: Buffers, dy, logits, w_gu, w_d, stream=None, x=None, w_gu_s=None
         shared_dx = b.dx_s
     if mx8:
         B.moe_combine_bwd_mx(dm, dy, b.row_to_token, b.split_sizes, b.row_offsets, b.mx_ws, stream)
-        B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace,
-                                 b.status, stream)
-        B.moe_gemm_down_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_d, b.status, stream)
-        B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status, stream)
-        B.moe_gemm_gate_up_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_gu, b.status, stream)
+        B.moe_grouped_mlp_bwd_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dxp, b.dw_gu, b.dw_d,
+                                 b.dw_rows, b.workspace, b.status, stream)
     else:
         B.moe_combine_bwd(dm, dy, b.token_to_row, b.split_sizes, b.row_offsets, b.dy_rows, stream)
         B.moe_grouped_mlp_bwd(dm, b.xp, b.row_offsets, b.w_rows, w_gu, w_d, b.gu, b.h, b.dy_rows, b.dgu,

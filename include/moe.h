@@ -61,7 +61,10 @@ typedef enum moe_status {
 } moe_status;
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
-enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 };
+/* MOE_PREC_MXFP8_W4: FP8 x FP4 experts -- activations and gradients MXFP8 (E4M3), the
+ * expert weights MXFP4 (E2M1 codes with one E8M0 scale per 32 elements); see the MXFP8
+ * layer calls below. */
+enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1, MOE_PREC_MXFP8_W4 = 2 };
 enum { MOE_ROW_ALIGN = 128 };
 
 typedef struct moe_dims {
@@ -391,7 +394,36 @@ moe_status moe_gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* 
                           moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream);
 
 /*
- * The layer with MXFP8 GEMM operands (dims->prec may be either value; f % 128 == 0).
+ * FP8 x FP4 building blocks [MEGA "ทิศทางการปรับปรุงในระดับลึกยิ่งขึ้น": FP8 x FP4 mixed
+ * precision as the next step for the expert GEMMs].  The weight operand is MXFP4: E2M1
+ * codes (sign, two exponent bits with bias 1, one mantissa bit: magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6) with one E8M0 scale per 32 elements along the contraction, scale rule
+ * e = floor(log2(amax)) - 2 clamped to [-127,127] (byte e + 127, 0 for an all-zero
+ * block), codes = E2M1(x * 2^-e), round to nearest even, saturating at 6.  Codes are
+ * packed two a byte, the element with the lower index in the lower four bits; the SF
+ * tiles are laid out as for MXFP8.
+ *
+ * moe_mx4_quantize_cols: src bf16 [batch][rows][C] -> codes_t [batch][C][rows / 2] bytes
+ *   with per-batch SF tiles (blocks of 32 rows down each column; K = rows), and codes
+ *   [batch * rows][C / 2] bytes with SF tiles of K = C (blocks along each row), from one
+ *   read.  rows % 128 == 0, C % 128 == 0; pointers 16-byte aligned.
+ * moe_gemm_mxf8f4: C[M][N] bf16 = sum_k deq(A)(m,k) deq(B)(n,k), A E4M3 codes [M][K] and
+ *   B E2M1 codes [N][K / 2] bytes (both K-major, B 32-byte aligned) with their SF tiles;
+ *   the block-scaled tcgen05 MMA with an E2M1 B operand, fp32 accumulation.  M, N, K
+ *   multiples of 128.
+ */
+moe_status moe_mx4_quantize_cols(const moe_bf16* src, int32_t batch, int64_t rows, int32_t C, uint8_t* codes_t,
+                                 uint8_t* scales_t, uint8_t* codes, uint8_t* scales, void* stream);
+moe_status moe_gemm_mxf8f4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b4, const uint8_t* b_sf,
+                           moe_bf16* c, int32_t M, int32_t N, int32_t K, int32_t* dev_status, void* stream);
+
+/*
+ * The layer with MXFP8 GEMM operands (dims->prec may be any value; f % 128 == 0).
+ * With dims->prec == MOE_PREC_MXFP8_W4 the experts are FP8 x FP4: wq (and wq_s) hold the
+ * weights as MXFP4 codes (moe_mx_weights_size shrinks accordingly; wq and wq_s must be
+ * 32-byte aligned) and the four products with a weight operand (gate/up and down
+ * forward, their input gradients) run with an E2M1 B operand; the weight gradients
+ * stay FP8 x FP8.
  * Every GEMM operand is quantised along its own contraction axis, in the kernel that
  * produces it: the routed token rows by moe_permute_mx and dY's routed rows by
  * moe_combine_bwd_mx, each in one gathered pass that writes both the row-wise codes
@@ -438,6 +470,31 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_of
                                      void* mx_ws, moe_bf16* dxp, int32_t* dev_status, void* stream);
 moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const int32_t* row_offsets, void* mx_ws,
                                      moe_bf16* dw_gu, int32_t* dev_status, void* stream);
+
+/*
+ * Steps 3-5 with MXFP8 operands as one call, and their backward as one call
+ * [BIO "צמצום הזיכרון ותקורות הכימות": GroupedLinear -> ScaledSwiGLU -> GroupedLinear
+ * as one fused MXFP8 operation with a backward counterpart; DROPLESS "Csoportosított
+ * mátrixszorzás és összevont adatmozgatás": group-aware MXFP8 quantisation for the
+ * expert GEMMs].  The MXFP8 counterparts of moe_grouped_mlp_fwd / moe_grouped_mlp_bwd:
+ *   moe_grouped_mlp_fwd_mx = moe_gemm_gate_up_mx + moe_gemm_down_mx.  Reads the routed
+ *     x codes that moe_permute_mx left in mx_ws and the weight codes in wq; writes gu
+ *     (saved G|U, bf16 [rows][2f]), y_rows (bf16 [rows][d]) and h's codes (in mx_ws).
+ *   moe_grouped_mlp_bwd_mx = moe_gemm_down_dgrad_mx + moe_gemm_down_wgrad_mx +
+ *     moe_gemm_gate_up_dgrad_mx + moe_gemm_gate_up_wgrad_mx.  Reads dY's routed codes
+ *     (moe_combine_bwd_mx), h's and x's codes in mx_ws, gu and wq; writes dw_rows (fp32
+ *     [rows]), dW_d [E][d][f], dxp [rows][d], dW_gu [E][2f][d] (bf16) and dG|dU's codes
+ *     (in mx_ws); workspace >= moe_workspace_size bytes.
+ * Same kernels and results as the per-GEMM calls; an argument error is returned
+ * before any kernel is enqueued.
+ */
+moe_status moe_grouped_mlp_fwd_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, moe_bf16* gu, moe_bf16* y_rows, int32_t* dev_status,
+                                  void* stream);
+moe_status moe_grouped_mlp_bwd_mx(const moe_dims* dims, const int32_t* row_offsets, const float* w_rows,
+                                  const void* wq, void* mx_ws, const moe_bf16* gu, moe_bf16* dxp, moe_bf16* dw_gu,
+                                  moe_bf16* dw_d, float* dw_rows, void* workspace, int32_t* dev_status,
+                                  void* stream);
 
 /*
  * The shared expert with MXFP8 GEMM operands (DeepSeek-V3 shape in MXFP8; f_shared and

@@ -236,3 +236,37 @@ def test_mx_weights_cached_across_micro_batches(name):
             assert torch.equal(cached.dw_gu_s, ref.dw_gu_s) and torch.equal(cached.dw_d_s, ref.dw_d_s)
     assert torch.equal(cached.wq, wq0)
     assert not torch.equal(getattr(_run(cfg, micro[1])[0], "y"), getattr(_run(cfg, micro[0])[0], "y"))
+
+
+def test_mx_composites_equal_the_per_gemm_calls():
+    """moe_grouped_mlp_fwd_mx / moe_grouped_mlp_bwd_mx (used by layer.forward/backward, which the
+    tests above compare with the oracle) give the same bits as the six per-GEMM calls in order."""
+    need_gpu()
+    from dropless_mixture_experts_warp_gb300 import binding as B
+    cfg = CASES["mx-zipf"]
+    b, inp, w_gu_b, w_d_b = _run(cfg)
+    dm = b.dims
+    got = {k: getattr(b, k).clone() for k in ("gu", "y_rows", "dxp", "dw_gu", "dw_d", "dw_rows")}
+    # repeat the MLP steps through the per-GEMM calls on the same quantised operands
+    for name in ("gu", "y_rows", "dxp", "dw_gu", "dw_d", "dw_rows"):
+        getattr(b, name).zero_()
+    B.moe_gemm_gate_up_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.status)
+    B.moe_gemm_down_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.y_rows, b.status)
+    B.moe_combine_bwd_mx(dm, bf16_dev(inp["dy"]), b.row_to_token, b.split_sizes, b.row_offsets, b.mx_ws)
+    B.moe_gemm_down_dgrad_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, b.dw_rows, b.workspace, b.status)
+    B.moe_gemm_down_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_d, b.status)
+    B.moe_gemm_gate_up_dgrad_mx(dm, b.row_offsets, b.wq, b.mx_ws, b.dxp, b.status)
+    B.moe_gemm_gate_up_wgrad_mx(dm, b.row_offsets, b.mx_ws, b.dw_gu, b.status)
+    assert B.moe_check_status(b.status) == 0
+    n = int(host(b.row_offsets)[-1])
+    real = torch.zeros(b.rows, dtype=torch.bool, device=b.row_to_token.device)
+    real[:n] = b.row_to_token[:n] >= 0              # rows holding a token (padding rows aside)
+    for name, ref in got.items():
+        cur = getattr(b, name)
+        if cur.shape[0] == b.rows:
+            assert torch.equal(cur[real], ref[real]), name
+        else:
+            assert torch.equal(cur, ref), name
+    with pytest.raises(B.MoeError):       # an argument error comes back before anything runs
+        B.moe_grouped_mlp_bwd_mx(dm, b.row_offsets, b.w_rows, b.wq, b.mx_ws, b.gu, None, b.dw_gu, b.dw_d,
+                                 b.dw_rows, b.workspace, b.status)
