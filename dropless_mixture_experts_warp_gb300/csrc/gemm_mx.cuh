@@ -41,9 +41,10 @@ __host__ __device__ constexpr int mx_smem_bytes(int epi) {
   return MX_XBUF_OFF + (epi_quantises(epi) ? mx_epi_warps(epi) * XBUF_FLOATS * 4 : 0) +
          (epi == 0 ? mx_epi_warps(epi) * 2048 : 0) + 1024;
 }
-// Bytes a TMA load of one 128-element E2M1 row counts on its mbarrier: the 128 bytes it
-// fills in shared memory (16 codes in 8 bytes, then 8 bytes of gap), not the 64 it reads.
-constexpr int MX_W4_TX_ROW_BYTES = 128;
+// Bytes a TMA load of one 128-element E2M1 row counts on its mbarrier: the 64 bytes of
+// packed codes it moves, although the row spans 128 bytes of shared memory (each 8 bytes
+// of codes followed by an 8-byte gap that the load leaves unwritten).
+constexpr int MX_W4_TX_ROW_BYTES = 64;
 constexpr int MX_SF_TMEM_COL = 256;                         // first scale-factor column
 constexpr int MX_SF_COLS_PER_STAGE = 16;                    // 4 for A, up to 8 for B
 // BN = 256 (four stages): the TMEM columns after the scale factors hold accumulator
@@ -113,7 +114,10 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   // 4 or 6 operand stages; the SwiGLU' GEMM at BN = 256 keeps 3 and holds its warps'
   // G/U boxes in the fourth stage's memory
   const bool gu_boxes = EPI == EPI_SWIGLU_BWD_MX && BN == 256;
-  const int stages = gu_boxes ? 3 : MX_CODE_BYTES / stage_bytes;
+  // the weight gradients (ragged K, many short-K tiles) give their last stage to two
+  // staging boxes per epilogue warp, so a tile's stores do not wait on each other
+  constexpr bool two_boxes = SCHED == SCHED_KGROUP && EPI == EPI_STORE;
+  const int stages = gu_boxes ? 3 : MX_CODE_BYTES / stage_bytes - (two_boxes ? 1 : 0);
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
-    uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 2048;
+    uint8_t* stg = two_boxes ? smem + stages * stage_bytes + (warp - 2) * 4096   // 32 KB <= a stage
+                             : smem + MX_XBUF_OFF + (warp - 2) * 2048;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
     uint32_t gu_phase = 0;
     bool gu_inflight = false;  // a G/U box load not yet waited for
@@ -239,7 +244,10 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
         // output rows: the padded row space (SCHED_ROWS) or expert e's block of M rows
         const long long y0 = (SCHED == SCHED_KGROUP ? static_cast<long long>(c.e) * p.M : 0ll) + c.out_row + q * 32;
-        store_chunks_tma(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
+        if (two_boxes)
+          store_chunks_tma<2>(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
+        else
+          store_chunks_tma<1>(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
         continue;
       }
       if (EPI == EPI_SWIGLU_FWD_MX) {
