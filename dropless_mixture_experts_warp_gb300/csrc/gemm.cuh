@@ -314,21 +314,17 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int lane, const flo
 }
 
 // Part 2: the chunks (columns x0 .. x0 + 32 nc of output rows y0 .. y0 + 31) leave as
-// bf16 through the warp's 2 KB staging buffers (64-byte swizzle: 16-byte chunk j of row r
+// bf16 through the warp's 2 KB staging buffer (64-byte swizzle: 16-byte chunk j of row r
 // at chunk j ^ ((r >> 1) & 3), free of bank conflicts)
-// and one tensor store each, while the next tile accumulates.  With NBUF buffers (at
-// stg + 2 KB * b) chunk i goes to buffer i % NBUF once the store NBUF chunks back has
-// read it; nc is even, so every tile starts on buffer 0.
-template <int NBUF = 1>
+// and one tensor store each, while the next tile accumulates.
 __device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const uint32_t (&r)[4][32], int nc, int x0,
                                                  int y0, int lane, uint8_t* stg) {
+  const uint32_t row_addr = smem_u32(stg) + lane * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (i < nc) {
-      uint8_t* buf = stg + 2048 * (i % NBUF);
-      const uint32_t row_addr = smem_u32(buf) + lane * 64;
-      if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that used this buffer has read it
+      if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -340,7 +336,7 @@ __device__ __forceinline__ void store_chunks_tma(const CUtensorMap* tmC, const u
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tmC, buf, x0 + 32 * i, y0);
+        tma_store_2d(tmC, stg, x0 + 32 * i, y0);
         bulk_commit();
       }
     }

@@ -31,23 +31,13 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES_MAX;
 // write through staging boxes and tensor stores.
 __host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 0 ? 8 : epi_warps(epi); }
 __host__ __device__ constexpr int pair_threads(int epi) { return 64 + 32 * pair_epi_warps(epi); }
-// Staging boxes per STORE epilogue warp: two for the weight gradients (SCHED_KGROUP),
-// whose short-K tiles (experts with a few hundred rows) leave the epilogue, not the
-// MMAs, on the critical path: a box is written while the previous one is still being
-// read by its tensor store.  The row-scheduled products keep one and a sixth stage.
-__host__ __device__ constexpr int pair_store_boxes(int sched) { return sched == SCHED_KGROUP ? 2 : 1; }
-// Operand stages: six; five for SwiGLU' (whose warps also hold a G/U box) and for the
-// weight gradients (whose warps hold two staging boxes).
-__host__ __device__ constexpr int pair_stages(int sched, int epi) {
-  return (epi == 2 || (epi == 0 && pair_store_boxes(sched) > 1)) ? 5 : P_STAGES;
-}
-// per epilogue warp: STORE 2 KB per staging box; SwiGLU 6 KB (its G, U and h boxes);
+// Operand stages: six, five for SwiGLU' (whose warps also hold a G/U box).
+__host__ __device__ constexpr int pair_stages(int epi) { return epi == 2 ? 5 : P_STAGES; }
+// per epilogue warp: STORE 2 KB (staging box); SwiGLU 6 KB (its G, U and h boxes);
 // SwiGLU' 6 KB (a dG/dU staging box and the 4 KB box of the saved G and U)
-__host__ __device__ constexpr int pair_epi_bytes(int sched, int epi) {
-  return epi == 0 ? 2048 * pair_store_boxes(sched) : 6144;
-}
-__host__ __device__ constexpr int p_smem_bytes(int sched, int epi) {
-  return pair_stages(sched, epi) * P_STAGE_BYTES + pair_epi_warps(epi) * pair_epi_bytes(sched, epi) + 1024;
+__host__ __device__ constexpr int pair_epi_bytes(int epi) { return epi == 0 ? 2048 : 6144; }
+__host__ __device__ constexpr int p_smem_bytes(int epi) {
+  return pair_stages(epi) * P_STAGE_BYTES + pair_epi_warps(epi) * pair_epi_bytes(epi) + 1024;
 }
 
 struct PairTile {
@@ -128,7 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
   __shared__ int s_pt[MAX_EXPERTS + 1];
-  constexpr int STAGES = pair_stages(SCHED, EPI);
+  constexpr int STAGES = pair_stages(EPI);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag};
-    uint8_t* stg = smem + STAGES * P_STAGE_BYTES + (warp - 2) * pair_epi_bytes(SCHED, EPI);
+    uint8_t* stg = smem + STAGES * P_STAGE_BYTES + (warp - 2) * pair_epi_bytes(EPI);
     uint32_t gu_phase = 0;
     bool gu_inflight = false;  // a G/U box load not yet waited for
     for (int rnd = 0, tile = sched_tile(0, pair, npairs, snake); tile < total;
@@ -292,8 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
         if (t.c.out_row + q * 32 < t.row_end) {  // 32-row blocks never straddle an expert's end
           const long long y0 =
               (SCHED == SCHED_KGROUP ? static_cast<long long>(t.c.e) * p.M : 0ll) + t.c.out_row + q * 32;
-          store_chunks_tma<pair_store_boxes(SCHED)>(&tmC, r, BN / 64, t.c.out_col + col0, static_cast<int>(y0),
-                                                    lane, stg);
+          store_chunks_tma(&tmC, r, BN / 64, t.c.out_col + col0, static_cast<int>(y0), lane, stg);
         }
         continue;
       }

@@ -114,10 +114,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
   // 4 or 6 operand stages; the SwiGLU' GEMM at BN = 256 keeps 3 and holds its warps'
   // G/U boxes in the fourth stage's memory
   const bool gu_boxes = EPI == EPI_SWIGLU_BWD_MX && BN == 256;
-  // the weight gradients (ragged K, many short-K tiles) give their last stage to two
-  // staging boxes per epilogue warp, so a tile's stores do not wait on each other
-  constexpr bool two_boxes = SCHED == SCHED_KGROUP && EPI == EPI_STORE;
-  const int stages = gu_boxes ? 3 : MX_CODE_BYTES / stage_bytes - (two_boxes ? 1 : 0);
+  const int stages = gu_boxes ? 3 : MX_CODE_BYTES / stage_bytes;
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
   const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
@@ -221,8 +218,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
     int acc = 0;
     uint32_t acc_phase = 0, dw_phase = 0;
     float* xbuf = reinterpret_cast<float*>(smem + MX_XBUF_OFF) + (warp - 2) * XBUF_FLOATS;
-    uint8_t* stg = two_boxes ? smem + stages * stage_bytes + (warp - 2) * 4096   // 32 KB <= a stage
-                             : smem + MX_XBUF_OFF + (warp - 2) * 2048;
+    uint8_t* stg = smem + MX_XBUF_OFF + (warp - 2) * 2048;
     const DwHandoff hand{s_dw, dw_full_bar, dw_empty_bar, &dw_phase, abort_flag, xbuf};
     uint32_t gu_phase = 0;
     bool gu_inflight = false;  // a G/U box load not yet waited for
@@ -244,10 +240,7 @@ __global__ void __launch_bounds__(mx_threads(EPI), 1)
         if (++acc == num_acc) { acc = 0; acc_phase ^= 1; }
         // output rows: the padded row space (SCHED_ROWS) or expert e's block of M rows
         const long long y0 = (SCHED == SCHED_KGROUP ? static_cast<long long>(c.e) * p.M : 0ll) + c.out_row + q * 32;
-        if (two_boxes)
-          store_chunks_tma<2>(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
-        else
-          store_chunks_tma<1>(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
+        store_chunks_tma(&tmC, r, BN / 64, c.out_col + col0, static_cast<int>(y0), lane, stg);
         continue;
       }
       if (EPI == EPI_SWIGLU_FWD_MX) {

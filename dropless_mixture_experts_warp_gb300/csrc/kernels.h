@@ -92,11 +92,10 @@ template <int SCHED, int EPI, bool A_MN, bool B_MN>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                                const CUtensorMap& dd, const GemmParams& p, cudaStream_t stream) {
   auto kern = grouped_gemm_pair_kernel<SCHED, EPI, A_MN, B_MN>;
-  constexpr int smem = p_smem_bytes(SCHED, EPI);
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem_bytes(EPI));
   if (err != cudaSuccess) return err;
-  static const int grid = pair_grid(reinterpret_cast<const void*>(kern), pair_threads(EPI), smem);
-  kern<<<grid, pair_threads(EPI), smem, stream>>>(a, b, c, dd, p);
+  static const int grid = pair_grid(reinterpret_cast<const void*>(kern), pair_threads(EPI), p_smem_bytes(EPI));
+  kern<<<grid, pair_threads(EPI), p_smem_bytes(EPI), stream>>>(a, b, c, dd, p);
   count_launch();
   return cudaGetLastError();
 }
