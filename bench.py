@@ -59,7 +59,8 @@ def workload_name(cfg) -> str:
              "qwen235b-zipf": "Qwen3-235B-A22B-shaped MoE layer (Zipf routing)",
              "dsv3": "DeepSeek-V3-shaped routed-expert layer",
              "dsv3-grouped": "DeepSeek-V3-shaped routed-expert layer with group-limited routing",
-             "mixtral-e2": "Mixtral-8x7B-shaped experts (2 of them) MoE layer"}
+             "mixtral-e2": "Mixtral-8x7B-shaped experts (2 of them) MoE layer",
+             "dsv3-proxy": "DeepSeek-V3-width experts (64 of them, d=2048) MoE layer"}
     return names.get(cfg.name, cfg.name) + " fwd+bwd"
 
 

@@ -89,6 +89,11 @@ CONFIGS: Dict[str, MoEConfig] = {
     # (x 256 MB, routed rows 512 MB) with small experts
     "hbm-probe": MoEConfig("hbm-probe", T=32768, d=4096, f=128, E=8, k=2, score=SOFTMAX,
                            bias="normal", bias_param=0.5, seed=1008),
+    # profiling case for the ragged-K weight gradients: DeepSeek-V3's expert width
+    # (f = 2048) and routing (sigmoid, Zipf(1.0) load, top-8) at about 256 rows per expert
+    # and 64 experts, near 3.5 GB of device memory
+    "dsv3-proxy": MoEConfig("dsv3-proxy", T=2048, d=2048, f=2048, E=64, k=8, score=SIGMOID,
+                            bias="zipf", bias_param=1.0, forced_empty=1, seed=1010),
     # DeepSeek-V3 shape with its group-limited router: 8 groups of 32, 4 eligible,
     # routed scale 2.5, a small per-expert selection bias
     "dsv3-grouped": MoEConfig("dsv3-grouped", T=16384, d=7168, f=2048, E=256, k=8, score=SIGMOID,
