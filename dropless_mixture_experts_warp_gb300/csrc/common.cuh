@@ -382,8 +382,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// Arrive on a barrier of either CTA of the pair (a shared::cluster address) with the default
+// semantics (release at CTA scope).  The epilogue's arrive that frees an accumulator needs
+// no more: its tensor-memory loads have completed (tcgen05.wait::ld) and been fenced
+// (tcgen05.fence::before_thread_sync) before it; a cluster-scope release here cost the
+// epilogue warps a memory barrier on every tile.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on an mbarrier
