@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libmoe.so")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "noalloc.cu", "quant.cu", "gemm_mx.cu", "api_mx.cu", "gemm_pair.cu"]
+SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "noalloc.cu", "quant.cu", "gemm_mx.cu", "api_mx.cu", "gemm_pair.cu", "gemm_mx_pair.cu"]
 
 
 def nvcc() -> str:

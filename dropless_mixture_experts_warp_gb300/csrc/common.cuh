@@ -482,6 +482,24 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// CTA-pair forms (issued by the leader): the copy runs in both CTAs of the pair, each from
+// its own shared memory (same address) into its own TMEM; the MMA spans both CTAs (M =
+// 256), each holding its 128 rows of A, half of B's rows, the scale factors of its A rows
+// and those of all of B's rows.
+__device__ __forceinline__ void tc_cp_32x128b_x4_pair(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor for kind::mxf8f6f4 with an E4M3 A, UE8M0 scales, fp32 D:
 //   bits 4-5 B scale-factor id, 7-9 A format (0 = E4M3), 10-12 B format (0 = E4M3,
 //   5 = E2M1), 15/16 majorness (0 = K-major), 17-22 N>>3, bit 23 scale type (1 =

@@ -112,6 +112,11 @@ struct MxMat {
 // GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  p.sfa/p.sfb are taken from a
 // and b.
 cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmParams p, cudaStream_t stream);
+// The CTA-pair form for GEMM_ROWS_STORE and GEMM_KGROUP_STORE (BN = 256 or 128, B boxes
+// of BN / 2 rows, SF maps from make_tensor_map_sf; SCHED_KGROUP needs p.M % 256 == 0).
+cudaError_t launch_gemm_mx_pair(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sfa,
+                                const CUtensorMap& sfb, const CUtensorMap& c, const GemmParams& p,
+                                cudaStream_t stream);
 cudaError_t launch_route_maps(int T, int E, int k, const int32_t* topk_idx, const float* topk_w,
                               const int32_t* split_sizes, const int32_t* row_offsets, const RouteScratch& ws,
                               int32_t* row_to_token, int32_t* token_to_row, float* w_rows, int rows_cap,
@@ -128,6 +133,7 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint
                           uint32_t box_inner, uint32_t box_outer);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
+bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes);
 // Packed 4-bit codes [outer][inner / 2] bytes loaded as 16-element groups padded to 16
 // bytes in shared memory (the layout the block-scaled MMA reads for E2M1 under
 // kind::mxf8f6f4), 128B swizzle; box_inner must be 128 elements.
