@@ -190,21 +190,10 @@ static bool pair_ok(GemmKind kind, const GemmParams& p) {
   return true;
 }
 
-// Row-scheduled products of grouped rows on CTA pairs: an expert with an odd number of
-// 128-row tiles would waste half of its last pair tile (at the DeepSeek-V3 shape the pairs
-// would compute 1.28x the rows instead of 1.12x), so the pairs take each expert's whole
-// 256-row pairs and a second, single-CTA launch on the same stream takes the odd last
-// tiles (b_single: the B map of the single-CTA kernel where its box differs).
 cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
-                        const GemmParams& p, cudaStream_t s, const CUtensorMap* b_single) {
-  if (!pair_ok(kind, p)) return bwd ? launch_gemm_bwd(kind, a, b, p, s) : launch_gemm_fwd(kind, a, b, p, s);
-  if (kind == GEMM_KGROUP_STORE || !p.row_offsets) return launch_gemm_pair(kind, a, b, p, s);
-  GemmParams q = p;
-  q.tail_mode = 1;
-  const cudaError_t err = launch_gemm_pair(kind, a, b, q, s);
-  if (err != cudaSuccess) return err;
-  const CUtensorMap& bs = b_single ? *b_single : b;
-  return bwd ? launch_gemm_bwd(kind, a, bs, q, s) : launch_gemm_fwd(kind, a, bs, q, s);
+                        const GemmParams& p, cudaStream_t s) {
+  if (pair_ok(kind, p)) return launch_gemm_pair(kind, a, b, p, s);
+  return bwd ? launch_gemm_bwd(kind, a, b, p, s) : launch_gemm_fwd(kind, a, b, p, s);
 }
 
 static GemmParams gemm_params() {
@@ -351,16 +340,15 @@ moe_status moe_gemm_down(const moe_dims* dims, const moe_bf16* h, const int32_t*
   const int64_t R_cap = row_capacity(d);
   const int64_t R = static_cast<int64_t>(d.T) * d.k;
   const int bn = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
-  CUtensorMap ta, tb, tb1;
+  CUtensorMap ta, tb;
   if (!make_map(&ta, h, d.f, R_cap, 64, BM) ||
-      !make_map(&tb, w_d, d.f, static_cast<uint64_t>(d.d) * d.E, 64, bn / 2) ||   // CTA-pair boxes
-      !make_map(&tb1, w_d, d.f, static_cast<uint64_t>(d.d) * d.E, 64, bn))        // single-CTA tails
+      !make_map(&tb, w_d, d.f, static_cast<uint64_t>(d.d) * d.E, 64, bn / 2))   // CTA-pair boxes
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets;
   p.b_rows_per_expert = d.d; p.m_fastest = (R / d.E <= d.d) ? 1 : 0;
   p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
-  return cuda_status(launch_best(GEMM_ROWS_STORE, false, ta, tb, p, static_cast<cudaStream_t>(stream), &tb1));
+  return cuda_status(launch_gemm_pair(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* xp,

@@ -83,10 +83,6 @@ struct GemmParams {
   int a_sf_ktiles;
   int b_sf_ktiles;
   int b_fmt;                    // B element format: MX_FMT_E4M3 (0) or MX_FMT_E2M1 (FP4 weights)
-  // SCHED_ROWS with row_offsets, bf16: 0 = every 128-row tile (single CTA) or every pair
-  // tile, an odd last tile padded (CTA pair); 1 = the CTA pair takes each expert's whole
-  // 256-row pairs and the single-CTA kernel its odd last 128-row tile (see launch_best)
-  int tail_mode;
   // fused MXFP8 outputs of the *_MX epilogues: row-wise codes [rows][width] with SF
   // tiles (K = width), and column-wise codes [width][q_cols_ld] with SF tiles
   // (K = rows, q_cols_ktiles = q_cols_ld / 128); width = f (h) or 2f (dG|dU)
@@ -150,21 +146,7 @@ template <int SCHED, int EPI, bool B_MN, int KB = BK>
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* s_ro, const int* order, int E,
                                                 int n_tiles, int tile) {
   TileCoord c;
-  if (SCHED == SCHED_ROWS && p.tail_mode) {
-    // only the last 128-row tile of each expert with an odd tile count: order[] lists them
-    const int e = order[tile / n_tiles];
-    c.n = tile % n_tiles;
-    c.m = (s_ro[e + 1] - s_ro[e]) / BM - 1;
-    c.e = e;
-    c.kblocks = p.K / KB;
-    c.a_m = s_ro[e] + c.m * BM;
-    c.a_k = 0;
-    c.out_col = gu_split(EPI) ? c.n * (p.BN / 2) : c.n * p.BN;
-    c.b_n = B_MN ? c.out_col : e * p.b_rows_per_expert + c.out_col;
-    c.b_k = B_MN ? e * p.b_k_per_expert : 0;
-    c.out_row = c.a_m;
-    c.out_base = 0;
-  } else if (SCHED == SCHED_ROWS) {
+  if (SCHED == SCHED_ROWS) {
     int lo = 0, hi = E - 1;  // last expert whose first tile is <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -681,8 +663,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_ro[MAX_EXPERTS + 1];
-  __shared__ int s_order[MAX_EXPERTS];  // KGROUP: visiting order; ROWS tails: experts with an odd tail
-  __shared__ int s_ntail;
+  __shared__ int s_order[SCHED == SCHED_KGROUP ? MAX_EXPERTS : 1];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -701,14 +682,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     const int per = (p.M / BM) * (p.N / p.BN);
     snake = kgroup_order(s_ro, E, per, gridDim.x, s_order);  // complete at the barrier below
   }
-  if (SCHED == SCHED_ROWS && p.tail_mode) __syncthreads();  // s_ro complete for the tail list
   if (threadIdx.x == 0) {
-    if (SCHED == SCHED_ROWS && p.tail_mode) {
-      int n = 0;
-      for (int e = 0; e < E; ++e)
-        if (((s_ro[e + 1] - s_ro[e]) / BM) & 1) s_order[n++] = e;
-      s_ntail = n;
-    }
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull_bar[a], 1); mbar_init(&tempty_bar[a], epi_warps(EPI)); }
     mbar_init(&drain_bar, 1);
@@ -725,8 +699,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 
   const int BN = p.BN;
   const int n_tiles = gu_split(EPI) ? p.N / (BN / 2) : p.N / BN;
-  const int total = (SCHED == SCHED_ROWS) ? (p.tail_mode ? s_ntail : s_ro[E] / BM) * n_tiles
-                                           : E * (p.M / BM) * n_tiles;
+  const int total = (SCHED == SCHED_ROWS) ? (s_ro[E] / BM) * n_tiles : E * (p.M / BM) * n_tiles;
   volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {

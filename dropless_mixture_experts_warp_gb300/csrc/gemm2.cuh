@@ -62,7 +62,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
     }
     const int e = lo;
     const int local = tile - s_pt[e];
-    const int mt2 = ((s_ro[e + 1] - s_ro[e]) / BM + (p.tail_mode ? 0 : 1)) / 2;
+    const int mt2 = ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2;
     if (p.m_fastest) { c.m = local % mt2; c.n = local / mt2; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
@@ -141,12 +141,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
       SCHED == SCHED_KGROUP && kgroup_order(s_ro, E, (p.M / (2 * BM)) * n_tiles, npairs, s_pt);
   if (threadIdx.x == 0) {
     if (SCHED == SCHED_ROWS) {
-      // pair tiles per expert, exclusive prefix (E <= 1024, once per launch); in tail mode
-      // only whole 256-row pairs (a single-CTA launch takes the odd last tiles)
+      // pair tiles per expert, exclusive prefix (E <= 1024, once per launch)
       int run = 0;
       for (int e = 0; e < E; ++e) {
         s_pt[e] = run;
-        run += ((s_ro[e + 1] - s_ro[e]) / BM + (p.tail_mode ? 0 : 1)) / 2 * n_tiles;
+        run += ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2 * n_tiles;
       }
       s_pt[E] = run;
     }

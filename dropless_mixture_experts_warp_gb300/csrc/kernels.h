@@ -76,10 +76,9 @@ cudaError_t launch_gemm_pair(GemmKind kind, const CUtensorMap& a, const CUtensor
 
 // The CTA-pair kernel where the product allows it (tiles at least 128 columns wide;
 // weight gradients in 256-row pairs), else the single-CTA kernel (bwd selects the
-// translation unit holding the backward instantiations); grouped row products run their
-// whole 256-row pairs on the pair kernel and each expert's odd last tile on the single one.
+// translation unit holding the backward instantiations).
 cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUtensorMap& b,
-                        const GemmParams& p, cudaStream_t stream, const CUtensorMap* b_single = nullptr);
+                        const GemmParams& p, cudaStream_t stream);
 
 // Grid of a persistent CTA-pair kernel: as many pairs as can be resident at once
 // (an SM whose TPC neighbour is unavailable cannot host half of a pair), at most
