@@ -87,8 +87,10 @@ def config_json(cfg, prec="bf16", weights_cached=False):
 # unchanged.
 KERNEL_SOURCES = {
     "bf16": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_pair.cu", "kernels.h", "api.cu"),
-    "mxfp8": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "kernels.h", "api_mx.cu"),
-    "mxfp8-w4": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "kernels.h", "api_mx.cu", "api.cu"),
+    "mxfp8": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh", "gemm_mx_pair.cu",
+              "kernels.h", "api_mx.cu"),
+    "mxfp8-w4": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh", "gemm_mx_pair.cu",
+                 "kernels.h", "api_mx.cu", "api.cu"),
 }
 
 

@@ -325,7 +325,7 @@ moe_status moe_gemm_gate_up(const moe_dims* dims, const moe_bf16* xp,
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets;
-  p.b_rows_per_expert = 2 * d.f; p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f;
+  p.b_rows_per_expert = 2 * d.f; p.m_fastest = ORDER_PER_GROUP; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_out = gu; p.h_out = h; p.status = dev_status;
   return cuda_status(launch_best(GEMM_ROWS_SWIGLU_FWD, false, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -346,7 +346,7 @@ moe_status moe_gemm_down(const moe_dims* dims, const moe_bf16* h, const int32_t*
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets;
-  p.b_rows_per_expert = d.d; p.m_fastest = (R / d.E <= d.d) ? 1 : 0;
+  p.b_rows_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP;
   p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   return cuda_status(launch_gemm_pair(GEMM_ROWS_STORE, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -413,7 +413,7 @@ moe_status moe_gemm_down_dgrad(const moe_dims* dims, const moe_bf16* dy_rows,
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets;
-  p.b_k_per_expert = d.d; p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f;
+  p.b_k_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu; p.dgu_out = dgu; p.dw_part = c.dw_part;
   p.dw_stride = d.f / bn; p.status = dev_status;
   if (launch_best(GEMM_ROWS_SWIGLU_BWD, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -458,7 +458,7 @@ moe_status moe_gemm_gate_up_dgrad(const moe_dims* dims, const moe_bf16* dgu,
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets;
-  p.b_k_per_expert = 2 * d.f; p.m_fastest = (R / d.E <= d.d) ? 1 : 0;
+  p.b_k_per_expert = 2 * d.f; p.m_fastest = ORDER_PER_GROUP;
   p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   return cuda_status(launch_best(GEMM_ROWS_STORE_BMN, true, ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -521,14 +521,14 @@ moe_status moe_shared_mlp_fwd(const moe_dims* dims, const moe_bf16* x, const moe
   if (!make_map(&ta, x, d.d, d.T, 64, BM) || !make_map(&tb, w_gu_s, d.d, 2ll * fs, 64, bn1 / 2))
     return MOE_ERR_CUDA;
   GemmParams p = gemm_params();
-  p.BN = bn1; p.N = fs; p.K = d.d; p.M = d.T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1;
+  p.BN = bn1; p.N = fs; p.K = d.d; p.M = d.T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = ORDER_PER_GROUP;
   p.f = fs; p.row_limit = d.T; p.gu_out = gu_s; p.h_out = h_s; p.status = dev_status;
   if (launch_best(GEMM_ROWS_SWIGLU_FWD, false, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   // down
   const int bn2 = bn_for(d.d) == 64 ? 128 : bn_for(d.d);
   if (!make_map(&ta, h_s, fs, d.T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, bn2 / 2)) return MOE_ERR_CUDA;
   p = gemm_params();
-  p.BN = bn2; p.N = d.d; p.K = fs; p.M = d.T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.BN = bn2; p.N = d.d; p.K = fs; p.M = d.T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP;
   p.out = y_s; p.ldo = d.d; p.row_limit = d.T; p.status = dev_status;
   return cuda_status(launch_gemm_pair(GEMM_ROWS_STORE, ta, tb, p, s));
 }
@@ -564,7 +564,7 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
     // dH = dy W_d_s (MN-major B) with the SwiGLU' epilogue, weight 1, no dw
     if (!make_map(&ta, dy, d.d, T, 64, BM) || !make_map(&tb, w_d_s, fs, d.d, 64, 64)) return MOE_ERR_CUDA;
     p = gemm_params();
-    p.BN = bn_for(fs); p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_k_per_expert = d.d; p.m_fastest = 1;
+    p.BN = bn_for(fs); p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_k_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP;
     p.f = fs; p.row_limit = T; p.gu_in = gu_s; p.dgu_out = dgu_s; p.status = dev_status;
     if (launch_best(GEMM_ROWS_SWIGLU_BWD, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
@@ -580,7 +580,7 @@ moe_status moe_shared_mlp_bwd(const moe_dims* dims, const moe_bf16* x, const moe
     if (!make_map(&ta, dgu_s, 2ll * fs, T, 64, BM) || !make_map(&tb, w_gu_s, d.d, 2ll * fs, 64, 64))
       return MOE_ERR_CUDA;
     p = gemm_params();
-    p.BN = bnd; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_k_per_expert = 2 * fs; p.m_fastest = 1;
+    p.BN = bnd; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_k_per_expert = 2 * fs; p.m_fastest = ORDER_PER_GROUP;
     p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
     if (launch_best(GEMM_ROWS_STORE_BMN, true, ta, tb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   }

@@ -259,7 +259,7 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets,
   MxMat mb = mat(w.gu_rows, d.d, 2ll * d.f * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = 256; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = 2 * d.f;
-  p.m_fastest = (R / d.E <= 2ll * d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
+  p.m_fastest = ORDER_PER_GROUP; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows;
   p.gu_out = gu; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
@@ -282,7 +282,7 @@ moe_status moe_gemm_down_mx(const moe_dims* dims, const int32_t* row_offsets, co
   MxMat mb = mat(w.d_rows, d.f, static_cast<uint64_t>(d.d) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
-  p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
+  p.m_fastest = ORDER_PER_GROUP; p.out = y_rows; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   p.a_sf_ktiles = d.f / 128; p.b_sf_ktiles = d.f / 128;
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -306,7 +306,7 @@ moe_status moe_gemm_down_dgrad_mx(const moe_dims* dims, const int32_t* row_offse
   MxMat mb = mat(w.d_cols, d.d, static_cast<uint64_t>(d.f) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.f;
-  p.m_fastest = (R / d.E <= d.f) ? 1 : 0; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
+  p.m_fastest = ORDER_PER_GROUP; p.f = d.f; p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu;
   p.dw_part = dw_part; p.dw_stride = d.f / bn; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
@@ -351,7 +351,7 @@ moe_status moe_gemm_gate_up_dgrad_mx(const moe_dims* dims, const int32_t* row_of
   MxMat mb = mat(w.gu_cols, 2ll * d.f, static_cast<uint64_t>(d.d) * d.E, w4(d));
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.K = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets; p.b_rows_per_expert = d.d;
-  p.m_fastest = (R / d.E <= d.d) ? 1 : 0; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
+  p.m_fastest = ORDER_PER_GROUP; p.out = dxp; p.ldo = d.d; p.row_limit = R_cap; p.status = dev_status;
   p.a_sf_ktiles = 2 * d.f / 128; p.b_sf_ktiles = 2 * d.f / 128;
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -505,7 +505,8 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   ma = mat(a.xp_rows, d.d, T);
   mb = mat(w.gu_rows, d.d, 2ll * fs, w4(d));
   p = mx_params();
-  p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs; p.m_fastest = 1; p.f = fs;
+  p.BN = 256; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = 2 * fs;
+  p.m_fastest = ORDER_PER_GROUP; p.f = fs;
   p.row_limit = T; p.gu_out = gu_s; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
@@ -515,7 +516,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   ma = mat(a.h_rows, fs, T);
   mb = mat(w.d_rows, fs, d.d, w4(d));
   p = mx_params();
-  p.BN = bn; p.N = d.d; p.K = fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.BN = bn; p.N = d.d; p.K = fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP;
   p.out = y_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
   p.a_sf_ktiles = fs / 128; p.b_sf_ktiles = fs / 128;
   return cuda_st(launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s));
@@ -553,7 +554,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
   ma = mat(a.dy_rows, d.d, T);
   mb = mat(w.d_cols, d.d, fs, w4(d));
   p = mx_params();
-  p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = 1; p.f = fs;
+  p.BN = bn; p.N = fs; p.K = d.d; p.M = T; p.E = 1; p.b_rows_per_expert = fs; p.m_fastest = ORDER_PER_GROUP; p.f = fs;
   p.row_limit = T; p.gu_in = gu_s; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.dgu_rows.codes; p.q_rows_sf = a.dgu_rows.sf; p.q_cols = a.dgu_cols.codes;
@@ -572,7 +573,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
   ma = mat(a.dgu_rows, 2ll * fs, T);
   mb = mat(w.gu_cols, 2ll * fs, d.d, w4(d));
   p = mx_params();
-  p.BN = bn; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = 1;
+  p.BN = bn; p.N = d.d; p.K = 2 * fs; p.M = T; p.E = 1; p.b_rows_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP;
   p.out = dx_s; p.ldo = d.d; p.row_limit = T; p.status = dev_status;
   p.a_sf_ktiles = 2 * fs / 128; p.b_sf_ktiles = 2 * fs / 128;
   if (launch_gemm_mx(GEMM_ROWS_STORE, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -64,7 +64,8 @@ struct GemmParams {
   const int32_t* row_offsets;   // [E+1] padded row offsets; NULL = one group of M rows
   int b_rows_per_expert;        // B K-major: rows of the B tensor per expert
   int b_k_per_expert;           // B MN-major (SCHED_ROWS): K rows per expert
-  int m_fastest;                // tile order inside a group: 1 = M fastest
+  int m_fastest;                // tile order inside a group: 0 = N fastest, 1 = M fastest,
+                                // ORDER_PER_GROUP (SCHED_ROWS): chosen per group, see rows_m_fastest
   int f;                        // SwiGLU epilogues: intermediate width (offset of U)
   moe_bf16* out;                // EPI_STORE output
   long long ldo;                // its leading dimension (elements)
@@ -140,6 +141,17 @@ __device__ __forceinline__ int sched_tile(int r, int w, int W, bool snake) {
   return r * W + ((snake && (r & 1)) ? W - 1 - w : w);
 }
 
+// Tile order of one group of SCHED_ROWS.  Each group sweeps its shorter side fastest: the
+// panels along that side (all of them) are revisited at every step along the longer side
+// and stay in L2, while each panel of the longer side is read once, by the workers on it at
+// the same time.  For a cold expert that is M (its few activation panels); for a hot expert
+// with more row tiles than column tiles it is N (its weight panels) -- sweeping M first
+// there streams its large block of activations from DRAM once per column of tiles.
+constexpr int ORDER_PER_GROUP = 2;
+__device__ __forceinline__ bool rows_m_fastest(int mode, int m_tiles, int n_tiles) {
+  return mode == ORDER_PER_GROUP ? m_tiles <= n_tiles : mode != 0;
+}
+
 // order: the experts in their visiting order (SCHED_KGROUP, kgroup_order; unused for
 // SCHED_ROWS)
 template <int SCHED, int EPI, bool B_MN, int KB = BK>
@@ -155,7 +167,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
     const int e = lo;
     const int local = tile - (s_ro[e] / BM) * n_tiles;
     const int mt = (s_ro[e + 1] - s_ro[e]) / BM;
-    if (p.m_fastest) { c.m = local % mt; c.n = local / mt; }
+    if (rows_m_fastest(p.m_fastest, mt, n_tiles)) { c.m = local % mt; c.n = local / mt; }
     else { c.n = local % n_tiles; c.m = local / n_tiles; }
     c.e = e;
     c.kblocks = p.K / KB;
