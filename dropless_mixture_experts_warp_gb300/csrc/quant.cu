@@ -104,11 +104,22 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   const long long rtiles = (limit + 127) / 128;  // row tiles that hold rows
   const long long total = static_cast<long long>(batch) * rtiles * ctiles;
   const long long k_tiles = rows / 128;
+  // tile t -> (batch, row tile, column tile) in 32-bit unsigned arithmetic (the launcher
+  // keeps the tile count below 2^31): a 64-bit division is a long software sequence, and
+  // three of them per tile and thread were a third of this kernel's instructions
+  const unsigned u_ct = static_cast<unsigned>(ctiles), u_rt = static_cast<unsigned>(rtiles);
+  struct Coord {
+    unsigned b, rti, cti;
+  };
+  auto coord = [&](long long t) {
+    const unsigned q = static_cast<unsigned>(t) / u_ct;
+    return Coord{q / u_rt, q % u_rt, static_cast<unsigned>(t) - q * u_ct};
+  };
 
   // the source rows of this thread's eight rows of tile t (-1: a zero row); with a row
   // map these are global loads, issued one tile ahead of the copies that use them
   auto rows_of = [&](long long t, int (&sr)[8]) {
-    const long long rti = t < total ? (t / ctiles) % rtiles : 0;
+    const long long rti = t < total ? coord(t).rti : 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const long long r = rti * 128 + (threadIdx.x >> 4) + 16 * j;
@@ -118,8 +129,9 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
   // issue the loads of tile t into input buffer `buf`
   auto fetch = [&](long long t, int buf, const int (&sr)[8]) {
     if (t < total) {
-      const int cti = static_cast<int>(t % ctiles);
-      const long long b = t / (static_cast<long long>(ctiles) * rtiles);
+      const Coord tc = coord(t);
+      const int cti = static_cast<int>(tc.cti);
+      const long long b = tc.b;
       const uint16_t* s = src + (row_map ? 0 : b * rows * C);
       uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
 #pragma unroll
@@ -146,9 +158,10 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
     cp_async_wait_prev();  // this tile's group has landed
     __syncthreads();
     const uint16_t(*tile)[QC_IN_LD] = reinterpret_cast<const uint16_t(*)[QC_IN_LD]>(qsm + buf * QC_IN_BYTES);
-    const int cti = static_cast<int>(t % ctiles);
-    const long long rti = (t / ctiles) % rtiles;
-    const long long b = t / (static_cast<long long>(ctiles) * rtiles);
+    const Coord tc = coord(t);
+    const int cti = static_cast<int>(tc.cti);
+    const long long rti = tc.rti;
+    const long long b = tc.b;
     const long long r0 = rti * 128;
     const int c0 = cti * 128;
     {
@@ -326,6 +339,7 @@ cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int 
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(batch) * (rows / 128) * (C / 128);
+  if (tiles >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernel indexes tiles in 32 bits
   const int grid = static_cast<int>(tiles < 2ll * num_sms() ? tiles : 2ll * num_sms());  // two blocks per SM
   kern<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), batch, rows, C, nrows_dev, codes, sf,
                                        row_map, codes_rows, sf_rows);
