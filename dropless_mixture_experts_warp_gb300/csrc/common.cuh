@@ -275,10 +275,14 @@ __device__ __forceinline__ float exp2_neg(int e) {
   return f > 0 ? __uint_as_float(static_cast<uint32_t>(f) << 23) : __uint_as_float(0x00400000u);
 }
 
-// Two fp32 -> two E4M3 bytes (lo from `lo`, hi from `hi`), RNE, saturating.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// Four fp32 -> four E4M3 bytes in one word (x0 in the lowest byte), RNE, saturating; the
+// two halves are joined inside the asm (as one packing move, not a widen, shift and or).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tcvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\tmov.b32 %0, {l, h};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
   return r;
 }
 
@@ -314,7 +318,7 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
     float x0 = v[4 * w + 0], x1 = v[4 * w + 1], x2 = v[4 * w + 2], x3 = v[4 * w + 3];
     mul_f32x2(x0, x1, ss);
     mul_f32x2(x2, x3, ss);
-    codes[w] = cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16);
+    codes[w] = cvt_e4m3x4(x0, x1, x2, x3);
   }
   return static_cast<uint32_t>(e + 127);
 }

@@ -285,7 +285,7 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
       float x0 = cv[4 * q], x1 = cv[4 * q + 1], x2 = cv[4 * q + 2], x3 = cv[4 * q + 3];
       mul_f32x2(x0, x1, ss);
       mul_f32x2(x2, x3, ss);
-      w[q] = cvt_e4m3x2(x0, x1) | (cvt_e4m3x2(x2, x3) << 16);
+      w[q] = cvt_e4m3x4(x0, x1, x2, x3);
     }
     const int col = col0 + 16 * s + cc;
     if (ok) {
