@@ -290,12 +290,14 @@ def expert_rows_mx(x_rows, w_rows, dy_rows, w_gu_e, w_d_e, dtype=np.float64, ful
 
 
 def expert_wgrad_sampled_mx(x, logits, dy, w_gu_e, w_d_e, e, k, gu_rows, d_cols, score="softmax",
-                            dtype=np.float64):
+                            dtype=np.float64, wq=None):
     """Selected entries of expert e's weight gradients in the MXFP8 layer.
 
     dW_gu[e][gu_rows, :] and dW_d[e][:, d_cols], by the formulas of moe_backward_mx
     restricted to the intermediate columns those entries need (each quantisation
-    block lies inside one row or one column, so the restriction is exact).
+    block lies inside one row or one column, so the restriction is exact).  ``wq`` is the
+    quantise-dequantise of the weight operands (default qdq, E4M3; qdq4 for FP8 x FP4
+    experts, the layer of moe_backward_mx with wmatmul=mx_matmul_w4).
     """
     from . import moe_oracle as om
     idx, w = om.route(logits, k, score, dtype)
@@ -314,8 +316,10 @@ def expert_wgrad_sampled_mx(x, logits, dy, w_gu_e, w_d_e, e, k, gu_rows, d_cols,
     qx = qdq(xe)                      # X_e along d (forward)
     qdy = qdq(dye)                    # dY_e along d (dgrad)
 
+    wq = qdq if wq is None else wq
+
     def gu_cols(cols):                # columns of G and U = mx(X_e, W_gu[e])
-        return qx @ qdq(wg[cols]).T, qx @ qdq(wg[f + cols]).T
+        return qx @ wq(wg[cols]).T, qx @ wq(wg[f + cols]).T
 
     # dW_d[:, c] = mx(dY_e^T, H_e^T): both along the rows of e
     g2, u2 = gu_cols(d_cols)
@@ -325,7 +329,7 @@ def expert_wgrad_sampled_mx(x, logits, dy, w_gu_e, w_d_e, e, k, gu_rows, d_cols,
     cols = gu_rows % f
     g, u = gu_cols(cols)
     sg = om._sigmoid(g)
-    dh = qdy @ qdq(wd.T[cols]).T       # dH = mx(dY_e, W_d[e]^T), columns `cols`
+    dh = qdy @ wq(wd.T[cols]).T        # dH = mx(dY_e, W_d[e]^T), columns `cols`
     da = we * dh
     dg = da * u * sg * (1.0 + g * (1.0 - sg))
     du = da * g * sg
@@ -406,14 +410,35 @@ def mx4_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return (v * np.exp2(scales.astype(np.float64) - 127)[..., None]).reshape(codes.shape)
 
 
+def e2m1_round(a: np.ndarray) -> np.ndarray:
+    """Value of e2m1_encode, computed arithmetically: |a| rounded to the E2M1 grid.
+
+    For |a| >= 1 the grid step is 2^(floor(log2|a|) - 1), below it 0.5 (the subnormal
+    0.5); np.rint rounds half to even, which is the even code; the result saturates at 6.
+    """
+    a = np.asarray(a, np.float64)
+    mag = np.minimum(np.abs(a), E2M1_MAX)
+    _, ex = np.frexp(mag)                         # mag = m 2^ex, m in [0.5, 1)
+    step = np.ldexp(1.0, np.maximum(ex - 1, 0) - 1)
+    r = np.minimum(np.rint(mag / step) * step, E2M1_MAX)
+    return np.copysign(r, a)
+
+
 def qdq4(x: np.ndarray) -> np.ndarray:
-    """E2M1 quantise-dequantise along the last axis, zero-padding it to a multiple of 32."""
+    """E2M1 quantise-dequantise along the last axis, zero-padding it to a multiple of 32.
+
+    Equal to mx4_dequantize(*mx4_quantize(x)) (checked in the tests), computed without
+    the code table so whole expert weights stay cheap.
+    """
     x = np.asarray(x, np.float64)
     K = x.shape[-1]
     pad = (-K) % BLOCK
     if pad:
         x = np.concatenate([x, np.zeros((*x.shape[:-1], pad))], axis=-1)
-    return mx4_dequantize(*mx4_quantize(x))[..., :K]
+    blocks = x.reshape(*x.shape[:-1], x.shape[-1] // BLOCK, BLOCK)
+    e = scale_exponent_e2m1(np.abs(blocks).max(axis=-1))
+    scale = np.ldexp(1.0, e)[..., None]
+    return (e2m1_round(blocks / scale) * scale).reshape(x.shape)[..., :K]
 
 
 def mx_matmul_w4(a: np.ndarray, b: np.ndarray, dtype=np.float64) -> np.ndarray:

@@ -5,7 +5,8 @@ receives the same bf16 bits.  Routing, counts and the permutation are compared i
 bit for bit (the group-limited router: bit for bit on tokens clear of a near-tie, checked for
 validity on the rest).  Y, dX and d_logits are compared on 256 random tokens; the weight
 gradients in full for the hottest, the coldest non-empty and one random expert, and in full
-(exact zeros) for empty experts.  The shared expert's weight gradients are compared on
+(exact zeros) for empty experts.  FP8 x FP4 experts (mxfp8-w4) are checked the same way
+against the MXFP8 oracle with E2M1 weight operands.  The shared expert's weight gradients are compared on
 sampled rows and columns.
 
 The oracle goes through the experts one at a time (oracle.expert_rows / expert_rows_mx, the
@@ -32,7 +33,7 @@ TOL_MXFP8 = 6e-2
 MARGIN = 2e-6
 CASES = [("mixtral", "bf16"), ("qwen30b", "bf16"), ("qwen235b", "bf16"), ("qwen235b-zipf", "bf16"),
          ("dsv3", "bf16"), ("dsv3-grouped", "bf16"), ("qwen30b", "mxfp8"), ("qwen235b", "mxfp8"),
-         ("qwen235b-zipf", "mxfp8"), ("dsv3", "mxfp8")]
+         ("qwen235b-zipf", "mxfp8"), ("dsv3", "mxfp8"), ("qwen235b", "mxfp8-w4"), ("dsv3", "mxfp8-w4")]
 N_TOKENS = 256
 N_ENTRIES = 12
 THREADS = max(1, min(8, os.cpu_count() or 1))   # each holds about 1 GB of one expert's arrays
@@ -72,14 +73,16 @@ def _routing(cfg, logits, bufs):
 def _expert_job(e, rows_t, rows_j, full, ctx):
     """Oracle rows of expert e (forward and backward) on the given (token, slot) pairs."""
     from oracle import mx
-    inp, w, mx8 = ctx["inp"], ctx["w"], ctx["mx8"]
+    inp, w, mx8, w4 = ctx["inp"], ctx["w"], ctx["mx8"], ctx["w4"]
     toks = torch.from_numpy(rows_t).to(inp["x"].device)
     x = host(inp["x"][toks])
     dy = host(inp["dy"][toks])
     w_gu = inp["w_gu"][e].float().cpu().numpy()
     w_d = inp["w_d"][e].float().cpu().numpy()
-    fn = mx.expert_rows_mx if mx8 else om.expert_rows
-    return fn(x, w[rows_t, rows_j], dy, w_gu, w_d, dtype=np.float32, full=full)
+    if mx8:   # FP8 x FP4 experts: the products with a weight operand take E2M1 weights
+        return mx.expert_rows_mx(x, w[rows_t, rows_j], dy, w_gu, w_d, dtype=np.float32, full=full,
+                                 wmatmul=mx.mx_matmul_w4 if w4 else None)
+    return om.expert_rows(x, w[rows_t, rows_j], dy, w_gu, w_d, dtype=np.float32, full=full)
 
 
 @pytest.mark.parametrize("name,prec", CASES)
@@ -88,7 +91,8 @@ def test_full_size_layer(name, prec):
     from dropless_mixture_experts_warp_gb300 import layer
     from oracle import mx
     cfg = synth.CONFIGS[name]
-    mx8 = prec == "mxfp8"
+    mx8 = prec in ("mxfp8", "mxfp8-w4")
+    w4 = prec == "mxfp8-w4"
     tol = TOL_MXFP8 if mx8 else TOL_BF16
     inp = synth.torch_inputs(cfg, torch.device("cuda"))
     dims = layer.dims_of(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.f_shared, cfg.score, prec)
@@ -121,7 +125,7 @@ def test_full_size_layer(name, prec):
             t_sel = sub[t_sub]
         if t_sel.size:
             jobs[e] = (t_sel, j_sel, e in full_experts)
-    ctx = {"inp": inp, "w": w.astype(np.float32), "mx8": mx8}
+    ctx = {"inp": inp, "w": w.astype(np.float32), "mx8": mx8, "w4": w4}
     with cf.ThreadPoolExecutor(THREADS) as pool:
         futs = {e: pool.submit(_expert_job, e, t, j, full, ctx) for e, (t, j, full) in jobs.items()}
         res = {e: f.result() for e, f in futs.items()}
@@ -141,9 +145,10 @@ def test_full_size_layer(name, prec):
     skw = {}
     if cfg.f_shared:                     # the shared expert: one dense expert with weight 1
         skw = {"w_gu_s": host(inp["w_gu_s"]), "w_d_s": host(inp["w_d_s"])}
+        rs_kw = {"wmatmul": mx.mx_matmul_w4} if w4 else {}
         fn = mx.expert_rows_mx if mx8 else om.expert_rows
         rs = fn(host(inp["x"][sub_t]), np.ones(N_TOKENS, np.float32), host(inp["dy"][sub_t]), skw["w_gu_s"],
-                skw["w_d_s"], dtype=np.float32, full=False)
+                skw["w_d_s"], dtype=np.float32, full=False, **rs_kw)
         y_ref, dx_ref = y_ref + rs["y"], dx_ref + rs["dx"]
     scale = 1.0 if gr is None else gr["routed_scale"]
     dl_ref = om.route_backward(logits[sub], idx[sub], w[sub], dw, om.SIGMOID if gr else cfg.score, np.float64,
@@ -159,8 +164,9 @@ def test_full_size_layer(name, prec):
         fs = cfg.f_shared
         rows = rng.choice(2 * fs, size=N_ENTRIES, replace=False)
         cols = rng.choice(fs, size=N_ENTRIES, replace=False)
+        wq_kw = {"wq": mx.qdq4} if w4 else {}
         s = wg_fn(host(inp["x"]), np.zeros((cfg.T, 1), np.float32), host(inp["dy"]), skw["w_gu_s"], skw["w_d_s"],
-                  0, 1, rows, cols, om.SOFTMAX, dtype=np.float32)
+                  0, 1, rows, cols, om.SOFTMAX, dtype=np.float32, **wq_kw)
         errs["dW_gu_s"] = rel_err(host(bufs.dw_gu_s[torch.from_numpy(rows).cuda()]), s["dW_gu_rows"])
         errs["dW_d_s"] = rel_err(host(bufs.dw_d_s[:, torch.from_numpy(cols).cuda()]), s["dW_d_cols"])
     print(f"{name} {prec}: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()) + f" (limit {tol})")

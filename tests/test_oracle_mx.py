@@ -152,6 +152,41 @@ def test_sampled_mx_wgrad_entries_match_full_mx_backward():
         np.testing.assert_allclose(s["dW_d_cols"], b1["dW_d"][e][:, cols], rtol=1e-10, atol=1e-12)
 
 
+def test_sampled_fp4_weight_wgrad_entries_match_full_backward():
+    """The same restriction with E2M1 weights: the entries equal the FP8 x FP4 layer's."""
+    x, logits, w_gu, w_d, dy, _ = _small(seed=11, T=90, E=3, k=2)
+    f1 = mx.moe_forward_mx(x, logits, w_gu, w_d, 2, wmatmul=mx.mx_matmul_w4)
+    b1 = mx.moe_backward_mx(x, logits, w_gu, w_d, dy, f1, 2, wmatmul=mx.mx_matmul_w4)
+    b8 = mx.moe_backward_mx(x, logits, w_gu, w_d, dy, mx.moe_forward_mx(x, logits, w_gu, w_d, 2), 2)
+    rows = np.array([0, 7, 31, 32, 50, 63])
+    cols = np.array([1, 17, 30])
+    for e in range(3):
+        s = mx.expert_wgrad_sampled_mx(x, logits, dy, w_gu[e], w_d[e], e, 2, rows, cols, wq=mx.qdq4)
+        np.testing.assert_allclose(s["dW_gu_rows"], b1["dW_gu"][e][rows], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(s["dW_d_cols"], b1["dW_d"][e][:, cols], rtol=1e-10, atol=1e-12)
+        assert not np.allclose(s["dW_gu_rows"], b8["dW_gu"][e][rows], rtol=1e-6)   # FP4 weights do change it
+
+
+def test_fast_qdq4_equals_code_table_path():
+    """The arithmetic E2M1 path gives the code-table path's values bit for bit: every bf16
+    value in blocks of every scale, the E2M1 ties, saturation, zeros of both signs."""
+    rng = np.random.default_rng(10)
+    v = _all_bf16_finite()
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 6.5, 7.0, 100.0])
+    x = np.concatenate([v, rng.standard_normal(4096) * 1e-3, np.zeros(64), -np.zeros(32), ties, -ties])
+    x = np.concatenate([x, np.zeros((-x.size) % 32)]).reshape(-1, 32)
+    ref = mx.mx4_dequantize(*mx.mx4_quantize(x))
+    got = mx.qdq4(x)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+    y = rng.standard_normal((50, 96)) * np.exp2(rng.integers(-30, 30, (50, 1)))
+    assert np.array_equal(mx.qdq4(y), mx.mx4_dequantize(*mx.mx4_quantize(y)))
+    # blocks whose scale puts the ties exactly on grid midpoints (amax 6: scale 2^0)
+    t = np.concatenate([ties[:8], -ties[:8], np.full(16, 0.1)])[None, :]
+    t[0, 0] = 6.0
+    assert np.array_equal(mx.qdq4(t), mx.mx4_dequantize(*mx.mx4_quantize(t)))
+
+
 def test_fast_qdq_equals_code_table_path():
     rng = np.random.default_rng(9)
     v = _all_bf16_finite()
