@@ -40,6 +40,9 @@ __host__ __device__ constexpr int p_smem_bytes(int epi) {
   return pair_stages(epi) * P_STAGE_BYTES + pair_epi_warps(epi) * pair_epi_bytes(epi) + 1024;
 }
 
+// A row coordinate past every tensor's rows: a tensor load there reads the zero fill.
+constexpr int DEAD_ROW = 1 << 30;
+
 struct PairTile {
   TileCoord c;
   long long row_end;  // rows at or beyond this are not stored
@@ -196,7 +199,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
           }
           const int k0 = kb * BK;
           if (!A_MN) {
-            tma_load_2d_pair(sa, &tmA, bar, c.a_k + k0, c.a_m);
+            // The upper half of an expert's last pair tile when it has an odd number of 128-row
+            // tiles lies past the expert's rows: its results are never stored, so it reads the
+            // zero fill of rows beyond the tensor instead of the next expert's rows.
+            const int a_row = (SCHED == SCHED_ROWS && c.a_m >= t.row_end) ? DEAD_ROW : c.a_m;
+            tma_load_2d_pair(sa, &tmA, bar, c.a_k + k0, a_row);
           } else {
             tma_load_2d_pair(sa, &tmA, bar, c.a_m, c.a_k + k0);
             tma_load_2d_pair(sa + 8192, &tmA, bar, c.a_m + 64, c.a_k + k0);
