@@ -45,8 +45,8 @@ GEMM_FLOP_FACTOR = {"gate_up": 4, "down": 2, "down_dgrad": 2, "down_wgrad": 2, "
                     "gate_up_wgrad": 4}   # x R*d*f
 GEMM_KERNEL_MX = {"gate_up": "grouped_gemm_mx_kernel<0,3>", "down": "grouped_gemm_mx_kernel<0,0>",
                   "down_dgrad": "grouped_gemm_mx_kernel<0,4> + dw_reduce_kernel",
-                  "down_wgrad": "grouped_gemm_mx_kernel<1,0>", "gate_up_dgrad": "grouped_gemm_mx_kernel<0,0>",
-                  "gate_up_wgrad": "grouped_gemm_mx_kernel<1,0>"}
+                  "down_wgrad": "grouped_gemm_mx_pair_kernel<1>", "gate_up_dgrad": "grouped_gemm_mx_kernel<0,0>",
+                  "gate_up_wgrad": "grouped_gemm_mx_pair_kernel<1>"}
 GEMM_KERNEL = {"gate_up": "grouped_gemm_pair_kernel<0,1,0,0>", "down": "grouped_gemm_pair_kernel<0,0,0,0>",
                "down_dgrad": "grouped_gemm_pair_kernel<0,2,0,1> + dw_reduce_kernel",
                "down_wgrad": "grouped_gemm_pair_kernel<1,0,1,1>", "gate_up_dgrad": "grouped_gemm_pair_kernel<0,0,0,1>",
@@ -87,10 +87,10 @@ def config_json(cfg, prec="bf16", weights_cached=False):
 # unchanged.
 KERNEL_SOURCES = {
     "bf16": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_pair.cu", "kernels.h", "api.cu"),
-    "mxfp8": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh", "gemm_mx_pair.cu",
-              "kernels.h", "api_mx.cu"),
-    "mxfp8-w4": ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh", "gemm_mx_pair.cu",
-                 "kernels.h", "api_mx.cu", "api.cu"),
+    "mxfp8": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh",
+              "gemm_mx_pair.cu", "kernels.h", "api_mx.cu"),
+    "mxfp8-w4": ("common.cuh", "gemm.cuh", "gemm2.cuh", "gemm_mx.cuh", "gemm_mx.cu", "gemm_mx2.cuh",
+                 "gemm_mx_pair.cu", "kernels.h", "api_mx.cu", "api.cu"),
 }
 
 

@@ -199,6 +199,7 @@ cudaError_t launch_best(GemmKind kind, bool bwd, const CUtensorMap& a, const CUt
 static GemmParams gemm_params() {
   GemmParams p;
   memset(&p, 0, sizeof(p));
+  p.band_krows = BAND_KROWS_BF16;
   return p;
 }
 

@@ -164,6 +164,7 @@ static moe_status mx_common(const moe_dims* dims) {
 static GemmParams mx_params() {
   GemmParams p;
   memset(&p, 0, sizeof(p));
+  p.band_krows = BAND_KROWS_E4M3;
   return p;
 }
 

@@ -66,6 +66,7 @@ struct GemmParams {
   int b_k_per_expert;           // B MN-major (SCHED_ROWS): K rows per expert
   int m_fastest;                // tile order inside a group: 0 = N fastest, 1 = M fastest,
                                 // ORDER_PER_GROUP (SCHED_ROWS): chosen per group, see rows_m_fastest
+  int band_krows;               // SCHED_ROWS, > 0: the fast side in bands of band_krows / K tiles (banded)
   int f;                        // SwiGLU epilogues: intermediate width (offset of U)
   moe_bf16* out;                // EPI_STORE output
   long long ldo;                // its leading dimension (elements)
@@ -152,6 +153,32 @@ __device__ __forceinline__ bool rows_m_fastest(int mode, int m_tiles, int n_tile
   return mode == ORDER_PER_GROUP ? m_tiles <= n_tiles : mode != 0;
 }
 
+// SCHED_ROWS: when the panels along the fast side of a large group (K elements deep each)
+// are more than L2 keeps beside the other side's stream, how much of them survives a sweep
+// depends on the timing of every other worker (the same bf16 schedule read 1.2x to 1.6x its
+// operand bytes from box to box).  So the fast side goes in bands: a band of b tiles of the
+// fast side is swept fastest against the whole slow side, then the next band; b =
+// band_krows / K keeps a band's panels within a fixed budget, and the slow side is streamed
+// once per band.  (The ragged-K weight gradients keep one sweep: banding them by each
+// expert's K measured 3-4 % slower.)
+// band_krows for a 32 MB band of 256-row panels: bf16 and E4M3 operands
+constexpr int BAND_KROWS_BF16 = (32 << 20) / (256 * 2);
+constexpr int BAND_KROWS_E4M3 = (32 << 20) / 256;
+__device__ __forceinline__ int band_of(const GemmParams& p, int K) {
+  return p.band_krows > 0 ? max(1, p.band_krows / max(K, 1)) : (1 << 30);
+}
+// local tile -> (m, n) inside an mt x nt group; m_fast: M is the fast side
+__device__ __forceinline__ void banded(int local, int mt, int nt, bool m_fast, int band, int& m, int& n) {
+  const int r = m_fast ? mt : nt, l = m_fast ? nt : mt;
+  const int b = band < r ? band : r;
+  const int k = local / (b * l);
+  const int rem = local - k * (b * l);
+  const int w = min(b, r - k * b);  // the last band may be narrower
+  const int fast = k * b + rem % w, slow = rem / w;
+  m = m_fast ? fast : slow;
+  n = m_fast ? slow : fast;
+}
+
 // order: the experts in their visiting order (SCHED_KGROUP, kgroup_order; unused for
 // SCHED_ROWS)
 template <int SCHED, int EPI, bool B_MN, int KB = BK>
@@ -167,8 +194,7 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, const int* 
     const int e = lo;
     const int local = tile - (s_ro[e] / BM) * n_tiles;
     const int mt = (s_ro[e + 1] - s_ro[e]) / BM;
-    if (rows_m_fastest(p.m_fastest, mt, n_tiles)) { c.m = local % mt; c.n = local / mt; }
-    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    banded(local, mt, n_tiles, rows_m_fastest(p.m_fastest, mt, n_tiles), band_of(p, p.K), c.m, c.n);
     c.e = e;
     c.kblocks = p.K / KB;
     c.a_m = s_ro[e] + c.m * BM;

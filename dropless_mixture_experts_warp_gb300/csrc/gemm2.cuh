@@ -66,8 +66,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, const int* s_
     const int e = lo;
     const int local = tile - s_pt[e];
     const int mt2 = ((s_ro[e + 1] - s_ro[e]) / BM + 1) / 2;
-    if (rows_m_fastest(p.m_fastest, mt2, n_tiles)) { c.m = local % mt2; c.n = local / mt2; }
-    else { c.n = local % n_tiles; c.m = local / n_tiles; }
+    banded(local, mt2, n_tiles, rows_m_fastest(p.m_fastest, mt2, n_tiles), band_of(p, p.K), c.m, c.n);
     c.e = e;
     c.kblocks = p.K / KB;
     c.a_m = s_ro[e] + c.m * 2 * BM + rank * BM;

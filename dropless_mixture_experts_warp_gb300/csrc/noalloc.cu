@@ -79,7 +79,7 @@ extern "C" moe_status moe_gemm_down_dgrad_noalloc(const moe_dims* dims, const mo
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.BN = bn; p.N = d.f; p.K = d.d; p.E = d.E; p.row_offsets = row_offsets;
-  p.b_k_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP; p.f = d.f;
+  p.b_k_per_expert = d.d; p.m_fastest = ORDER_PER_GROUP; p.band_krows = BAND_KROWS_BF16; p.f = d.f;
   p.row_limit = R_cap; p.w_rows = w_rows; p.gu_in = gu; p.dgu_out = dgu; p.dw_part = scratch;
   p.dw_stride = n_tiles; p.status = dev_status;
   // the same kernel choice as moe_gemm_down_dgrad, so both give the same bits
