@@ -101,12 +101,12 @@ bool make_tensor_map_fp4(CUtensorMap* m, const void* base, uint64_t inner, uint6
 // SF tiles viewed as [bytes / 256][256] bytes, box of two rows: one 512-byte tile per load
 // (the MXFP8 pair kernel fetches scale tiles by tensor loads so that both CTAs' bytes
 // count on the leader's barrier).
-bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes) {
+bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes, uint32_t box_rows) {
   auto fn = encode_fn();
-  if (!fn || bytes % 512 != 0 || bytes == 0) return false;
+  if (!fn || bytes % (256 * box_rows) != 0 || bytes == 0) return false;
   cuuint64_t dims[2] = {256, bytes / 256};
   cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {256, 2};
+  cuuint32_t box[2] = {256, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -130,10 +130,15 @@ static MxWeights carve_weights(const moe_dims& d, void* base) {
   return w;
 }
 
-// Quantised activations of one step, each along the contraction axis of its GEMM.
+// Quantised activations of one step, each along the contraction axis of its GEMM; after
+// them, the SF tiles of x's and h's column-wise codes again in the replicated form
+// (SF_REP_TILE_BYTES a tile) that the CTA-pair weight gradients read for their B operand.
 struct MxActs {
   MxOp xp_rows, xp_cols, h_rows, h_cols, dy_rows, dy_cols, dgu_rows, dgu_cols;
+  uint8_t* xp_cols_sf_rep;
+  uint8_t* h_cols_sf_rep;
 };
+static size_t sf_rep_bytes(size_t elems) { return a256(elems / 32 * 4); }
 
 static MxActs carve_acts(const moe_dims& d, int64_t R_cap, void* base) {
   uint8_t* p = static_cast<uint8_t*>(base);
@@ -147,6 +152,10 @@ static MxActs carve_acts(const moe_dims& d, int64_t R_cap, void* base) {
   a.dy_cols = carve_op(p, rd);
   a.dgu_rows = carve_op(p, 2 * rf);
   a.dgu_cols = carve_op(p, 2 * rf);
+  a.xp_cols_sf_rep = p;
+  p += sf_rep_bytes(rd);
+  a.h_cols_sf_rep = p;
+  p += sf_rep_bytes(rf);
   return a;
 }
 
@@ -183,7 +192,7 @@ size_t moe_mx_workspace_size(const moe_dims* dims) {
   if (mx_common(dims) != MOE_OK) return 0;
   const size_t R = static_cast<size_t>(moe_row_capacity(dims));
   const size_t rd = R * dims->d, rf = R * dims->f;
-  return 4 * op_bytes(rd) + 2 * op_bytes(rf) + 2 * op_bytes(2 * rf);
+  return 4 * op_bytes(rd) + 2 * op_bytes(rf) + 2 * op_bytes(2 * rf) + sf_rep_bytes(rd) + sf_rep_bytes(rf);
 }
 
 moe_status moe_mx_quantize_weights(const moe_dims* dims, const moe_bf16* w_gu, const moe_bf16* w_d, void* wq,
@@ -226,7 +235,7 @@ moe_status moe_permute_mx(const moe_dims* dims, const moe_bf16* x, const int32_t
     return MOE_ERR_CUDA;
   if (d.T == 0) return MOE_OK;
   return cuda_st(launch_quant_cols_t(x, 1, R_cap, d.d, row_offsets + d.E, a.xp_cols.codes, a.xp_cols.sf, s,
-                                     row_to_token, a.xp_rows.codes, a.xp_rows.sf));
+                                     row_to_token, a.xp_rows.codes, a.xp_rows.sf, false, a.xp_cols_sf_rep));
 }
 
 moe_status moe_combine_bwd_mx(const moe_dims* dims, const moe_bf16* dy, const int32_t* row_to_token,
@@ -264,6 +273,7 @@ moe_status moe_gemm_gate_up_mx(const moe_dims* dims, const int32_t* row_offsets,
   p.gu_out = gu; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
+  p.q_cols_sf_rep = a.h_cols_sf_rep;
   p.q_cols_ld = R_cap; p.q_cols_ktiles = static_cast<int>(R_cap / 128);
   return cuda_st(launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ma, mb, p, static_cast<cudaStream_t>(stream)));
 }
@@ -329,6 +339,7 @@ moe_status moe_gemm_down_wgrad_mx(const moe_dims* dims, const int32_t* row_offse
   const int bn = bn_mx(d.f);
   MxMat ma = mat(a.dy_cols, R_cap, d.d);
   MxMat mb = mat(a.h_cols, R_cap, d.f);
+  mb.sf_rep = a.h_cols_sf_rep;
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.f; p.M = d.d; p.E = d.E; p.row_offsets = row_offsets; p.m_fastest = (d.d <= d.f) ? 1 : 0;
   p.out = dw_d; p.ldo = d.f; p.row_limit = d.d; p.status = dev_status;
@@ -370,6 +381,7 @@ moe_status moe_gemm_gate_up_wgrad_mx(const moe_dims* dims, const int32_t* row_of
   const int bn = bn_mx(d.d);
   MxMat ma = mat(a.dgu_cols, R_cap, 2ll * d.f);
   MxMat mb = mat(a.xp_cols, R_cap, d.d);
+  mb.sf_rep = a.xp_cols_sf_rep;
   GemmParams p = mx_params();
   p.BN = bn; p.N = d.d; p.M = 2 * d.f; p.E = d.E; p.row_offsets = row_offsets;
   p.m_fastest = (2 * d.f <= d.d) ? 1 : 0; p.out = dw_gu; p.ldo = d.d; p.row_limit = 2 * d.f;
@@ -440,6 +452,10 @@ static MxActs carve_shared_acts(const moe_dims& d, void* base) {
   a.dy_cols = carve_op(p, td);
   a.dgu_rows = carve_op(p, 2 * tf);
   a.dgu_cols = carve_op(p, 2 * tf);
+  a.xp_cols_sf_rep = p;
+  p += sf_rep_bytes(td);
+  a.h_cols_sf_rep = p;
+  p += sf_rep_bytes(tf);
   return a;
 }
 
@@ -464,7 +480,7 @@ size_t moe_mx_shared_weights_size(const moe_dims* dims) {
 size_t moe_mx_shared_workspace_size(const moe_dims* dims) {
   if (mx_shared_common(dims) != MOE_OK) return 0;
   const size_t td = static_cast<size_t>(dims->T) * dims->d, tf = static_cast<size_t>(dims->T) * dims->f_shared;
-  return 4 * op_bytes(td) + 2 * op_bytes(tf) + 2 * op_bytes(2 * tf);
+  return 4 * op_bytes(td) + 2 * op_bytes(tf) + 2 * op_bytes(2 * tf) + sf_rep_bytes(td) + sf_rep_bytes(tf);
 }
 
 moe_status moe_mx_quantize_shared_weights(const moe_dims* dims, const moe_bf16* w_gu_s, const moe_bf16* w_d_s,
@@ -501,7 +517,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   GemmParams p;
   // x along d (gate/up GEMM) and along T (its weight gradient, in the backward pass)
   if (launch_quant_cols_t(x, 1, T, d.d, nullptr, a.xp_cols.codes, a.xp_cols.sf, s, nullptr, a.xp_rows.codes,
-                          a.xp_rows.sf) != cudaSuccess)
+                          a.xp_rows.sf, false, a.xp_cols_sf_rep) != cudaSuccess)
     return MOE_ERR_CUDA;
   ma = mat(a.xp_rows, d.d, T);
   mb = mat(w.gu_rows, d.d, 2ll * fs, w4(d));
@@ -511,6 +527,7 @@ moe_status moe_shared_mlp_fwd_mx(const moe_dims* dims, const moe_bf16* x, const 
   p.row_limit = T; p.gu_out = gu_s; p.status = dev_status;
   p.a_sf_ktiles = d.d / 128; p.b_sf_ktiles = d.d / 128;
   p.q_rows = a.h_rows.codes; p.q_rows_sf = a.h_rows.sf; p.q_cols = a.h_cols.codes; p.q_cols_sf = a.h_cols.sf;
+  p.q_cols_sf_rep = a.h_cols_sf_rep;
   p.q_cols_ld = T; p.q_cols_ktiles = T / 128;
   if (launch_gemm_mx(GEMM_ROWS_SWIGLU_FWD_MXQ, ma, mb, p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int bn = bn_mx(d.d);
@@ -564,6 +581,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
   // dW_d_s = dy^T h_s (K = T): dy column codes, h_s column codes from the forward
   ma = mat(a.dy_cols, T, d.d);
   mb = mat(a.h_cols, T, fs);
+  mb.sf_rep = a.h_cols_sf_rep;
   p = mx_params();
   p.BN = bn; p.N = fs; p.M = d.d; p.K = T; p.E = 1; p.m_fastest = (d.d <= fs) ? 1 : 0;
   p.out = dw_d_s; p.ldo = fs; p.row_limit = d.d; p.status = dev_status;
@@ -581,6 +599,7 @@ moe_status moe_shared_mlp_bwd_mx(const moe_dims* dims, const void* wq_s, void* m
   // dW_gu_s = dgu_s^T x (K = T)
   ma = mat(a.dgu_cols, T, 2ll * fs);
   mb = mat(a.xp_cols, T, d.d);
+  mb.sf_rep = a.xp_cols_sf_rep;
   p = mx_params();
   p.BN = bn; p.N = d.d; p.M = 2 * fs; p.K = T; p.E = 1; p.m_fastest = (2 * fs <= d.d) ? 1 : 0;
   p.out = dw_gu_s; p.ldo = d.d; p.row_limit = 2 * fs; p.status = dev_status;

@@ -493,6 +493,12 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
 __device__ __forceinline__ void tc_cp_32x128b_x4_pair(uint32_t taddr, uint64_t s_desc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
+// 128 rows x 256 bits from each CTA's shared memory into TMEM lanes 0..127 (8 columns from
+// `taddr`) of each CTA of the pair; the source is K-major without swizzle: row r's two 16-byte
+// halves at r * 16 (8-row groups `sbo` apart) and `lbo` bytes further.
+__device__ __forceinline__ void tc_cp_128x256b_pair(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
 __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(

@@ -94,7 +94,20 @@ struct GemmParams {
   uint8_t* q_cols_sf;
   long long q_cols_ld;
   int q_cols_ktiles;
+  // the column-wise SF tiles again, each written four times over (SF_REP_TILE_BYTES per tile):
+  // the operand form the CTA-pair weight-gradient kernel reads for B (NULL: not written)
+  uint8_t* q_cols_sf_rep;
+  int sfb_rep;                  // CTA-pair MXFP8 kernel: B's SF tiles are in that replicated form
 };
+
+// A replicated SF tile: the 512-byte tile four times, so that one 128x256b tensor-pipe copy of
+// two of them fills the four TMEM lane quarters with both (see gemm_mx2.cuh).
+constexpr int SF_REP_TILE_BYTES = 4 * 512;
+__device__ __forceinline__ void store_sf_rep(uint8_t* rep, size_t off, uint8_t v) {
+  uint8_t* t = rep + (off >> 9) * SF_REP_TILE_BYTES + (off & 511);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) t[r * 512] = v;
+}
 
 struct TileCoord {
   int e, m, n, kblocks;
@@ -286,7 +299,7 @@ constexpr int XBUF_FLOATS = 32 * 17;
 // 16 codes leave as one 16-byte store.  codes: [cols][ld] (K = rows), scales: SF tiles.
 __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* xb, int lane, uint8_t* codes,
                                                    uint8_t* scales, long long ld, int ktiles, int col0,
-                                                   long long rblk, bool ok) {
+                                                   long long rblk, bool ok, uint8_t* scales_rep = nullptr) {
   const int cc = lane & 15, hh = lane >> 4;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
@@ -317,7 +330,11 @@ __device__ __forceinline__ void quant_cols_chunk32(const float (&v)[32], float* 
     if (ok) {
       *reinterpret_cast<uint4*>(codes + static_cast<long long>(col) * ld + rblk + hh * 16) =
           make_uint4(w[0], w[1], w[2], w[3]);
-      if (hh == 0) scales[sf_byte_offset(col, rblk, ktiles)] = static_cast<uint8_t>(e + 127);
+      if (hh == 0) {
+        const size_t off = sf_byte_offset(col, rblk, ktiles);
+        scales[off] = static_cast<uint8_t>(e + 127);
+        if (scales_rep) store_sf_rep(scales_rep, off, static_cast<uint8_t>(e + 127));
+      }
     }
   }
 }
@@ -427,7 +444,8 @@ __device__ __forceinline__ void fwd_mx_store_chunk(const GemmParams& p, long lon
     qd[1] = make_uint4(q[4], q[5], q[6], q[7]);
     p.q_rows_sf[sf_byte_offset(row, col, p.f / 128)] = static_cast<uint8_t>(sb);
   }
-  quant_cols_chunk32(f.h, xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok);
+  quant_cols_chunk32(f.h, xbuf, lane, p.q_cols, p.q_cols_sf, p.q_cols_ld, p.q_cols_ktiles, col, rblk, blk_ok,
+                     p.q_cols_sf_rep);
 }
 
 // Quantising SwiGLU' epilogue (EPI_SWIGLU_BWD_MX) pieces.  The saved G and U of one

@@ -55,10 +55,13 @@ cudaError_t launch_gemm_mx(GemmKind kind, const MxMat& a, const MxMat& b, GemmPa
     if (!make_tensor_map_store(&tc, p.out, p.N, p.ldo, rows)) return cudaErrorInvalidValue;
   }
   if (pair) {
+    // B's SF tiles in the replicated form where the caller has them (one 2 KB tensor load a
+    // tile, one tensor-pipe copy for both tiles of a 256-row B tile)
+    p.sfb_rep = (b.sf_rep && p.BN == 256) ? 1 : 0;
     CUtensorMap tsa, tsb;
-    if (!make_tensor_map_sf(&tsa, a.sf, a.inner * a.outer / 32) ||
-        !make_tensor_map_sf(&tsb, b.sf, b.inner * b.outer / 32))
-      return cudaErrorInvalidValue;
+    const bool sfb_ok = p.sfb_rep ? make_tensor_map_sf(&tsb, b.sf_rep, 4 * b.inner * b.outer / 32, 8)
+                                  : make_tensor_map_sf(&tsb, b.sf, b.inner * b.outer / 32);
+    if (!make_tensor_map_sf(&tsa, a.sf, a.inner * a.outer / 32) || !sfb_ok) return cudaErrorInvalidValue;
     return launch_gemm_mx_pair(kind, ta, tb, tsa, tsb, tc, p, stream);
   }
   switch (kind) {

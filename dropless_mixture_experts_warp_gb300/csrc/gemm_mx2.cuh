@@ -15,7 +15,12 @@
 // and tensor stores.  Block scales: each CTA fetches, by tensor loads counted on the
 // leader's barrier, the SF tile of its own 128 A rows and the SF tiles of all BN rows of
 // B; the leader's pair copies (tcgen05.cp.cta_group::2) move each CTA's tiles into its own
-// TMEM.  TMEM holds one 256-column accumulator (two of 128 at BN = 128) in columns
+// TMEM.  A copy's cost is per instruction, not per byte, and a third copy a stage cost this
+// mainloop ~16 % (dense timing variants: 2.5 PFLOP/s with three, 2.9-3.2 with two or one, the
+// same with one 4 KB 128x256b copy in place of two 32x128b.warpx4).  So where the producers of
+// B left its SF tiles also in a replicated form (each 512-byte tile four times over: the weight
+// gradients' B, x's and h's column-wise codes), both of a 256-row B tile's SF tiles arrive by
+// two 2 KB tensor loads and go into all four TMEM lane quarters by one 128x256b copy.  TMEM holds one 256-column accumulator (two of 128 at BN = 128) in columns
 // 0..255 and the scale factors of each stage from column 256 on.  B may be E2M1 (FP4
 // weights) as in the single-CTA kernel.
 #pragma once
@@ -27,8 +32,10 @@ namespace moe {
 
 constexpr int MXP_A_BYTES = BM * MX_BK;                       // 16 KB
 constexpr int MXP_STAGE_BYTES = MXP_A_BYTES + 128 * MX_BK;    // + half of a 256-row B tile
-constexpr int MXP_STAGES = 6;
-constexpr int MXP_SF_STAGE = 1536;                            // SFA 512 B, SFB up to 1 KB
+constexpr int MXP_STAGES = 5;
+// SF tiles of a stage: SFA (512 B), then SFB: with p.sfb_rep each of B's two 128-row tiles in
+// its replicated form (2 KB), else up to two plain tiles.
+constexpr int MXP_SF_STAGE = 512 + 2 * SF_REP_TILE_BYTES;
 constexpr int MXP_SF_OFF = MXP_STAGES * MXP_STAGE_BYTES;
 constexpr int MXP_EPI_OFF = MXP_SF_OFF + MXP_STAGES * MXP_SF_STAGE;
 constexpr int MXP_EPI_WARPS = 8;
@@ -103,12 +110,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MXP_THREADS, 1)
   const int total = (SCHED == SCHED_ROWS) ? s_pt[E] : E * (p.M / (2 * BM)) * n_tiles;
   volatile int* abort_flag = &s_abort;
   const int n_sfb = BN / 128;  // SF tiles of the BN rows of B
+  const bool sfb_rep = p.sfb_rep != 0 && n_sfb == 2;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const uint32_t b_row_tx = p.b_fmt == MX_FMT_E2M1 ? MX_W4_TX_ROW_BYTES : MX_BK;
-      const uint32_t cta_tx = MXP_A_BYTES + (BN / 2) * b_row_tx + 512 + n_sfb * 512;
+      const uint32_t cta_tx = MXP_A_BYTES + (BN / 2) * b_row_tx + 512 + n_sfb * (sfb_rep ? SF_REP_TILE_BYTES : 512);
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
@@ -135,8 +143,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MXP_THREADS, 1)
           tma_load_2d_pair(sb, &tmB, bar, kbb, c.b_n);
           // SF tile (r / 128, k / 128) is rows 2t, 2t + 1 of the [bytes / 256][256] view
           tma_load_2d_pair(sf, &tmSFA, bar, 0, 2 * ((c.a_m / 128) * p.a_sf_ktiles + ka / MX_BK));
-          for (int i = 0; i < n_sfb; ++i)
-            tma_load_2d_pair(sf + 512 + 512 * i, &tmSFB, bar, 0, 2 * ((b0 / 128 + i) * p.b_sf_ktiles + kbb / MX_BK));
+          // SF tile (r / 128, k / 128) is rows 2t, 2t + 1 (replicated: rows 8t .. 8t + 7) of its view
+          for (int i = 0; i < n_sfb; ++i) {
+            const int t_sf = (b0 / 128 + i) * p.b_sf_ktiles + kbb / MX_BK;
+            if (sfb_rep) tma_load_2d_pair(sf + 512 + SF_REP_TILE_BYTES * i, &tmSFB, bar, 0, 8 * t_sf);
+            else tma_load_2d_pair(sf + 512 + 512 * i, &tmSFB, bar, 0, 2 * t_sf);
+          }
           if (++stage == MXP_STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -168,8 +180,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MXP_THREADS, 1)
           const uint32_t sfb_t = sfa_t + 4;
           // scale tiles: 32 rows x 16 B each, 8-row core matrices 128 B apart
           tc_cp_32x128b_x4_pair(sfa_t, smem_desc_plain(sf, 0, 128));
-          for (int i = 0; i < n_sfb; ++i)
-            tc_cp_32x128b_x4_pair(sfb_t + 4 * i, smem_desc_plain(sf + 512 + 512 * i, 0, 128));
+          if (sfb_rep)  // row r of both tiles: 16 bytes at sf + 512 + 16 r and 2048 bytes on
+            tc_cp_128x256b_pair(sfb_t, smem_desc_plain(sf + 512, SF_REP_TILE_BYTES, 128));
+          else
+            for (int i = 0; i < n_sfb; ++i)
+              tc_cp_32x128b_x4_pair(sfb_t + 4 * i, smem_desc_plain(sf + 512 + 512 * i, 0, 128));
 #pragma unroll
           for (int kk = 0; kk < MX_BK / 32; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);

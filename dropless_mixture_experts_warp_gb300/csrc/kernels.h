@@ -107,6 +107,7 @@ struct MxMat {
   const uint8_t* sf;
   uint64_t inner, outer;
   bool fp4;
+  const uint8_t* sf_rep = nullptr;  // the SF tiles each four times over (SF_REP_TILE_BYTES), or NULL
 };
 // MXFP8 grouped GEMM; kind is one of GEMM_ROWS_STORE, GEMM_KGROUP_STORE,
 // GEMM_ROWS_SWIGLU_FWD_MXQ, GEMM_ROWS_SWIGLU_BWD_MXQ.  p.sfa/p.sfb are taken from a
@@ -125,15 +126,16 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
                               uint8_t* codes, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map = nullptr,
-                                uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr, bool fp4 = false);
+                                uint8_t* codes_rows = nullptr, uint8_t* sf_rows = nullptr, bool fp4 = false,
+                                uint8_t* sf_rep = nullptr);
 RouteScratch route_scratch(const moe_dims& d, void* ws);
 float* workspace_dw_part(const moe_dims& d, void* ws);
+bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes, uint32_t box_rows = 2);
 bool make_tensor_map_store(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ld, uint64_t rows);
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                           uint32_t box_inner, uint32_t box_outer);
 bool make_tensor_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer);
-bool make_tensor_map_sf(CUtensorMap* m, const void* base, uint64_t bytes);
 // Packed 4-bit codes [outer][inner / 2] bytes loaded as 16-element groups padded to 16
 // bytes in shared memory (the layout the block-scaled MMA reads for E2M1 under
 // kind::mxf8f6f4), 128B swizzle; box_inner must be 128 elements.

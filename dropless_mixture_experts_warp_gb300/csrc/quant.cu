@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                            const int32_t* __restrict__ row_map,
                                                            uint8_t* __restrict__ codes_rows,
-                                                           uint8_t* __restrict__ sf_rows) {
+                                                           uint8_t* __restrict__ sf_rows,
+                                                           uint8_t* __restrict__ sf_rep) {
   extern __shared__ __align__(16) uint8_t qsm[];
   uint8_t* ct = qsm + 2 * QC_IN_BYTES;  // column-wise codes [128 cols][QC_LD]
   uint8_t* rt = ct + 128 * QC_LD;       // row-wise codes [128 rows][QC_LD]
@@ -246,8 +247,12 @@ __global__ void __launch_bounds__(256) quant_cols_t_kernel(const uint16_t* __res
           *reinterpret_cast<const uint4*>(ct + line * QC_LD + q * 16);
     }
     if (threadIdx.x < 32) {
-      uint8_t* sfb = sf + b * (static_cast<long long>(C) * rows / 32) + ((c0 / 128) * k_tiles + r0 / 128) * 512;
-      reinterpret_cast<uint4*>(sfb)[threadIdx.x] = reinterpret_cast<const uint4*>(sft)[threadIdx.x];
+      const long long tile_sf = b * (static_cast<long long>(C) * rows / 32 / 512) + (c0 / 128) * k_tiles + r0 / 128;
+      const uint4 v = reinterpret_cast<const uint4*>(sft)[threadIdx.x];
+      reinterpret_cast<uint4*>(sf + tile_sf * 512)[threadIdx.x] = v;
+      if (sf_rep)  // the same tile four times over (the CTA-pair weight gradients' B form)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) reinterpret_cast<uint4*>(sf_rep + tile_sf * 2048 + r * 512)[threadIdx.x] = v;
     }
     if (codes_rows) {
       const long long grow0 = b * rows + r0;
@@ -333,7 +338,7 @@ cudaError_t launch_quant_rows(const void* src, long long rows, int C, long long 
 
 cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int C, const int32_t* nrows_dev,
                                 uint8_t* codes, uint8_t* sf, cudaStream_t stream, const int32_t* row_map,
-                                uint8_t* codes_rows, uint8_t* sf_rows, bool fp4) {
+                                uint8_t* codes_rows, uint8_t* sf_rows, bool fp4, uint8_t* sf_rep) {
   if (rows == 0 || batch == 0) return cudaSuccess;  // callers pass rows % 128 == 0, C % 128 == 0
   auto kern = fp4 ? quant_cols_t_kernel<true> : quant_cols_t_kernel<false>;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
@@ -342,7 +347,7 @@ cudaError_t launch_quant_cols_t(const void* src, int batch, long long rows, int 
   if (tiles >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernel indexes tiles in 32 bits
   const int grid = static_cast<int>(tiles < 2ll * num_sms() ? tiles : 2ll * num_sms());  // two blocks per SM
   kern<<<grid, 256, QC_SMEM, stream>>>(static_cast<const uint16_t*>(src), batch, rows, C, nrows_dev, codes, sf,
-                                       row_map, codes_rows, sf_rows);
+                                       row_map, codes_rows, sf_rows, sf_rep);
   count_launch();
   return cudaGetLastError();
 }
